@@ -1,0 +1,406 @@
+"""CPU oracle of the per-token sparse-MLP decode path, in float64.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+benchmark's CPU-baseline / reference leg may import this module; the product
+path (the C-ABI library and its Python binding) never calls it and shares no
+code with it.  Inputs come from the seeded generators in `workloads`.
+
+Every step is written out plainly, in the order the pages give:
+
+* dense prefix, predictor after layer 0, active set from centroid masks, set
+  difference against the resident rows, slot map update, staged records copied
+  into the three projection buffers, sparse FFN over the resident active rows
+  (NeuroPrefetcher: Storage-Aware Sparse LLM Inference via Delta Prefetching,
+  sections "System Overview", "Shared Activation Predictor", "Predictive Delta
+  Prefetching", "I/O Path"; full-text HTML: Figure 2 execution flow, delta
+  runtime, slot map, neuron-centric layout, launch_deinterleave_scatter);
+* the window residency and up|down bundling variant (LLM in a flash: Efficient
+  Large Language Model Inference with Limited Memory, sections 3.1 "Reducing
+  Data Transfer" and 3.2 "Increasing Transfer Throughput").
+
+Readings where the pages are silent or disagree (each also listed in the
+design notes):
+
+* the combine operator is a parameter: the pages intersect gate and up masks,
+  the measured configuration takes their union;
+* K_max is a cap: when the combined set is larger, the K_max lowest neuron IDs
+  are kept;
+* the lost set-difference formula is D_in = A_t minus R_{t-1} and
+  D_out = R_{t-1} minus R_t (R = resident set);
+* freed slots are handed out in ascending slot order to incoming neurons in
+  ascending ID order;
+* activation h_n = relu(g_n . x) * (u_n . x) (ReLU-fied Llama), or
+  relu(u_n . x) without a gate (OPT);
+* the rest of the transformer block is replaced by a residual stream
+  h <- h + y with a weightless RMSNorm (eps 1e-6) in front of every FFN and of
+  the predictor;
+* argmax ties go to the lowest centroid index; the per-layer predictor fires
+  when its logit is strictly positive (sigmoid > 0.5);
+* batched decoding rounds the normalised input to bf16 before every dot
+  product (the GPU's tensor-core operands) and takes the union of the
+  sequences' active sets.
+
+Functions without an external pin say so in their docstring ("parity
+unpinned"); all others are pinned by the CPU tests against closed forms, brute
+force and the pages' printed numbers.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+RMS_EPS = 1e-6
+
+
+# ---------------------------------------------------------------------------
+# Elementary steps
+# ---------------------------------------------------------------------------
+def f64(a) -> np.ndarray:
+    """Widen a torch tensor / numpy array exactly to float64 on the CPU."""
+    if isinstance(a, torch.Tensor):
+        return a.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bf16 (ties to even), via torch."""
+    return torch.from_numpy(np.asarray(x, dtype=np.float64)).to(torch.float32) \
+        .to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def rmsnorm(h: np.ndarray) -> np.ndarray:
+    """x_hat = h / sqrt(mean(h^2) + eps).  Stand-in for the norm in front of
+    each MLP; the pages keep normalisation parameters resident but give no
+    formula (reading)."""
+    h = np.asarray(h, dtype=np.float64)
+    return h / np.sqrt(np.mean(h * h) + RMS_EPS)
+
+
+def ffn_rows(gate: np.ndarray | None, up: np.ndarray, down_t: np.ndarray,
+             xhat: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """FFN over an explicit list of neurons.
+
+    gate, up, down_t: [n, D] rows (row n of the gate, up and down^T
+    projections of neuron n: NeuroPrefetcher full text, delta runtime: "for
+    each active neuron i, the runtime uses row i of the gate, up, and down^T
+    projections").  Returns (y[D], h[n]) with
+        h_n = relu(gate_n . x) * (up_n . x)   (ReLU-fied Llama)
+        h_n = relu(up_n . x)                   (no gate: OPT)
+        y   = sum_n h_n * down_t_n.
+    """
+    b = up @ xhat
+    if gate is None:
+        hn = np.maximum(b, 0.0)
+    else:
+        a = gate @ xhat
+        hn = np.where(a > 0.0, a, 0.0) * b
+    y = down_t.T @ hn
+    return y, hn
+
+
+def predictor_logits(w1: np.ndarray, w2: np.ndarray, b2: np.ndarray | None,
+                     xhat: np.ndarray) -> np.ndarray:
+    """z = relu(W1 x); logits = W2 z (+ b2).  The pages' predictor (feature
+    projection, residual trunk, 2x31 linear heads: NeuroPrefetcher "Shared
+    Activation Predictor") is reduced to one hidden layer; the per-layer
+    low-rank predictor of LLM in a flash ("Reducing Data Transfer") has the
+    same form plus an output bias."""
+    z = np.maximum(w1 @ xhat, 0.0)
+    out = w2 @ z
+    if b2 is not None:
+        out = out + b2
+    return out
+
+
+def head_argmax(logits: np.ndarray, n_heads: int, n_centroids: int) -> np.ndarray:
+    """Per head, the centroid with the highest logit; ties go to the lowest
+    index ("selecting the highest-probability centroid for each layer",
+    NeuroPrefetcher "Shared Activation Predictor")."""
+    return np.argmax(logits.reshape(n_heads, n_centroids), axis=1).astype(np.int64)
+
+
+def head_index(layer: int, proj: int) -> int:
+    """Head of absolute layer `layer` >= 1; proj 0 = gate, 1 = up.  The
+    predictor emits 2 x (L-1) IDs: one gate and one up centroid for each of
+    layers 1..L-1 (NeuroPrefetcher full text: 2 x 31 = 62 for 32 layers)."""
+    return 2 * (layer - 1) + proj
+
+
+def mask_ids(words: np.ndarray, d_ff: int) -> list[int]:
+    """Neuron IDs set in a packed mask (bit n lives in word n//32, bit n%32)."""
+    bits = np.unpackbits(np.asarray(words, dtype="<u4").view(np.uint8),
+                         bitorder="little")[:d_ff]
+    return [int(n) for n in np.flatnonzero(bits)]
+
+
+def combine_sets(gate_ids: list[int], up_ids: list[int], mode: str) -> list[int]:
+    """A = gate mask (intersect | union) up mask, sorted ascending
+    (NeuroPrefetcher "Predictive Delta Prefetching": gate and up centroid masks
+    are intersected; the measured configuration uses the union)."""
+    g, u = set(gate_ids), set(up_ids)
+    if mode == "intersect":
+        return sorted(g & u)
+    if mode == "union":
+        return sorted(g | u)
+    raise ValueError(mode)
+
+
+def cap_set(active: list[int], k_max: int) -> tuple[list[int], int]:
+    """Keep the k_max lowest IDs ("K_max, the maximum number of active
+    intermediate neurons kept per sparse layer", NeuroPrefetcher full text,
+    evaluation budgets).  Returns (kept, number dropped)."""
+    active = sorted(active)
+    if len(active) <= k_max:
+        return active, 0
+    return active[:k_max], len(active) - k_max
+
+
+def set_delta(active: list[int], resident_prev: list[int],
+              resident_next: list[int]) -> tuple[list[int], list[int]]:
+    """D_in = A_t minus R_{t-1}; D_out = R_{t-1} minus R_t (the set difference
+    of NeuroPrefetcher's delta runtime; with the slot-map policy R_t = A_t)."""
+    a, rp, rn = set(active), set(resident_prev), set(resident_next)
+    return sorted(a - rp), sorted(rp - rn)
+
+
+def assign_slots(slotmap: np.ndarray, inv: np.ndarray, d_in: list[int],
+                 d_out: list[int], k_max: int) -> list[tuple[int, int]]:
+    """Release the slots of D_out and give free slots to D_in, in place.
+
+    Per-layer slot map S[n] = slot of neuron n or -1 (NeuroPrefetcher full
+    text, delta runtime: "clears slot-map entries for outgoing rows, assigns
+    freed slots to incoming rows").  Reading: the i-th incoming neuron in
+    ascending ID order takes the i-th free slot in ascending slot order.
+    Returns the (neuron, slot) pairs of D_in."""
+    for n in d_out:
+        s = int(slotmap[n])
+        assert s >= 0
+        slotmap[n] = -1
+        inv[s] = -1
+    free = [s for s in range(k_max) if inv[s] < 0]
+    assert len(free) >= len(d_in), "resident set larger than K_max"
+    pairs = list(zip(d_in, free[:len(d_in)]))
+    for n, s in pairs:
+        slotmap[n] = s
+        inv[s] = n
+    return pairs
+
+
+def window_resident(resident_prev: list[int], active: list[int], last_seen: dict,
+                    t: int, window: int, k_max: int) -> list[int]:
+    """Resident set after token t under windowing: the neurons active in the
+    last `window` tokens (this one included) that were resident or are active
+    now (LLM in a flash, 3.1 "Windowing retains weights predicted to be active
+    for recent tokens").  If more than k_max remain, the ones whose last use is
+    oldest go first, ties by ascending ID; neurons active now never go
+    (reading: the pages give no cap rule).  `last_seen` must already hold t
+    for the active neurons."""
+    cand = (set(resident_prev) | set(active))
+    cand = {n for n in cand if t - last_seen[n] < window}
+    if len(cand) > k_max:
+        act = set(active)
+        order = sorted((n for n in cand if n not in act), key=lambda n: (last_seen[n], n))
+        for n in order[:len(cand) - k_max]:
+            cand.discard(n)
+    return sorted(cand)
+
+
+# ---------------------------------------------------------------------------
+# Whole-token decode
+# ---------------------------------------------------------------------------
+@dataclass
+class TokenRecord:
+    """Everything the oracle computed for one token (per sparse layer lists are
+    indexed by s = layer - n_dense)."""
+    logits: list = field(default_factory=list)      # per sequence: fp64 logits
+    ids: list = field(default_factory=list)         # per sequence: int64[heads]
+    active: list = field(default_factory=list)      # per layer: sorted IDs
+    overflow: list = field(default_factory=list)    # per layer: dropped by the cap
+    d_in: list = field(default_factory=list)        # per layer: [(neuron, slot)]
+    d_out: list = field(default_factory=list)       # per layer: sorted IDs
+    y: list = field(default_factory=list)           # per layer: [B][D] fp64
+    pred_logits_layer: list = field(default_factory=list)  # per-layer predictor
+    h: np.ndarray | None = None                     # [B][D] after the last layer
+
+
+class OracleDecoder:
+    """Decode state (slot maps, resident buffers) plus the per-token step."""
+
+    def __init__(self, wl, materialize_buffers: bool = True):
+        cfg = self.cfg = wl.cfg
+        self.wl = wl
+        S, F, K, D = cfg.n_sparse, cfg.d_ff, cfg.k_max, cfg.d_model
+        self.slotmap = np.full((S, F), -1, dtype=np.int64)
+        self.inv = np.full((S, K), -1, dtype=np.int64)
+        self.resident = [[] for _ in range(S)]
+        self.last_seen = [dict() for _ in range(S)]
+        self.t = 0
+        self.materialize = materialize_buffers
+        # Projection buffers start zeroed; storage dtype kept (exact copies).
+        self.bufs = (torch.zeros((S, cfg.n_proj, K, D), dtype=wl.store.dtype)
+                     if materialize_buffers else None)
+        self._w1 = self._w2 = self._b2 = None
+
+    # -- weights, widened on demand --------------------------------------
+    def _pred(self, layer: int | None = None):
+        wl = self.wl
+        if layer is None:
+            if self._w1 is None:
+                self._w1, self._w2 = f64(wl.pred_w1), f64(wl.pred_w2)
+            return self._w1, self._w2, None
+        return f64(wl.pred_w1[layer]), f64(wl.pred_w2[layer]), f64(wl.pred_b2[layer])
+
+    def _dense_rows(self, layer: int):
+        w = f64(self.wl.dense_w[layer])
+        return w[0], w[1], w[2]
+
+    def _sparse_rows(self, s: int, ids: list[int]):
+        """Rows of the active neurons, read through the slot map from the
+        resident buffers (or from the store when buffers are not kept)."""
+        cfg = self.cfg
+        if self.materialize:
+            slots = [int(self.slotmap[s][n]) for n in ids]
+            assert all(x >= 0 for x in slots), "active neuron not resident"
+            rec = f64(self.bufs[s][:, slots, :])          # [n_proj][n][D]
+        else:
+            rec = f64(self.wl.store[s][ids]).transpose(1, 0, 2)
+        if cfg.has_gate:
+            return rec[0], rec[1], rec[2]
+        return None, rec[0], rec[1]
+
+    def reset(self):
+        """Cold start: the next token loads its full predicted set."""
+        self.__init__(self.wl, self.materialize)
+
+    # -- the step ----------------------------------------------------------
+    def step(self, x: np.ndarray, ids_override=None, fire_override=None) -> TokenRecord:
+        """Decode one token (all sequences of the batch).
+
+        x: [B][D] token inputs (the residual stream entering layer 0).
+        ids_override: per sequence int[heads] to use instead of the oracle's
+            own argmax (staged parity near fp32 ties).
+        fire_override: per sparse layer, bool[F] firing decisions to use
+            instead of logit > 0 (per-layer predictor, staged parity)."""
+        cfg, wl = self.cfg, self.wl
+        B = cfg.batch
+        rnd = round_bf16 if B > 1 else (lambda v: v)
+        h = f64(x).reshape(B, cfg.d_model).copy()
+        rec = TokenRecord()
+        # Dense prefix (NeuroPrefetcher "System Overview": the first d layers
+        # keep their MLP fully resident).
+        for layer in range(cfg.n_dense):
+            g, u, dt = self._dense_rows(layer)
+            for b in range(B):
+                y, _ = ffn_rows(g, u, dt, rnd(rmsnorm(h[b])))
+                h[b] += y
+            if layer == 0:
+                self._predict_shared(h, rec, ids_override)
+        if cfg.n_dense == 0 and cfg.pred_kind == "shared_argmax":
+            self._predict_shared(h, rec, ids_override)
+        # Sparse suffix.
+        for s in range(cfg.n_sparse):
+            layer = cfg.n_dense + s
+            if cfg.pred_kind == "shared_argmax":
+                active = self._active_from_ids(s, layer, rec.ids)
+            else:
+                w1, w2, b2 = self._pred(layer)
+                xs = rmsnorm(h[0])
+                lg = predictor_logits(w1, w2, b2, xs)
+                rec.pred_logits_layer.append(lg)
+                fire = (lg > 0.0) if fire_override is None else np.asarray(fire_override[s])
+                active = [int(n) for n in np.flatnonzero(fire)]
+            active, dropped = cap_set(active, cfg.k_max)
+            rec.active.append(active)
+            rec.overflow.append(dropped)
+            # Residency and delta.
+            prev = self.resident[s]
+            if cfg.residency == "window":
+                for n in active:
+                    self.last_seen[s][n] = self.t
+                nxt = window_resident(prev, active, self.last_seen[s], self.t,
+                                      cfg.window, cfg.k_max)
+            else:
+                nxt = active
+            d_in, d_out = set_delta(active, prev, nxt)
+            pairs = assign_slots(self.slotmap[s], self.inv[s], d_in, d_out, cfg.k_max)
+            self.resident[s] = nxt
+            rec.d_in.append(pairs)
+            rec.d_out.append(d_out)
+            # Scatter: each staged record's rows go to the slot the delta
+            # runtime assigned (NeuroPrefetcher "I/O Path",
+            # launch_deinterleave_scatter).
+            if self.materialize:
+                for n, slot in pairs:
+                    for p in range(cfg.n_proj):
+                        self.bufs[s, p, slot] = wl.store[s, n, p]
+            # Sparse FFN over the resident active rows.
+            g, u, dt = self._sparse_rows(s, active)
+            ys = np.zeros((B, cfg.d_model))
+            for b in range(B):
+                ys[b], _ = ffn_rows(g, u, dt, rnd(rmsnorm(h[b])))
+                h[b] += ys[b]
+            rec.y.append(ys)
+        rec.h = h
+        self.t += 1
+        return rec
+
+    def _predict_shared(self, h, rec, ids_override):
+        cfg = self.cfg
+        w1, w2, _ = self._pred()
+        rnd = round_bf16 if cfg.batch > 1 else (lambda v: v)
+        for b in range(cfg.batch):
+            lg = predictor_logits(w1, w2, None, rnd(rmsnorm(h[b])))
+            rec.logits.append(lg)
+            ids = head_argmax(lg, cfg.n_heads, cfg.n_centroids)
+            if ids_override is not None:
+                ids = np.asarray(ids_override[b], dtype=np.int64)
+            rec.ids.append(ids)
+
+    def _active_from_ids(self, s: int, layer: int, ids_per_seq) -> list[int]:
+        cfg, wl = self.cfg, self.wl
+        out: set[int] = set()
+        for ids in ids_per_seq:
+            g = mask_ids(wl.centroids[s, 0, ids[head_index(layer, 0)]], cfg.d_ff)
+            u = mask_ids(wl.centroids[s, 1, ids[head_index(layer, 1)]], cfg.d_ff)
+            out |= set(combine_sets(g, u, cfg.combine))
+        return sorted(out)
+
+
+# ---------------------------------------------------------------------------
+# Accounting (bytes the method must move)
+# ---------------------------------------------------------------------------
+def record_bytes(d_model: int, elem_bytes: int, n_proj: int = 3) -> int:
+    """One neuron-centric record: gate | up | down^T rows of d_model elements
+    (NeuroPrefetcher "I/O Path"), or up | down^T with row-column bundling
+    (LLM in a flash 3.2: 2 d_model num_bytes)."""
+    return n_proj * d_model * elem_bytes
+
+
+def h2d_bytes(rec: TokenRecord, d_model: int, elem_bytes: int, n_proj: int) -> int:
+    """Bytes read from the storage tier for one token: |D_in| records."""
+    return sum(len(p) for p in rec.d_in) * record_bytes(d_model, elem_bytes, n_proj)
+
+
+def rel_l2(got, ref) -> float:
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    den = np.linalg.norm(ref)
+    num = np.linalg.norm(got - ref)
+    return float(num / den) if den > 0 else float(num)
+
+
+def fp32_dot_bound(w: np.ndarray, v: np.ndarray, v_rel_err: float) -> np.ndarray:
+    """Bound on |fp32 result - exact| for rows of w . v with fp32 accumulation
+    over k terms (error <= k * 2^-24 * sum |w_i v_i|, doubled for safety) plus
+    the propagated relative error of the input vector."""
+    k = w.shape[-1]
+    mag = np.abs(w) @ np.abs(v)
+    return mag * (2.0 * k * 2.0 ** -24 + v_rel_err)
+
+
+def argmax_tolerance(w1, w2, xhat, x_rel_err: float = 1e-5) -> np.ndarray:
+    """Per-logit error bound of an fp32 predictor evaluation."""
+    z = np.maximum(w1 @ xhat, 0.0)
+    z_err = fp32_dot_bound(w1, xhat, x_rel_err)
+    return fp32_dot_bound(w2, z, 0.0) + np.abs(w2) @ z_err
