@@ -1,0 +1,348 @@
+#!/usr/bin/env python
+"""Decode benchmark: sparse-MLP decode tokens/s on the Llama-2-7B ReLU shape
+(32 layers, dense layer 0, d_model 4096, d_ff 11008, fp16, K_max 2048, 1024
+centroids per projection at 10% density, persistence 0.83, gate|up union),
+with per-kernel GB/s against the measured GB300 HBM and host-link peaks.
+
+One step = one decoded token through the whole path: dense layer 0,
+predictor, active sets + delta + slot assignment, host-link gather and
+deinterleave-scatter of the incoming rows, 31 sparse FFNs.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl cuda|reference]
+
+Under torchrun each rank decodes its own independent sequence (replicas: the
+path has no exchange step); value = tokens of all ranks / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLP decode tok/s + delta-scatter GB/s, % of GB300 HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
+# keyed by kernel source file; valid only while that file is unchanged.
+NCU_TRAFFIC = {}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=256)
+    p.add_argument("--warmup", type=int, default=128)
+    p.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    p.add_argument("--config", default="llama2-7b-relu")
+    p.add_argument("--h2d-mode", default="staged", choices=["staged", "fused"])
+    p.add_argument("--cpu-sample-tokens", type=int, default=3)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def h2d_peak_gbs(torch):
+    """Best contiguous pinned-host -> device copy bandwidth (GB/s)."""
+    n = 1 << 30
+    src = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(n, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(4):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best = max(best, n / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del src, dst
+    return best
+
+
+def file_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def kernel_table(prof, peaks, h2d_peak):
+    """Per kind: launches, time, algorithmic GB/s and fraction of its peak."""
+    out = {}
+    for kind, d in prof.items():
+        if d["launches"] == 0:
+            continue
+        ms = d["ms"]
+        gbs = d["bytes"] / (ms * 1e-3) / 1e9 if ms > 0 and d["bytes"] > 0 else None
+        bound = "host_link" if kind == "gather" else "hbm"
+        peak = h2d_peak if bound == "host_link" else peaks["hbm_gbs"]
+        out[kind] = {"launches": d["launches"], "ms_total": round(ms, 4),
+                     "us_per_launch": round(1e3 * ms / d["launches"], 3),
+                     "bytes_per_launch": d["bytes"] // d["launches"] if d["bytes"] else 0,
+                     "gbs": round(gbs, 1) if gbs else None, "bound": bound,
+                     "frac": round(gbs / peak, 4) if gbs else None}
+    return out
+
+
+def run_cuda(args):
+    import torch
+    import torch.distributed as dist
+    from sparse_activation_decode_gb300 import decoder_for
+    from sparse_activation_decode_gb300.build import build
+    from workloads import CONFIGS, make_workload
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        build()
+    if world > 1:
+        dist.barrier()
+    build()
+    peaks = load_peaks()
+    W, K = args.warmup, args.steps
+    base = CONFIGS[args.config]
+    T = min(W + 3 * K, base.n_centroids - 24 if base.n_centroids else 10 ** 9)
+    cfg = base.replace(n_warm=0, n_decode=T, seed=base.seed + 7919 * rank)
+    t0 = time.time()
+    wl = make_workload(cfg, device="cuda")
+    gen_s = time.time() - t0
+    dec = decoder_for(wl, h2d_mode=args.h2d_mode)
+    xs = wl.x.to("cuda")                                  # [T][B][D], resident before timing
+
+    def tok(i):
+        return xs[i % T].clone()
+
+    h2d_peak = h2d_peak_gbs(torch) if rank == 0 else None
+    # warm-up (includes the cold start)
+    for i in range(W):
+        dec.decode_token(tok(i))
+    torch.cuda.synchronize()
+    hs = [tok(W + k) for k in range(K)]
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    main = dec.main_stream
+    n0 = dec.launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(main)
+        for k in range(K):
+            dec.decode_token(hs[k])
+        ev1.record(main)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    launches = dec.launch_count() - n0
+    ms_t = torch.tensor([ms], device="cuda")
+    if world > 1:
+        dist.barrier()
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = world * K / (ms_max * 1e-3)
+
+    # live per-kernel durations (events on each kernel's own stream)
+    dec.profile()
+    dec.set_profiling(True)
+    hs2 = [tok(W + K + k) for k in range(K)]
+    for k in range(K):
+        dec.decode_token(hs2[k])
+    prof = dec.profile()
+    dec.set_profiling(False)
+    table = kernel_table(prof, peaks, h2d_peak or 0.0)
+
+    # end to end through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        D, B = cfg.d_model, cfg.batch
+        hin = torch.stack([xs[(W + 2 * K + k) % T] for k in range(K)]).cpu().pin_memory()
+        hout = torch.empty_like(hin).pin_memory()
+        hdev = torch.empty((B, D), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        ev0.record(main)
+        for k in range(K):
+            hdev.copy_(hin[k], non_blocking=True)
+            dec.decode_token(hdev)
+            hout[k].copy_(hdev, non_blocking=True)
+        ev1.record(main)
+        torch.cuda.synchronize()
+        ms_e = ev0.elapsed_time(ev1)
+        e2e = {"value": round(world * K / (ms_e * 1e-3), 2), "unit": "tok/s",
+               "h2d_bytes_per_step": B * D * 4, "d2h_bytes_per_step": B * D * 4}
+    dec.close()
+
+    if rank != 0:
+        return None
+    dom = max(((k, v) for k, v in table.items() if k != "finish"), key=lambda kv: kv[1]["ms_total"])
+    dk, dv = dom
+    src = {"gather": "np_scatter.cu", "scatter": "np_scatter.cu", "ffn": "np_ffn.cu", "dense": "np_ffn.cu",
+           "predictor": "np_pred.cu", "set": "np_set.cu"}.get(dk)
+    traffic = None
+    ent = NCU_TRAFFIC.get((dk, cfg.name))
+    if ent and src and ent["src_hash"] == file_hash(os.path.join(ROOT, "sparse_activation_decode_gb300",
+                                                                 "csrc", src)):
+        traffic = ent["bytes_per_launch"]
+    peak = h2d_peak if dv["bound"] == "host_link" else peaks["hbm_gbs"]
+    roofline = {"kernel": dk, "bound": dv["bound"], "achieved": dv["gbs"], "peak": round(peak, 1),
+                "unit": "GB/s", "frac": dv["frac"], "traffic": traffic,
+                "peak_source": "measured live: pinned host->device copy" if dv["bound"] == "host_link"
+                else f"MEASURED_PEAKS.json hbm_gbs ({peaks['source']})"}
+    hbm_kernels = {k: {"gbs": table[k]["gbs"], "frac_of_measured_hbm": table[k]["frac"],
+                       "frac_of_nominal_8tbs": round(table[k]["gbs"] / 8000.0, 4) if table[k]["gbs"] else None}
+                   for k in ("ffn", "scatter", "dense", "predictor") if k in table}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 weights, f32 accumulate", "data": "synthetic (seeded; shapes of the pages' workloads)",
+        "config": {"workload": cfg.name, "layers": cfg.n_layers, "dense_prefix": cfg.n_dense,
+                   "d_model": cfg.d_model, "d_ff": cfg.d_ff, "k_max": cfg.k_max, "centroids": cfg.n_centroids,
+                   "combine": cfg.combine, "persistence": cfg.persistence, "batch": cfg.batch,
+                   "h2d_mode": args.h2d_mode, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (per-token weights ~2 GB > 129 MB)"},
+        "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": table,
+        "h2d_peak_gbs": round(h2d_peak, 1), "gpu_launches": launches,
+        "clocks": clk.summary(), "e2e": e2e, "workload_gen_s": round(gen_s, 1),
+    }
+    return line, wl
+
+
+def run_oracle_tokens(wl, n_tokens, budget_s=None):
+    """Decode tokens with the fp64 oracle from a cold start; returns
+    (tokens timed, seconds) excluding the first (cold-start) token."""
+    import numpy as np
+    from oracle import OracleDecoder
+    orc = OracleDecoder(wl, materialize_buffers=False)
+    orc.step(wl.x[0].numpy())
+    t0 = time.time()
+    n = 0
+    for t in range(1, 1 + n_tokens):
+        orc.step(wl.x[t % wl.x.shape[0]].numpy())
+        n += 1
+        if budget_s and time.time() - t0 > budget_s:
+            break
+    return n, time.time() - t0
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    res = run_cuda(args)
+    if res is None:
+        return
+    line, wl = res
+    if not args.no_cpu_baseline and args.gpus == 1 and int(os.environ.get("WORLD_SIZE", "1")) == 1:
+        n, sec = run_oracle_tokens(wl, args.cpu_sample_tokens, budget_s=45)
+        line["cpu_baseline"] = {"value": round(n / sec, 4), "unit": "tok/s", "cores": cores_used(),
+                                "kind": "oracle",
+                                "sample": f"{n} tokens of {wl.cfg.name} after a cold-start token, fp64 numpy"}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The reference arm is the fp64 oracle on the host cores, same config and
+    metric, on a bounded sample of tokens."""
+    import torch  # noqa: F401
+    from workloads import CONFIGS, make_workload
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    base = CONFIGS[args.config]
+    n_tok = max(1, min(args.steps, 8))
+    cfg = base.replace(n_warm=0, n_decode=n_tok + 1)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = make_workload(cfg, device=dev)
+    wl.dense_w = wl.dense_w.cpu() if wl.dense_w is not None else None
+    wl.pred_w1, wl.pred_w2 = wl.pred_w1.cpu(), wl.pred_w2.cpu()
+    n, sec = run_oracle_tokens(wl, n_tok, budget_s=120)
+    v = n / sec
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": n, "warmup": 1, "ms_per_step": round(1e3 * sec / n, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name},
+            "cpu_baseline": {"value": round(v, 4), "unit": "tok/s", "cores": cores_used(), "kind": "oracle",
+                             "sample": f"{n} tokens of {cfg.name} after a cold-start token"},
+            "e2e": {"value": round(v, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

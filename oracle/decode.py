@@ -221,7 +221,11 @@ class TokenRecord:
     d_in: list = field(default_factory=list)        # per layer: [(neuron, slot)]
     d_out: list = field(default_factory=list)       # per layer: sorted IDs
     y: list = field(default_factory=list)           # per layer: [B][D] fp64
+    h_in: list = field(default_factory=list)        # per layer: [B][D] input
+    y_dense: list = field(default_factory=list)     # per dense layer: [B][D]
+    h_in_dense: list = field(default_factory=list)  # per dense layer: [B][D] input
     pred_logits_layer: list = field(default_factory=list)  # per-layer predictor
+    pred_xhat: list = field(default_factory=list)   # predictor input per sequence / layer
     h: np.ndarray | None = None                     # [B][D] after the last layer
 
 
@@ -292,9 +296,12 @@ class OracleDecoder:
         # keep their MLP fully resident).
         for layer in range(cfg.n_dense):
             g, u, dt = self._dense_rows(layer)
+            rec.h_in_dense.append(h.copy())
+            yd = np.zeros((B, cfg.d_model))
             for b in range(B):
-                y, _ = ffn_rows(g, u, dt, rnd(rmsnorm(h[b])))
-                h[b] += y
+                yd[b], _ = ffn_rows(g, u, dt, rnd(rmsnorm(h[b])))
+                h[b] += yd[b]
+            rec.y_dense.append(yd)
             if layer == 0:
                 self._predict_shared(h, rec, ids_override)
         if cfg.n_dense == 0 and cfg.pred_kind == "shared_argmax":
@@ -308,6 +315,7 @@ class OracleDecoder:
                 w1, w2, b2 = self._pred(layer)
                 xs = rmsnorm(h[0])
                 lg = predictor_logits(w1, w2, b2, xs)
+                rec.pred_xhat.append(xs)
                 rec.pred_logits_layer.append(lg)
                 fire = (lg > 0.0) if fire_override is None else np.asarray(fire_override[s])
                 active = [int(n) for n in np.flatnonzero(fire)]
@@ -337,6 +345,7 @@ class OracleDecoder:
                         self.bufs[s, p, slot] = wl.store[s, n, p]
             # Sparse FFN over the resident active rows.
             g, u, dt = self._sparse_rows(s, active)
+            rec.h_in.append(h.copy())
             ys = np.zeros((B, cfg.d_model))
             for b in range(B):
                 ys[b], _ = ffn_rows(g, u, dt, rnd(rmsnorm(h[b])))
@@ -351,7 +360,9 @@ class OracleDecoder:
         w1, w2, _ = self._pred()
         rnd = round_bf16 if cfg.batch > 1 else (lambda v: v)
         for b in range(cfg.batch):
-            lg = predictor_logits(w1, w2, None, rnd(rmsnorm(h[b])))
+            xs = rnd(rmsnorm(h[b]))
+            lg = predictor_logits(w1, w2, None, xs)
+            rec.pred_xhat.append(xs)
             rec.logits.append(lg)
             ids = head_argmax(lg, cfg.n_heads, cfg.n_centroids)
             if ids_override is not None:

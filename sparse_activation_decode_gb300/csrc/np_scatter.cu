@@ -1,0 +1,137 @@
+// Incoming-row movement (sm_103a): host weight store -> device staging ->
+// projection buffers.
+//
+// NeuroPrefetcher section 3.5 ("I/O Path") and its full text: incoming
+// neuron IDs are sorted and read as neuron-centric records (gate | up |
+// down^T rows of one neuron, contiguous in a layer-major file) into a
+// capacity-bounded staging buffer; a fused deinterleave-and-scatter kernel
+// writes each record's rows into the slot the delta runtime assigned, and a
+// delta larger than the staging capacity is processed as independent
+// read+scatter chunks.
+//
+// Here the storage tier is CPU memory that the GPU reads over the host link
+// (NVLink-C2C on GB300).  Individual host-to-device copies per record are
+// limited by per-call overhead, so the read is a gather kernel: one CTA per
+// record, every thread keeping eight 16-byte loads in flight, which
+// saturates the link with a few dozen CTAs.  The scatter kernel works in
+// device memory and is HBM-bound: one CTA per (record, projection row).
+#include "np_common.cuh"
+#include "np_kernels.h"
+
+namespace np {
+
+constexpr int kMoveThreads = 256;
+constexpr int kIlp = 8;
+
+__device__ __forceinline__ void copy_vecs(const uint4* __restrict__ src, uint4* __restrict__ dst, int n) {
+  for (int base = threadIdx.x; base < n; base += kMoveThreads * kIlp) {
+    uint4 v[kIlp];
+#pragma unroll
+    for (int u = 0; u < kIlp; ++u) {
+      const int j = base + u * kMoveThreads;
+      if (j < n) v[u] = src[j];
+    }
+#pragma unroll
+    for (int u = 0; u < kIlp; ++u) {
+      const int j = base + u * kMoveThreads;
+      if (j < n) dst[j] = v[u];
+    }
+  }
+}
+
+__device__ __forceinline__ int chunk_end(const MoveLaunch& a) {
+  int cnt = *a.count;
+  if (cnt > a.K) cnt = a.K;
+  const int end = a.chunk_begin + a.chunk_cap;
+  return cnt < end ? cnt : end;
+}
+
+// staging[i - begin] = store[din_n[i]] for the chunk's records
+__global__ void __launch_bounds__(kMoveThreads) gather_kernel(MoveLaunch a) {
+  const int end = chunk_end(a);
+  const uint4* store = static_cast<const uint4*>(a.store_layer);
+  uint4* stg = static_cast<uint4*>(a.staging);
+  for (int i = a.chunk_begin + blockIdx.x; i < end; i += gridDim.x) {
+    const int n = a.din_n[i];
+    if ((unsigned)n >= (unsigned)a.F) {
+      if (threadIdx.x == 0) atomicExch(a.err, kDevErrBounds);
+      continue;
+    }
+    copy_vecs(store + (size_t)n * a.rec_vec, stg + (size_t)(i - a.chunk_begin) * a.rec_vec, a.rec_vec);
+  }
+}
+
+// bufs[p][din_s[i]] = staging[i - begin].row[p]: one CTA per (record, row)
+__global__ void __launch_bounds__(kMoveThreads) scatter_kernel(MoveLaunch a) {
+  const int end = chunk_end(a);
+  const int units = (end - a.chunk_begin) * a.n_proj;
+  const uint4* stg = static_cast<const uint4*>(a.staging);
+  uint4* bufs = static_cast<uint4*>(a.bufs_layer);
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int r = u / a.n_proj, p = u - r * a.n_proj;
+    const int slot = a.din_s[a.chunk_begin + r];
+    if ((unsigned)slot >= (unsigned)a.K) {
+      if (threadIdx.x == 0) atomicExch(a.err, kDevErrBounds);
+      continue;
+    }
+    copy_vecs(stg + (size_t)r * a.rec_vec + (size_t)p * a.row_vec,
+              bufs + ((size_t)p * a.K + slot) * a.row_vec, a.row_vec);
+  }
+}
+
+// store record -> buffers directly (no staging)
+__global__ void __launch_bounds__(kMoveThreads) fused_kernel(MoveLaunch a) {
+  const int end = chunk_end(a);
+  const uint4* store = static_cast<const uint4*>(a.store_layer);
+  uint4* bufs = static_cast<uint4*>(a.bufs_layer);
+  for (int i = a.chunk_begin + blockIdx.x; i < end; i += gridDim.x) {
+    const int n = a.din_n[i], slot = a.din_s[i];
+    if ((unsigned)n >= (unsigned)a.F || (unsigned)slot >= (unsigned)a.K) {
+      if (threadIdx.x == 0) atomicExch(a.err, kDevErrBounds);
+      continue;
+    }
+    const uint4* src = store + (size_t)n * a.rec_vec;
+    for (int p = 0; p < a.n_proj; ++p)
+      copy_vecs(src + (size_t)p * a.row_vec, bufs + ((size_t)p * a.K + slot) * a.row_vec, a.row_vec);
+  }
+}
+
+// Put back what the assigned slots held before this delta: the record of
+// content_old[slot], or zeros for a slot that never held a row.
+__global__ void __launch_bounds__(kMoveThreads) restore_kernel(MoveLaunch a) {
+  const int end = chunk_end(a);
+  const uint4* store = static_cast<const uint4*>(a.store_layer);
+  uint4* bufs = static_cast<uint4*>(a.bufs_layer);
+  for (int i = a.chunk_begin + blockIdx.x; i < end; i += gridDim.x) {
+    const int slot = a.din_s[i];
+    if ((unsigned)slot >= (unsigned)a.K) continue;
+    const int n = a.content_old[slot];
+    for (int p = 0; p < a.n_proj; ++p) {
+      uint4* dst = bufs + ((size_t)p * a.K + slot) * a.row_vec;
+      if ((unsigned)n < (unsigned)a.F) {
+        copy_vecs(store + (size_t)n * a.rec_vec + (size_t)p * a.row_vec, dst, a.row_vec);
+      } else {
+        for (int j = threadIdx.x; j < a.row_vec; j += kMoveThreads) dst[j] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+}
+
+cudaError_t launch_gather(const MoveLaunch& a, cudaStream_t st) {
+  gather_kernel<<<a.grid, kMoveThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+cudaError_t launch_scatter(const MoveLaunch& a, cudaStream_t st) {
+  scatter_kernel<<<a.grid, kMoveThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+cudaError_t launch_fused(const MoveLaunch& a, cudaStream_t st) {
+  fused_kernel<<<a.grid, kMoveThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+cudaError_t launch_restore(const MoveLaunch& a, cudaStream_t st) {
+  restore_kernel<<<a.grid, kMoveThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace np
