@@ -43,7 +43,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=128)
     p.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     p.add_argument("--config", default="llama2-7b-relu")
-    p.add_argument("--h2d-mode", default="staged", choices=["staged", "fused"])
+    p.add_argument("--h2d-mode", default="fused", choices=["staged", "fused"])
     p.add_argument("--cpu-sample-tokens", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -283,11 +283,11 @@ def run_oracle_tokens(wl, n_tokens, budget_s=None):
     import numpy as np
     from oracle import OracleDecoder
     orc = OracleDecoder(wl, materialize_buffers=False)
-    orc.step(wl.x[0].numpy())
+    orc.step(wl.x[0].cpu().numpy())
     t0 = time.time()
     n = 0
     for t in range(1, 1 + n_tokens):
-        orc.step(wl.x[t % wl.x.shape[0]].numpy())
+        orc.step(wl.x[t % wl.x.shape[0]].cpu().numpy())
         n += 1
         if budget_s and time.time() - t0 > budget_s:
             break

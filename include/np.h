@@ -186,9 +186,9 @@ np_status np_predict(np_model* m, int32_t layer, const float* h_dev, void* out_d
  * capped to the K_max lowest IDs; D_in = A minus R_prev, D_out = R_prev minus
  * R_next; incoming neurons in ascending ID order take free slots in ascending
  * slot order (NeuroPrefetcher full text, delta runtime and slot map).  The
- * new slot maps stay pending until np_scatter commits them.  `out` may be
- * NULL.  Errors: NP_ERR_ARG, NP_ERR_STATE (a delta for that layer is already
- * pending). */
+ * new state is written in place and stays pending until np_scatter succeeds
+ * (a failed read rolls it back).  `out` may be NULL.  Errors: NP_ERR_ARG,
+ * NP_ERR_STATE (a delta for that layer is already pending). */
 np_status np_delta(np_model* m, int32_t layer, const void* pred_dev, np_delta_view* out);
 
 /* Views of the last computed delta and predictor output (e.g. after
@@ -199,10 +199,10 @@ np_status np_last_delta(np_model* m, np_delta_view* out);
  * their rows into the resident buffers at the assigned slots, chunked by the
  * staging capacity (NeuroPrefetcher section 3.5, launch_deinterleave_scatter;
  * "independent submit-and-scatter chunks").  layer = -1: all pending layers;
- * layer = l: that layer only.  On success the pending slot maps become the
- * committed state.  If the read hook fails, rows already written are restored
- * from the store, the pending delta is discarded, and NP_ERR_IO is returned
- * with the committed state as before the call. */
+ * layer = l: that layer only.  On success the pending state is committed.
+ * If the read hook fails, rows already written are restored from the store,
+ * every pending delta is rolled back, and NP_ERR_IO is returned with the
+ * state as before the deltas. */
 np_status np_scatter(np_model* m, int32_t layer);
 
 /* Sparse FFN of sparse layer `layer` over its resident active rows, read
@@ -225,7 +225,8 @@ np_status np_dense_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_
 np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host);
 
 /* Copy the committed slot map [F] and inverse map [K] of sparse layer
- * `layer` to host memory (either pointer may be NULL).  Synchronous. */
+ * `layer` to host memory (either pointer may be NULL).  Synchronous.
+ * NP_ERR_STATE while a delta is pending for that layer. */
 np_status np_get_state(np_model* m, int32_t layer, int32_t* slotmap_host, int32_t* inv_host);
 
 /* Device pointer to resident buffer `proj` (0..n_proj-1) of sparse layer
@@ -256,6 +257,13 @@ np_status np_set_profiling(np_model* m, int32_t enable);
  * counts; bytes_out[NP_N_KINDS]: algorithmic bytes moved by those launches.
  * Any pointer may be NULL.  Resets the accumulators. */
 np_status np_get_profile(np_model* m, double* ms_out, int64_t* launches_out, int64_t* bytes_out);
+
+/* Timeline of the launches timed since the last np_get_profile, in issue
+ * order: kind (NP_KIND_*), start and end in milliseconds relative to the
+ * first one (events recorded on each launch's own stream).  Writes at most
+ * max_entries entries and their count to *n_out.  Synchronous. */
+np_status np_get_timeline(np_model* m, int32_t* kinds, float* start_ms, float* end_ms, int32_t max_entries,
+                          int32_t* n_out);
 
 /* Make a caller-owned host range readable by the device (page-locked,
  * mapped).  Synchronous.  Unregister before freeing the memory. */

@@ -67,6 +67,7 @@ SIGNATURES = {
     "np_check_error": (_I32, [_P]),
     "np_set_profiling": (_I32, [_P, _I32]),
     "np_get_profile": (_I32, [_P, _P, _P, _P]),
+    "np_get_timeline": (_I32, [_P, _P, _P, _P, _I32, _P]),
     "np_host_register": (_I32, [_P, _SZ]),
     "np_host_unregister": (_I32, [_P]),
     "np_launch_count": (_I64, [_P]),

@@ -6,18 +6,23 @@
 //   main: dense layer 0 -> predictor -> set/delta kernel -> [event set]
 //         -> dense layers 1..d-1 -> for each sparse layer: wait for that
 //         layer's rows, FFN, residual update
-//   side: wait [event set] -> for each sparse layer: gather its incoming
-//         records over the host link into staging, deinterleave-scatter them
-//         into the layer's buffers (chunked by the staging capacity)
-//         -> [event layer s]
+//   gather streams G0 (the caller's side stream) and G1, alternating by
+//         layer: wait [event set] -> gather the layer's incoming records over
+//         the host link into staging buffer s%2 -> [event gathered s]
+//   scatter stream X: wait [gathered s] -> deinterleave-scatter staging into
+//         the layer's buffers -> [event ready s]
+//   (chunked by the staging capacity; two layers' gathers can be in flight
+//   at once, so the host link does not idle while a layer is scattered)
 //
 // Decode state (slot maps, inverse maps, slot contents, resident bitmasks,
-// window history) is double-buffered per sparse layer: the set kernel reads
-// the committed half and writes the other; the host flips the layer's bit
-// once its rows are in place, so a failed read leaves the committed state
-// untouched (rows already overwritten are restored from the store).
+// window history) is updated in place by the set kernel, which records every
+// value it overwrites in the delta lists.  If the incoming rows cannot be
+// read, a rollback kernel restores the previous state from those lists and
+// the rows already overwritten are copied back from the store.
 #include <cuda_runtime.h>
 
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -64,15 +69,16 @@ struct np_model {
   int sms = 0;
   size_t smem_optin = 0;
   size_t row_bytes = 0, rec_bytes = 0;
-  cudaStream_t main = nullptr, side = nullptr;
+  cudaStream_t main = nullptr, side = nullptr;  // side = gather stream G0
+  cudaStream_t g1 = nullptr, xs = nullptr;        // gather stream G1, scatter stream X
   const unsigned char* store_dev = nullptr;
   // device allocations
   void* bufs = nullptr;
-  void* staging = nullptr;
+  void* staging = nullptr;  // two buffers of staging_rows records
   int *slotmap = nullptr, *inv = nullptr, *content = nullptr, *last_seen = nullptr;
   uint32_t* resbits = nullptr;
   int *counts = nullptr, *active = nullptr, *active_slot = nullptr, *din_n = nullptr, *din_s = nullptr,
-      *dout_n = nullptr;
+      *din_oldct = nullptr, *dout_n = nullptr, *dout_s = nullptr, *ls_old = nullptr;
   unsigned long long* totals = nullptr;
   int* err = nullptr;
   float* z = nullptr;
@@ -81,27 +87,38 @@ struct np_model {
   uint32_t* fire = nullptr;
   float* logits = nullptr;
   float* part = nullptr;
+  int* slice_cnt = nullptr;
   std::vector<void*> allocs;
   // launch shapes
-  int ffn_grid = 0, ffn_stages = 0, ffn_stages_dense = 0;
+  int ffn_grid = 0, ffn_cluster = 1, ffn_stages = 0, ffn_stages_dense = 0;
   int gather_grid = 0, scatter_grid = 0, pred_grid = 0;
   int rps1 = 1, rps2 = 1, ns1 = 2, ns2 = 2;
   // state
-  uint64_t cur_bits = 0, pending_bits = 0, committed_since_token = 0;
+  uint64_t pending_bits = 0, committed_since_token = 0;
   int64_t token = 0;
   int64_t launches = 0;
-  cudaEvent_t ev_set = nullptr, ev_side_done = nullptr;
-  std::vector<cudaEvent_t> ev_layer;
+  cudaEvent_t ev_set = nullptr, ev_side_done = nullptr, ev_j[3] = {nullptr, nullptr, nullptr};
+  std::vector<cudaEvent_t> ev_g, ev_layer;  // per sparse layer: gathered, ready
   // profiling
   bool prof = false;
-  std::vector<EventPair> prof_pending[NP_N_KINDS];
   std::vector<EventPair> prof_free;
   double prof_ms[NP_N_KINDS] = {};
   int64_t prof_launches[NP_N_KINDS] = {};
   int64_t prof_fixed_bytes[NP_N_KINDS] = {};
+  // timeline of timed launches in issue order: (kind, events)
+  std::vector<std::pair<int, EventPair>> trace;
 };
 
 namespace {
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  const int x = std::atoi(v);
+  return x > 0 ? x : dflt;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 uint64_t all_layers(const np_model* m) { return m->S >= 64 ? ~0ull : ((1ull << m->S) - 1ull); }
 
@@ -134,26 +151,27 @@ np_status prof_begin(np_model* m, int kind, cudaStream_t st, EventPair* ep) {
   return NP_OK;
 }
 
-np_status prof_fold(np_model* m, int kind, size_t keep) {
-  auto& v = m->prof_pending[kind];
-  if (v.size() <= keep) return NP_OK;
-  const size_t n = v.size() - keep;
+// Accumulate the durations of the oldest `n` traced launches and recycle
+// their events.
+np_status prof_fold(np_model* m, size_t n) {
+  if (n > m->trace.size()) n = m->trace.size();
   for (size_t i = 0; i < n; ++i) {
-    CUDA_TRY(cudaEventSynchronize(v[i].b));
+    const auto& t = m->trace[i];
+    CUDA_TRY(cudaEventSynchronize(t.second.b));
     float ms = 0.f;
-    CUDA_TRY(cudaEventElapsedTime(&ms, v[i].a, v[i].b));
-    m->prof_ms[kind] += ms;
-    m->prof_free.push_back(v[i]);
+    CUDA_TRY(cudaEventElapsedTime(&ms, t.second.a, t.second.b));
+    m->prof_ms[t.first] += ms;
+    m->prof_free.push_back(t.second);
   }
-  v.erase(v.begin(), v.begin() + n);
+  m->trace.erase(m->trace.begin(), m->trace.begin() + n);
   return NP_OK;
 }
 
 np_status prof_end(np_model* m, int kind, cudaStream_t st, const EventPair& ep) {
   CUDA_TRY(cudaEventRecord(ep.b, st));
-  m->prof_pending[kind].push_back(ep);
+  m->trace.push_back({kind, ep});
   m->prof_launches[kind] += 1;
-  if (m->prof_pending[kind].size() > 4096) NP_TRY(prof_fold(m, kind, 1024));
+  if (m->trace.size() > 16384) NP_TRY(prof_fold(m, 8192));
   return NP_OK;
 }
 
@@ -192,6 +210,10 @@ np_status enqueue_ffn(np_model* m, int kind, const unsigned char* base, size_t p
   a.list_cap = list_cap;
   a.row_limit = row_limit;
   a.part = m->part;
+  a.slice_cnt = m->slice_cnt;
+  a.cluster = m->ffn_cluster;
+  a.h_out = h_out;
+  a.y_out = y_out;
   a.D = m->D;
   a.dtype = m->d.dtype;
   a.dtype_bytes = m->esz;
@@ -200,10 +222,7 @@ np_status enqueue_ffn(np_model* m, int kind, const unsigned char* base, size_t p
   a.grid = m->ffn_grid;
   a.err = m->err;
   cudaStream_t st = m->main;
-  NP_TRY(launch(m, kind, st, fixed_bytes, [&] { return launch_ffn_rows(a, st); }));
-  NP_TRY(launch(m, NP_KIND_FINISH, st, 0,
-                [&] { return launch_ffn_finish(m->part, m->ffn_grid, m->D, h_in, h_out, y_out, st); }));
-  return NP_OK;
+  return launch(m, kind, st, fixed_bytes, [&] { return launch_ffn_rows(a, st); });
 }
 
 np_status enqueue_dense(np_model* m, int layer, const float* h_in, float* h_out, float* y_out) {
@@ -247,12 +266,13 @@ np_status enqueue_rowdot(np_model* m, const void* W, int n_rows, int len, const 
   return launch(m, NP_KIND_PRED, st, (int64_t)n_rows * len * m->esz, [&] { return launch_rowdot(a, st); });
 }
 
-np_status enqueue_predict(np_model* m, int layer, const float* h) {
+np_status enqueue_predict(np_model* m, int layer, const float* h, bool want_ids = true) {
   if (m->d.pred_kind == NP_PRED_SHARED_ARGMAX) {
     NP_TRY(enqueue_rowdot(m, m->d.pred_w1, m->H, m->D, h, 1, 0, nullptr, m->z, nullptr, 0, nullptr,
                           reinterpret_cast<uint32_t*>(m->keys), 2 * m->NH, m->rps1, m->ns1));
     NP_TRY(enqueue_rowdot(m, m->d.pred_w2, m->NH * m->C, m->H, m->z, 0, 1, nullptr, nullptr, m->keys, m->C,
                           nullptr, nullptr, 0, m->rps2, m->ns2));
+    if (!want_ids) return NP_OK;
     cudaStream_t st = m->main;
     return launch(m, NP_KIND_PRED, st, 0, [&] { return launch_keys_to_ids(m->keys, m->NH, m->ids, st); });
   }
@@ -266,38 +286,15 @@ np_status enqueue_predict(np_model* m, int layer, const float* h) {
                         m->ns2);
 }
 
-np_status enqueue_set(np_model* m, int first_sparse, int n_layers, const int* ids, const uint32_t* fire) {
-  SetLaunch a{};
-  a.n_layers_launch = n_layers;
-  a.first_sparse = first_sparse;
-  a.n_dense = m->dn;
-  a.F = m->F;
-  a.K = m->K;
-  a.C = m->C;
-  a.words = m->W;
-  a.combine = m->d.combine;
-  a.window = m->window;
-  a.batch = m->B;
-  a.n_heads = m->NH;
-  a.token = (int)m->token;
+SetLaunch set_args(np_model* m, int first_sparse, int n_layers);
+
+np_status enqueue_set(np_model* m, int first_sparse, int n_layers, const int* ids, const uint32_t* fire,
+                      const unsigned long long* keys = nullptr) {
+  SetLaunch a = set_args(m, first_sparse, n_layers);
   a.ids = ids;
+  a.keys = keys;
+  a.ids_out = keys ? m->ids : nullptr;
   a.fire = fire;
-  a.centroids = m->d.centroids;
-  a.cur_bits = m->cur_bits;
-  a.slotmap = m->slotmap;
-  a.inv = m->inv;
-  a.content = m->content;
-  a.resbits = m->resbits;
-  a.last_seen = m->last_seen;
-  a.S = m->S;
-  a.counts = m->counts;
-  a.active = m->active;
-  a.active_slot = m->active_slot;
-  a.din_n = m->din_n;
-  a.din_s = m->din_s;
-  a.dout_n = m->dout_n;
-  a.totals = m->totals;
-  a.err = m->err;
   cudaStream_t st = m->main;
   NP_TRY(launch(m, NP_KIND_SET, st, (int64_t)n_layers * m->W * 4 * 2 * m->B, [&] { return launch_set(a, st); }));
   CUDA_TRY(cudaEventRecord(m->ev_set, st));
@@ -315,69 +312,137 @@ MoveLaunch move_args(const np_model* m, int s) {
   a.din_n = m->din_n + (size_t)s * m->K;
   a.din_s = m->din_s + (size_t)s * m->K;
   a.count = m->counts + (size_t)s * 4 + 1;
-  a.staging = m->staging;
+  a.staging = static_cast<unsigned char*>(m->staging) + (size_t)(s & 1) * m->staging_rows * m->rec_bytes;
   a.bufs_layer = const_cast<unsigned char*>(layer_bufs(m, s));
   a.err = m->err;
   return a;
 }
 
-// Enqueue the reads and scatters of sparse layer s on the side stream.
+cudaStream_t gather_stream(const np_model* m, int s) { return (s & 1) ? m->g1 : m->side; }
+
+// Make `st` wait for all work queued so far on the gather and scatter streams.
+np_status join_side(np_model* m, cudaStream_t st) {
+  const cudaStream_t src[3] = {m->side, m->g1, m->xs};
+  for (int k = 0; k < 3; ++k) {
+    CUDA_TRY(cudaEventRecord(m->ev_j[k], src[k]));
+    CUDA_TRY(cudaStreamWaitEvent(st, m->ev_j[k], 0));
+  }
+  return NP_OK;
+}
+
+// Enqueue the reads and scatters of sparse layer s: gathers on G[s%2] into
+// staging buffer s%2, scatters on X; ev_layer[s] marks the rows in place.
 np_status enqueue_move(np_model* m, int s) {
-  cudaStream_t st = m->side;
+  cudaStream_t g = gather_stream(m, s), x = m->xs;
   MoveLaunch a = move_args(m, s);
   if (m->d.h2d_mode == NP_H2D_FUSED) {
     a.chunk_begin = 0;
     a.chunk_cap = m->K;
     a.grid = m->gather_grid;
-    NP_TRY(launch(m, NP_KIND_GATHER, st, 0, [&] { return launch_fused(a, st); }));
-  } else {
-    for (int c = 0; c * m->staging_rows < m->K; ++c) {
-      a.chunk_begin = c * m->staging_rows;
-      a.chunk_cap = m->staging_rows;
-      a.grid = m->gather_grid;
-      NP_TRY(launch(m, NP_KIND_GATHER, st, 0, [&] { return launch_gather(a, st); }));
-      a.grid = m->scatter_grid;
-      NP_TRY(launch(m, NP_KIND_SCATTER, st, 0, [&] { return launch_scatter(a, st); }));
-    }
+    NP_TRY(launch(m, NP_KIND_GATHER, g, 0, [&] { return launch_fused(a, g); }));
+    CUDA_TRY(cudaEventRecord(m->ev_layer[s], g));
+    return NP_OK;
   }
-  CUDA_TRY(cudaEventRecord(m->ev_layer[s], st));
+  for (int c = 0; c * m->staging_rows < m->K; ++c) {
+    // staging buffer s%2 is free once the scatter that last read it is done
+    if (c > 0) CUDA_TRY(cudaStreamWaitEvent(g, m->ev_layer[s], 0));
+    else if (s >= 2) CUDA_TRY(cudaStreamWaitEvent(g, m->ev_layer[s - 2], 0));
+    a.chunk_begin = c * m->staging_rows;
+    a.chunk_cap = m->staging_rows;
+    a.grid = m->gather_grid;
+    NP_TRY(launch(m, NP_KIND_GATHER, g, 0, [&] { return launch_gather(a, g); }));
+    CUDA_TRY(cudaEventRecord(m->ev_g[s], g));
+    CUDA_TRY(cudaStreamWaitEvent(x, m->ev_g[s], 0));
+    a.grid = m->scatter_grid;
+    NP_TRY(launch(m, NP_KIND_SCATTER, x, 0, [&] { return launch_scatter(a, x); }));
+    CUDA_TRY(cudaEventRecord(m->ev_layer[s], x));
+  }
   return NP_OK;
 }
 
 // Restore the slots written for sparse layer s by the pending delta.
 np_status enqueue_restore(np_model* m, int s) {
-  cudaStream_t st = m->side;
+  cudaStream_t st = m->xs;
+  CUDA_TRY(cudaStreamWaitEvent(st, m->ev_layer[s], 0));
   MoveLaunch a = move_args(m, s);
-  const int cb = (int)((m->cur_bits >> s) & 1ull);
-  a.content_old = m->content + ((size_t)cb * m->S + s) * m->K;
+  a.din_oldct = m->din_oldct + (size_t)s * m->K;
   a.chunk_begin = 0;
   a.chunk_cap = m->K;
   a.grid = m->gather_grid;
   return launch(m, NP_KIND_GATHER, st, 0, [&] { return launch_restore(a, st); });
 }
 
+SetLaunch set_args(np_model* m, int first_sparse, int n_layers) {
+  SetLaunch a{};
+  a.n_layers_launch = n_layers;
+  a.first_sparse = first_sparse;
+  a.n_dense = m->dn;
+  a.F = m->F;
+  a.K = m->K;
+  a.C = m->C;
+  a.words = m->W;
+  a.combine = m->d.combine;
+  a.window = m->window;
+  a.batch = m->B;
+  a.n_heads = m->NH;
+  a.token = (int)m->token;
+  a.centroids = m->d.centroids;
+  a.slotmap = m->slotmap;
+  a.inv = m->inv;
+  a.content = m->content;
+  a.resbits = m->resbits;
+  a.last_seen = m->last_seen;
+  a.S = m->S;
+  a.counts = m->counts;
+  a.active = m->active;
+  a.active_slot = m->active_slot;
+  a.din_n = m->din_n;
+  a.din_s = m->din_s;
+  a.din_oldct = m->din_oldct;
+  a.dout_n = m->dout_n;
+  a.dout_s = m->dout_s;
+  a.ls_old = m->ls_old;
+  a.totals = m->totals;
+  a.err = m->err;
+  return a;
+}
+
+// Drop every pending delta: copy back the bytes of the slots already written
+// for the layers in `moved`, then undo the state changes of all pending
+// layers from the recorded lists.
+np_status abort_pending(np_model* m, const std::vector<int>& moved) {
+  for (int s : moved) NP_TRY(enqueue_restore(m, s));
+  NP_TRY(join_side(m, m->main));
+  cudaStream_t st = m->main;
+  for (int s = 0; s < m->S; ++s) {
+    if (!(m->pending_bits & (1ull << s))) continue;
+    SetLaunch a = set_args(m, s, 1);
+    NP_TRY(launch(m, NP_KIND_SET, st, 0, [&] { return launch_rollback(a, st); }));
+  }
+  m->pending_bits = 0;
+  return NP_OK;
+}
+
 // Reads for the pending layers in `layers` (ascending), with the read hook.
-// On a hook failure the already-enqueued layers are restored and the pending
-// delta of every layer in `layers` is dropped.
-np_status move_layers(np_model* m, const std::vector<int>& layers) {
+// On a hook failure returns NP_ERR_IO with *n_moved = layers whose reads were
+// enqueued; the caller aborts the pending deltas.
+np_status move_layers(np_model* m, const std::vector<int>& layers, size_t* n_moved) {
+  *n_moved = 0;
   CUDA_TRY(cudaStreamWaitEvent(m->side, m->ev_set, 0));
+  CUDA_TRY(cudaStreamWaitEvent(m->g1, m->ev_set, 0));
   for (size_t k = 0; k < layers.size(); ++k) {
     const int s = layers[k];
     if (m->d.read_hook && m->d.read_hook(m->d.read_ctx, m->dn + s, (int32_t)m->token) != 0) {
-      for (size_t q = 0; q < k; ++q) NP_TRY(enqueue_restore(m, layers[q]));
-      for (int s2 : layers) m->pending_bits &= ~(1ull << s2);
-      CUDA_TRY(cudaEventRecord(m->ev_side_done, m->side));
-      CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_side_done, 0));
       g_last_err = "storage read hook failed";
       return NP_ERR_IO;
     }
     NP_TRY(enqueue_move(m, s));
+    *n_moved = k + 1;
   }
   return NP_OK;
 }
 
 void commit(np_model* m, uint64_t bits) {
-  m->cur_bits ^= bits;
   m->pending_bits &= ~bits;
   m->committed_since_token |= bits;
   if ((m->committed_since_token & all_layers(m)) == all_layers(m)) {
@@ -399,6 +464,8 @@ np_status read_device_error(np_model* m) {
 
 np_status sync_model(np_model* m) {
   CUDA_TRY(cudaStreamSynchronize(m->side));
+  CUDA_TRY(cudaStreamSynchronize(m->g1));
+  CUDA_TRY(cudaStreamSynchronize(m->xs));
   CUDA_TRY(cudaStreamSynchronize(m->main));
   return NP_OK;
 }
@@ -457,7 +524,8 @@ static np_status validate(const np_model_desc* d) {
   const int esz = d->dtype == NP_F32 ? 4 : 2;
   if (d->d_model < 8 || d->d_model > 8192 || (d->d_model * esz) % 16 != 0)
     return arg_fail("d_model must be in [8, 8192] with rows a multiple of 16 bytes");
-  if (d->d_model / (16 / esz) > kThreads * kMaxChunksPerThread) return arg_fail("d_model too large for dtype");
+  if (d->d_model / (16 / esz) > kThreads * kMaxChunksPerThread || d->d_model / (16 / esz) > ffn_max_chunks())
+    return arg_fail("d_model too large for dtype");
   if (d->d_ff < 1 || d->d_ff > 16384) return arg_fail("d_ff must be in [1, 16384]");
   if (d->k_max < 1 || d->k_max > d->d_ff || d->k_max > 8192) return arg_fail("k_max must be in [1, min(d_ff, 8192)]");
   if (d->has_gate != 0 && d->has_gate != 1) return arg_fail("has_gate must be 0 or 1");
@@ -543,12 +611,23 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
 
   // launch shapes: two streaming CTAs per SM
   const size_t per_cta = m->smem_optin > 2048 ? (m->smem_optin / 2) - 1024 : m->smem_optin;
-  m->ffn_stages = ffn_pick_stages(m->D, m->esz, m->nproj, per_cta);
-  m->ffn_stages_dense = m->ffn_stages;
-  if (m->ffn_stages < 2) return fail(arg_fail("d_model too large for the shared-memory ring"));
-  m->ffn_grid = 2 * m->sms;
-  m->gather_grid = 2 * m->sms;
-  m->scatter_grid = 4 * m->sms;
+  {
+    e = ffn_plan(m->d.dtype, m->d.has_gate, m->D, m->esz, m->smem_optin - 1024, m->sms, &m->ffn_stages,
+                 &m->ffn_cluster, &m->ffn_grid);
+    if (e != cudaSuccess) return fail(cuda_fail(e, "ffn_plan"));
+    m->ffn_stages_dense = m->ffn_stages;
+    // NP_TUNE_FFN_CTAS caps the FFN grid (rounded down to whole clusters)
+    const int cap = env_int("NP_TUNE_FFN_CTAS", 0);
+    if (cap > 0 && cap < m->ffn_grid) m->ffn_grid = (cap / m->ffn_cluster > 0 ? cap / m->ffn_cluster : 1) * m->ffn_cluster;
+    if (env_int("NP_TUNE_VERBOSE", 0) == 1)
+      std::fprintf(stderr, "np: ffn grid %d cluster %d ring %d slots; gather %d scatter %d CTAs\n", m->ffn_grid,
+                   m->ffn_cluster, m->ffn_stages, m->gather_grid, m->scatter_grid);
+  }
+  // Host-link gathers need only a few MB in flight to fill the link; keeping
+  // their grids small leaves the SMs to the FFN running beside them.
+  // NP_TUNE_GATHER_CTAS / NP_TUNE_SCATTER_CTAS override the defaults.
+  m->gather_grid = env_int("NP_TUNE_GATHER_CTAS", 32);
+  m->scatter_grid = env_int("NP_TUNE_SCATTER_CTAS", 4 * m->sms);
   m->pred_grid = 2 * m->sms;
   m->rps1 = pick_rps(m->row_bytes);
   m->rps2 = pick_rps((size_t)m->H * m->esz);
@@ -561,20 +640,24 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   const size_t Sa = S > 0 ? S : 1;
   if ((st = dev_alloc(m, reinterpret_cast<unsigned char**>(&m->bufs), Sa * m->nproj * K * m->row_bytes)) != NP_OK)
     return fail(st);
-  if ((st = dev_alloc(m, reinterpret_cast<unsigned char**>(&m->staging), (size_t)m->staging_rows * m->rec_bytes)) !=
-      NP_OK)
+  if (m->d.h2d_mode == NP_H2D_STAGED &&
+      (st = dev_alloc(m, reinterpret_cast<unsigned char**>(&m->staging), 2 * (size_t)m->staging_rows * m->rec_bytes)) !=
+          NP_OK)
     return fail(st);
-  if ((st = dev_alloc(m, &m->slotmap, 2 * Sa * F, 0xff)) != NP_OK) return fail(st);
-  if ((st = dev_alloc(m, &m->inv, 2 * Sa * K, 0xff)) != NP_OK) return fail(st);
-  if ((st = dev_alloc(m, &m->content, 2 * Sa * K, 0xff)) != NP_OK) return fail(st);
-  if ((st = dev_alloc(m, &m->resbits, 2 * Sa * m->W)) != NP_OK) return fail(st);
-  if (m->window > 1 && (st = dev_alloc(m, &m->last_seen, 2 * Sa * F)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->slotmap, Sa * F, 0xff)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->inv, Sa * K, 0xff)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->content, Sa * K, 0xff)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->resbits, Sa * m->W)) != NP_OK) return fail(st);
+  if (m->window > 1 && (st = dev_alloc(m, &m->last_seen, Sa * F)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->counts, Sa * 4)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->active, Sa * K)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->active_slot, Sa * K)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->din_n, Sa * K)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->din_s, Sa * K)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->din_oldct, Sa * K)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->dout_n, Sa * K)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->dout_s, Sa * K)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->ls_old, Sa * K)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->totals, 8)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->err, 4)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->z, (size_t)m->B * m->H)) != NP_OK) return fail(st);
@@ -582,16 +665,34 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if ((st = dev_alloc(m, &m->ids, (size_t)m->B * (m->NH > 0 ? m->NH : 1))) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->fire, (size_t)m->W)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->logits, F)) != NP_OK) return fail(st);
-  if ((st = dev_alloc(m, &m->part, (size_t)m->ffn_grid * m->B * m->D)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->part, (size_t)(m->ffn_grid / m->ffn_cluster) * m->B * m->D)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, reinterpret_cast<unsigned char**>(&m->slice_cnt), ffn_counter_bytes())) != NP_OK)
+    return fail(st);
 
   e = cudaEventCreateWithFlags(&m->ev_set, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
   e = cudaEventCreateWithFlags(&m->ev_side_done, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
+  for (int k = 0; k < 3; ++k) {
+    e = cudaEventCreateWithFlags(&m->ev_j[k], cudaEventDisableTiming);
+    if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
+  }
   m->ev_layer.assign(Sa, nullptr);
+  m->ev_g.assign(Sa, nullptr);
   for (size_t s = 0; s < S; ++s) {
     e = cudaEventCreateWithFlags(&m->ev_layer[s], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_g[s], cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
+  }
+  {
+    int lo = 0, hi = 0;
+    cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    // NP_TUNE_SIDE_PRIORITY=0 puts the internal gather/scatter streams at the
+    // default priority instead of the highest
+    const int pr = env_int("NP_TUNE_SIDE_PRIORITY", 1) == 1 ? hi : lo;
+    e = cudaStreamCreateWithPriority(&m->g1, cudaStreamNonBlocking, pr);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&m->xs, cudaStreamNonBlocking, pr);
+    if (e != cudaSuccess) return fail(cuda_fail(e, "cudaStreamCreate"));
   }
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaDeviceSynchronize"));
@@ -603,17 +704,24 @@ np_status np_free_model(np_model* m) {
   if (!m) return NP_OK;
   if (m->main) cudaStreamSynchronize(m->main);
   if (m->side) cudaStreamSynchronize(m->side);
+  if (m->g1) cudaStreamSynchronize(m->g1);
+  if (m->xs) cudaStreamSynchronize(m->xs);
   cudaDeviceSynchronize();
+  if (m->g1) cudaStreamDestroy(m->g1);
+  if (m->xs) cudaStreamDestroy(m->xs);
+  for (cudaEvent_t ev : m->ev_j)
+    if (ev) cudaEventDestroy(ev);
+  for (cudaEvent_t ev : m->ev_g)
+    if (ev) cudaEventDestroy(ev);
   for (void* p : m->allocs) cudaFree(p);
   if (m->ev_set) cudaEventDestroy(m->ev_set);
   if (m->ev_side_done) cudaEventDestroy(m->ev_side_done);
   for (cudaEvent_t ev : m->ev_layer)
     if (ev) cudaEventDestroy(ev);
-  for (auto& v : m->prof_pending)
-    for (auto& p : v) {
-      cudaEventDestroy(p.a);
-      cudaEventDestroy(p.b);
-    }
+  for (auto& t : m->trace) {
+    cudaEventDestroy(t.second.a);
+    cudaEventDestroy(t.second.b);
+  }
   for (auto& p : m->prof_free) {
     cudaEventDestroy(p.a);
     cudaEventDestroy(p.b);
@@ -624,21 +732,22 @@ np_status np_free_model(np_model* m) {
 
 np_status np_reset_sequence(np_model* m) {
   if (!m) return arg_fail("model is null");
+  // a delta that was never scattered already changed the slot contents
+  if (m->pending_bits) NP_TRY(abort_pending(m, std::vector<int>()));
   m->pending_bits = 0;
   m->committed_since_token = 0;
   m->token = 0;
   if (m->S == 0) return NP_OK;
   cudaStream_t st = m->main;
-  CUDA_TRY(cudaStreamWaitEvent(st, m->ev_set, 0));
-  CUDA_TRY(cudaEventRecord(m->ev_side_done, m->side));
-  CUDA_TRY(cudaStreamWaitEvent(st, m->ev_side_done, 0));
+  NP_TRY(join_side(m, st));
   return launch(m, NP_KIND_SET, st, 0, [&] {
-    return launch_reset_state(m->slotmap, m->inv, m->resbits, m->last_seen, m->S, m->F, m->K, m->W, st);
+    return launch_reset_state(m->slotmap, m->inv, m->resbits, m->S, m->F, m->K, m->W, st);
   });
 }
 
 np_status np_predict(np_model* m, int32_t layer, const float* h_dev, void* out_dev) {
   if (!m || !h_dev || !out_dev) return arg_fail("null argument");
+  if (!aligned16(h_dev)) return arg_fail("h_dev must be 16-byte aligned");
   if (m->d.pred_kind == NP_PRED_SHARED_ARGMAX) {
     if (layer != 0) return arg_fail("the shared predictor takes layer 0");
     NP_TRY(enqueue_predict(m, 0, h_dev));
@@ -711,9 +820,13 @@ np_status np_scatter(np_model* m, int32_t layer) {
     g_last_err = "no pending delta";
     return NP_ERR_STATE;
   }
-  NP_TRY(move_layers(m, layers));
-  CUDA_TRY(cudaEventRecord(m->ev_side_done, m->side));
-  CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_side_done, 0));
+  size_t n_moved = 0;
+  const np_status rs = move_layers(m, layers, &n_moved);
+  if (rs != NP_OK) {
+    NP_TRY(abort_pending(m, std::vector<int>(layers.begin(), layers.begin() + n_moved)));
+    return rs;
+  }
+  NP_TRY(join_side(m, m->main));
   uint64_t bits = 0;
   for (int s : layers) bits |= 1ull << s;
   commit(m, bits);
@@ -722,6 +835,7 @@ np_status np_scatter(np_model* m, int32_t layer) {
 
 np_status np_sparse_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_dev) {
   if (!m || !h_dev || !y_dev) return arg_fail("null argument");
+  if (!aligned16(h_dev) || !aligned16(y_dev)) return arg_fail("h_dev and y_dev must be 16-byte aligned");
   if (layer < m->dn || layer >= m->L) return arg_fail("layer is not a sparse layer");
   if (h_dev == y_dev) return arg_fail("y_dev may not alias h_dev");
   return enqueue_sparse(m, layer - m->dn, h_dev, nullptr, y_dev);
@@ -729,6 +843,7 @@ np_status np_sparse_mlp(np_model* m, int32_t layer, const float* h_dev, float* y
 
 np_status np_dense_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_dev) {
   if (!m || !h_dev || !y_dev) return arg_fail("null argument");
+  if (!aligned16(h_dev) || !aligned16(y_dev)) return arg_fail("h_dev and y_dev must be 16-byte aligned");
   if (layer < 0 || layer >= m->dn) return arg_fail("layer is not a dense layer");
   if (h_dev == y_dev) return arg_fail("y_dev may not alias h_dev");
   return enqueue_dense(m, layer, h_dev, nullptr, y_dev);
@@ -736,6 +851,7 @@ np_status np_dense_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_
 
 np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
   if (!m || !h_dev) return arg_fail("null argument");
+  if (!aligned16(h_dev)) return arg_fail("h_dev must be 16-byte aligned");
   if (m->pending_bits) {
     g_last_err = "a delta is pending; call np_scatter first";
     return NP_ERR_STATE;
@@ -745,12 +861,17 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
   for (int l = 0; l < m->dn; ++l) {
     NP_TRY(enqueue_dense(m, l, h_dev, h_dev, nullptr));
     if (l == 0 && shared && m->S > 0) {
-      NP_TRY(enqueue_predict(m, 0, h_dev));
-      NP_TRY(enqueue_set(m, 0, m->S, m->ids, nullptr));
+      NP_TRY(enqueue_predict(m, 0, h_dev, false));
+      NP_TRY(enqueue_set(m, 0, m->S, nullptr, nullptr, m->keys));
       m->pending_bits = all_layers(m);
       std::vector<int> layers(m->S);
       for (int s = 0; s < m->S; ++s) layers[s] = s;
-      NP_TRY(move_layers(m, layers));
+      size_t n_moved = 0;
+      const np_status rs = move_layers(m, layers, &n_moved);
+      if (rs != NP_OK) {
+        NP_TRY(abort_pending(m, std::vector<int>(layers.begin(), layers.begin() + n_moved)));
+        return rs;
+      }
     }
   }
   for (int s = 0; s < m->S; ++s) {
@@ -758,14 +879,14 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
       NP_TRY(enqueue_predict(m, m->dn + s, h_dev));
       NP_TRY(enqueue_set(m, s, 1, nullptr, m->fire));
       m->pending_bits |= 1ull << s;
-      const np_status rs = move_layers(m, std::vector<int>{s});
+      size_t n_moved = 0;
+      const np_status rs = move_layers(m, std::vector<int>{s}, &n_moved);
       if (rs != NP_OK) {
         // earlier layers of this token already hold their new rows: put the
-        // committed contents back and drop the whole token's delta
-        for (int q = 0; q < s; ++q) NP_TRY(enqueue_restore(m, q));
-        m->pending_bits = 0;
-        CUDA_TRY(cudaEventRecord(m->ev_side_done, m->side));
-        CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_side_done, 0));
+        // previous contents back and undo the whole token's delta
+        std::vector<int> moved;
+        for (int q = 0; q < s; ++q) moved.push_back(q);
+        NP_TRY(abort_pending(m, moved));
         return rs;
       }
     }
@@ -774,7 +895,6 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
   }
   if (m->S > 0) {
     m->committed_since_token = 0;
-    m->cur_bits ^= all_layers(m);
     m->pending_bits = 0;
     m->token += 1;
   }
@@ -802,14 +922,15 @@ np_status np_get_state(np_model* m, int32_t layer, int32_t* slotmap_host, int32_
   if (!m) return arg_fail("model is null");
   if (layer < m->dn || layer >= m->L) return arg_fail("layer is not a sparse layer");
   const int s = layer - m->dn;
+  if (m->pending_bits & (1ull << s)) {
+    g_last_err = "a delta is pending for this layer";
+    return NP_ERR_STATE;
+  }
   NP_TRY(sync_model(m));
-  const int cb = (int)((m->cur_bits >> s) & 1ull);
   if (slotmap_host)
-    CUDA_TRY(cudaMemcpy(slotmap_host, m->slotmap + ((size_t)cb * m->S + s) * m->F, sizeof(int) * m->F,
-                        cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemcpy(slotmap_host, m->slotmap + (size_t)s * m->F, sizeof(int) * m->F, cudaMemcpyDeviceToHost));
   if (inv_host)
-    CUDA_TRY(cudaMemcpy(inv_host, m->inv + ((size_t)cb * m->S + s) * m->K, sizeof(int) * m->K,
-                        cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemcpy(inv_host, m->inv + (size_t)s * m->K, sizeof(int) * m->K, cudaMemcpyDeviceToHost));
   return read_device_error(m);
 }
 
@@ -846,7 +967,7 @@ np_status np_set_profiling(np_model* m, int32_t enable) {
 np_status np_get_profile(np_model* m, double* ms_out, int64_t* launches_out, int64_t* bytes_out) {
   if (!m) return arg_fail("model is null");
   NP_TRY(sync_model(m));
-  for (int k = 0; k < NP_N_KINDS; ++k) NP_TRY(prof_fold(m, k, 0));
+  NP_TRY(prof_fold(m, m->trace.size()));
   unsigned long long tot[8] = {};
   CUDA_TRY(cudaMemcpy(tot, m->totals, sizeof(tot), cudaMemcpyDeviceToHost));
   CUDA_TRY(cudaMemset(m->totals, 0, sizeof(tot)));
@@ -868,6 +989,24 @@ np_status np_get_profile(np_model* m, double* ms_out, int64_t* launches_out, int
     m->prof_launches[k] = 0;
     m->prof_fixed_bytes[k] = 0;
   }
+  return NP_OK;
+}
+
+np_status np_get_timeline(np_model* m, int32_t* kinds, float* start_ms, float* end_ms, int32_t max_entries,
+                          int32_t* n_out) {
+  if (!m || !n_out) return arg_fail("null argument");
+  NP_TRY(sync_model(m));
+  const size_t n = m->trace.size() < (size_t)(max_entries > 0 ? max_entries : 0) ? m->trace.size()
+                                                                                  : (size_t)(max_entries > 0 ? max_entries : 0);
+  for (size_t i = 0; i < n; ++i) {
+    float a = 0.f, b = 0.f;
+    CUDA_TRY(cudaEventElapsedTime(&a, m->trace[0].second.a, m->trace[i].second.a));
+    CUDA_TRY(cudaEventElapsedTime(&b, m->trace[0].second.a, m->trace[i].second.b));
+    if (kinds) kinds[i] = m->trace[i].first;
+    if (start_ms) start_ms[i] = a;
+    if (end_ms) end_ms[i] = b;
+  }
+  *n_out = (int32_t)n;
   return NP_OK;
 }
 

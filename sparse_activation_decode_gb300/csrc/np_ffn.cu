@@ -4,224 +4,481 @@
 // neuron of a dense layer):
 //     h_r = relu(g_r . x) * (u_r . x)      (or relu(u_r . x) without a gate)
 //     y  += h_r * d_r
-// with x = rmsnorm(h_in) (NeuroPrefetcher full text, delta runtime: row i of
-// the gate, up and down^T projections serves active neuron i; the ReLU-fied
-// form of the activation).
+// with x = rmsnorm(h_in), then h_out = h_in + y (NeuroPrefetcher full text,
+// delta runtime: row i of the gate, up and down^T projections serves active
+// neuron i; ReLU-fied form of the activation).
 //
-// Design: the kernel is HBM-bound (2 flops per weight element).  Each CTA
-// streams whole rows into shared memory with 1-D bulk copies (TMA engine)
-// through an n_stages-deep ring guarded by mbarriers; one thread issues the
-// copies.  Thread t owns 16-byte column chunks t, t+256, ... of every row and
-// keeps the matching x values and y accumulators in registers, so a row
-// costs one block reduction (for its two dot products) and no reduction for
-// the down projection.  Each CTA writes its partial y; ffn_finish_kernel
-// sums the partials in CTA order (deterministic) and adds the residual.
+// Design (HBM-bound: 2 flops per weight element):
+//  * one CTA per SM, grouped in thread-block clusters; warp-specialized:
+//    warp 8 is the producer, warps 0-7 consume;
+//  * whole neuron records (gate|up|down^T rows) stream into a shared-memory
+//    ring through 1-D bulk copies (TMA engine); a "full" mbarrier per slot
+//    counts the bytes in, an "empty" mbarrier per slot counts the consumer
+//    warps done with it, so the producer refills a slot the moment it frees
+//    up and keeps the whole ring in flight;
+//  * thread t owns 16-byte column chunks t, t+256, ... of every row and keeps
+//    the matching x values and y accumulators in registers; products use
+//    packed FP32x2 FMAs.  Rows are consumed two at a time: the four dot
+//    products of a pair are reduce-scattered across each warp (6 shuffles),
+//    one block barrier combines the warps, and the down projection needs no
+//    reduction at all;
+//  * split-K over CTAs without any grid-wide wait: each CTA parks its
+//    partial y in shared memory, CTA r of a cluster sums column slice r over
+//    the cluster through distributed shared memory and writes one cluster
+//    partial; the last cluster to report slice r (an atomic counter per
+//    slice) sums the cluster partials in cluster order, writes h_out / y_out
+//    and resets the counter.  The summation order is fixed, so the result is
+//    bitwise reproducible.
+#include <cooperative_groups.h>
+
 #include "np_common.cuh"
 #include "np_kernels.h"
 
+namespace cg = cooperative_groups;
+
 namespace np {
 
-template <typename T, bool GATED>
-__global__ void __launch_bounds__(kThreads, 2)
-    ffn_rows_kernel(const float* __restrict__ h_in, const T* __restrict__ w_gate, const T* __restrict__ w_up,
-                    const T* __restrict__ w_down, const int* __restrict__ row_list, const int* __restrict__ n_rows_dev,
-                    int n_rows_host, int list_cap, int row_limit, float* __restrict__ part, int D, int n_stages,
-                    int* err) {
-  constexpr int E = Elem<T>::E;
+constexpr int kFfnThreads = 256;                 // consumer threads
+constexpr int kFfnWarps = kFfnThreads / 32;      // consumer warps
+constexpr int kFfnBlock = kFfnThreads + 32;      // plus one producer warp
+constexpr int kRowCache = 64;                    // row indices cached per CTA
+constexpr int kSliceCols = 16;                      // columns per reduction slice
+constexpr int kSliceGroups = kFfnThreads / kSliceCols;  // partial groups per slice
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
+// 16 bytes of T as E/2 float pairs
+template <typename T> struct Pairs;
+template <> struct Pairs<float> {
+  static constexpr int N = 2;
+  __device__ __forceinline__ static void load(const uint4& v, float2* f) {
+    f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+    f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
+};
+template <> struct Pairs<__half> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const uint4& v, float2* f) {
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = __half22float2(h[i]);
+  }
+};
+template <> struct Pairs<__nv_bfloat16> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const uint4& v, float2* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+  }
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() {  // warps 0-7 only
+  asm volatile("bar.sync 1, %0;" ::"n"(kFfnThreads) : "memory");
+}
+
+// Named barrier over the consumer warps that also ORs a predicate: every
+// consumer thread gets the same answer.
+__device__ __forceinline__ bool consumer_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(kFfnThreads)
+      : "memory");
+  return r != 0;
+}
+
+template <typename T, bool GATED, int MAXC>
+__global__ void __launch_bounds__(kFfnBlock, 1) ffn_rows_kernel(FfnLaunch a) {
+  constexpr int P = Pairs<T>::N;      // float pairs per 16-byte chunk
+  constexpr int E = 2 * P;            // elements per chunk
   constexpr int NPROJ = GATED ? 3 : 2;
+  constexpr int NV = GATED ? 4 : 2;   // dot products per pair of rows
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // up to 16 stages
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // [16]
+  uint64_t* empty = full + 16;                           // [16]
+  int* rows_s = reinterpret_cast<int*>(smem + 256);      // [kRowCache]
+  const int D = a.D, n_slots = a.n_stages;
   const uint32_t row_bytes = (uint32_t)D * sizeof(T);
-  const uint32_t stage_bytes = NPROJ * row_bytes;
-  unsigned char* stages = smem + 128;
-  float* xs = reinterpret_cast<float*>(stages + (size_t)n_stages * stage_bytes);
-  float* red = xs + D;              // [2][8][2] per-row partial dots
-  float* red1 = red + 32;           // [8] rmsnorm scratch
-
+  const uint32_t slot_bytes = NPROJ * row_bytes;
+  unsigned char* ring = smem + 512;
+  float* red = reinterpret_cast<float*>(ring + (size_t)n_slots * slot_bytes);
+  __shared__ int s_abort, s_issued;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int NC = D / E;  // 16-byte chunks per row
+  const int NC = D / E;
 
-  int n = n_rows_dev ? *n_rows_dev : n_rows_host;
-  if (n > list_cap) n = list_cap;
+  int n = a.n_rows_dev ? *a.n_rows_dev : a.n_rows_host;
+  if (n > a.list_cap) n = a.list_cap;
   if (n < 0) n = 0;
-  const int my_n = (n > (int)blockIdx.x) ? (n - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int G = (int)gridDim.x;
+  const int my_n = (n > (int)blockIdx.x) ? (n - 1 - (int)blockIdx.x) / G + 1 : 0;
 
   if (tid == 0) {
-    for (int s = 0; s < n_stages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < n_slots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kFfnWarps);
+    }
     fence_barrier_init();
+    s_abort = 0;
+    s_issued = 0;
   }
+  if (a.row_list)
+    for (int j = tid; j < my_n && j < kRowCache; j += kFfnBlock) rows_s[j] = a.row_list[blockIdx.x + j * G];
   __syncthreads();
 
-  const uint64_t pol = policy_evict_first();
-  auto issue = [&](int j) {
-    const int s = j % n_stages;
-    const int i = (int)blockIdx.x + j * (int)gridDim.x;
-    int r = row_list ? row_list[i] : i;
-    if ((unsigned)r >= (unsigned)row_limit) {
-      atomicExch(err, kDevErrBounds);
-      r = 0;
-    }
-    unsigned char* dst = stages + (size_t)s * stage_bytes;
-    mbar_arrive_expect_tx(&bars[s], stage_bytes);
-    int p = 0;
-    if (GATED) bulk_load(dst + (p++) * row_bytes, w_gate + (size_t)r * D, row_bytes, &bars[s], pol);
-    bulk_load(dst + (p++) * row_bytes, w_up + (size_t)r * D, row_bytes, &bars[s], pol);
-    bulk_load(dst + p * row_bytes, w_down + (size_t)r * D, row_bytes, &bars[s], pol);
-  };
-  if (tid == 0) {
-    const int pre = my_n < n_stages ? my_n : n_stages;
-    for (int j = 0; j < pre; ++j) issue(j);
-  }
+  float2 acc[MAXC][P];
+#pragma unroll
+  for (int k = 0; k < MAXC; ++k)
+#pragma unroll
+    for (int q = 0; q < P; ++q) acc[k][q] = make_float2(0.f, 0.f);
 
-  // x = rmsnorm(h_in) while the first rows stream in.
-  rmsnorm_to_smem(h_in, xs, D, red1);
-  float xr[kMaxChunksPerThread][E];
-  float acc[kMaxChunksPerThread][E];
-#pragma unroll
-  for (int k = 0; k < kMaxChunksPerThread; ++k) {
-    const int c = tid + k * kThreads;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      xr[k][e] = (c < NC) ? xs[c * E + e] : 0.f;
-      acc[k][e] = 0.f;
-    }
-  }
-
-  int issued_upto = my_n < n_stages ? my_n : n_stages;
-  bool aborted = false;
-  for (int j = 0; j < my_n; ++j) {
-    const int s = j % n_stages;
-    const uint32_t parity = (uint32_t)(j / n_stages) & 1u;
-    const bool ok = mbar_wait(&bars[s], parity, err);
-    const uint4* st = reinterpret_cast<const uint4*>(stages + (size_t)s * stage_bytes);
-    const uint4* st_up = st + (GATED ? NC : 0);
-    const uint4* st_dn = st + (GATED ? 2 * NC : NC);
-    float pa = 0.f, pb = 0.f;
-#pragma unroll
-    for (int k = 0; k < kMaxChunksPerThread; ++k) {
-      const int c = tid + k * kThreads;
-      if (c < NC) {
-        float f[E];
-        if (GATED) {
-          Elem<T>::load(st[c], f);
-#pragma unroll
-          for (int e = 0; e < E; ++e) pa = fmaf(f[e], xr[k][e], pa);
-        }
-        Elem<T>::load(st_up[c], f);
-#pragma unroll
-        for (int e = 0; e < E; ++e) pb = fmaf(f[e], xr[k][e], pb);
-      }
-    }
-    if (GATED) pa = warp_sum(pa);
-    pb = warp_sum(pb);
-    float* rb = red + (j & 1) * 16;
+  if (warp == kFfnWarps) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      rb[warp * 2] = pa;
-      rb[warp * 2 + 1] = pb;
+      const uint64_t pol = policy_evict_first();
+      const T* w_gate = static_cast<const T*>(a.w_gate);
+      const T* w_up = static_cast<const T*>(a.w_up);
+      const T* w_down = static_cast<const T*>(a.w_down);
+      for (int j = 0; j < my_n; ++j) {
+        const int s = j % n_slots;
+        if (j >= n_slots && !mbar_wait(&empty[s], (uint32_t)(j / n_slots - 1) & 1u, a.err)) {
+          s_abort = 1;
+          break;
+        }
+        int r = a.row_list ? (j < kRowCache ? rows_s[j] : a.row_list[blockIdx.x + j * G]) : (int)blockIdx.x + j * G;
+        if ((unsigned)r >= (unsigned)a.row_limit) {
+          atomicExch(a.err, kDevErrBounds);
+          r = 0;
+        }
+        unsigned char* dst = ring + (size_t)s * slot_bytes;
+        mbar_arrive_expect_tx(&full[s], slot_bytes);
+        int p = 0;
+        if (GATED) bulk_load(dst + (p++) * row_bytes, w_gate + (size_t)r * D, row_bytes, &full[s], pol);
+        bulk_load(dst + (p++) * row_bytes, w_up + (size_t)r * D, row_bytes, &full[s], pol);
+        bulk_load(dst + p * row_bytes, w_down + (size_t)r * D, row_bytes, &full[s], pol);
+        s_issued = j + 1;
+      }
     }
-    if (__syncthreads_or(!ok)) {  // uniform: every thread leaves together
-      aborted = true;
-      break;
-    }
-    // every thread is past row j-1: its stage can be refilled
-    if (tid == 0 && j >= 1 && j - 1 + n_stages < my_n) {
-      issue(j - 1 + n_stages);
-      ++issued_upto;
-    }
-    float a = 0.f, b = 0.f;
+  } else {
+    // ------------------------------------------------------------ consumers
+    // x = rmsnorm(h_in): each thread reads its own chunks of h.
+    float2 xr[MAXC][P];
+    float ss = 0.f;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
-      a += rb[w * 2];
-      b += rb[w * 2 + 1];
+    for (int k = 0; k < MAXC; ++k) {
+      const int c = tid + k * kFfnThreads;
+#pragma unroll
+      for (int q = 0; q < P; ++q) {
+        float2 v = make_float2(0.f, 0.f);
+        if (c < NC) v = *reinterpret_cast<const float2*>(a.h_in + c * E + 2 * q);
+        xr[k][q] = v;
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, ss));
+      }
     }
-    const float hv = GATED ? (a > 0.f ? a : 0.f) * b : (b > 0.f ? b : 0.f);
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    consumer_sync();
+    float tot = 0.f;
 #pragma unroll
-    for (int k = 0; k < kMaxChunksPerThread; ++k) {
-      const int c = tid + k * kThreads;
-      if (c < NC) {
-        float f[E];
-        Elem<T>::load(st_dn[c], f);
+    for (int w = 0; w < kFfnWarps; ++w) tot += red[w];
+    const float inv = rsqrtf(tot / (float)D + 1e-6f);
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[k][e] = fmaf(hv, f[e], acc[k][e]);
+    for (int k = 0; k < MAXC; ++k)
+#pragma unroll
+      for (int q = 0; q < P; ++q) {
+        xr[k][q].x *= inv;
+        xr[k][q].y *= inv;
+      }
+    consumer_sync();  // red is reused below
+
+    for (int j = 0; j < my_n; j += 2) {
+      const bool two = j + 1 < my_n;
+      const int s0 = j % n_slots, s1 = (j + 1) % n_slots;
+      bool ok = mbar_wait(&full[s0], (uint32_t)(j / n_slots) & 1u, a.err);
+      if (two) ok = mbar_wait(&full[s1], (uint32_t)((j + 1) / n_slots) & 1u, a.err) && ok;
+      const uint4* r0 = reinterpret_cast<const uint4*>(ring + (size_t)s0 * slot_bytes);
+      const uint4* r1 = reinterpret_cast<const uint4*>(ring + (size_t)s1 * slot_bytes);
+      float2 d2[NV];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) d2[v] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < MAXC; ++k) {
+        const int c = tid + k * kFfnThreads;
+        if (c < NC) {
+          float2 f[P];
+#pragma unroll
+          for (int row = 0; row < 2; ++row) {
+            if (row == 1 && !two) break;
+            const uint4* rr = row ? r1 : r0;
+            if (GATED) {
+              Pairs<T>::load(rr[c], f);
+#pragma unroll
+              for (int q = 0; q < P; ++q) d2[row * 2] = ffma2(f[q], xr[k][q], d2[row * 2]);
+              Pairs<T>::load(rr[NC + c], f);
+#pragma unroll
+              for (int q = 0; q < P; ++q) d2[row * 2 + 1] = ffma2(f[q], xr[k][q], d2[row * 2 + 1]);
+            } else {
+              Pairs<T>::load(rr[c], f);
+#pragma unroll
+              for (int q = 0; q < P; ++q) d2[row] = ffma2(f[q], xr[k][q], d2[row]);
+            }
+          }
+        }
+      }
+      // warp reduce-scatter: lane l ends with the warp sum of value vi(l)
+      float pv[NV];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) pv[v] = d2[v].x + d2[v].y;
+      int cnt = NV, vi = 0;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        if (cnt > 1) {
+          const bool up = (lane & off) != 0;
+          const int half = cnt >> 1;
+#pragma unroll
+          for (int q = 0; q < NV / 2; ++q) {
+            if (q < half) {
+              const float send = up ? pv[q] : pv[q + half];
+              const float keep = up ? pv[q + half] : pv[q];
+              pv[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+          }
+          vi = vi * 2 + (up ? 1 : 0);
+          cnt = half;
+        } else {
+          pv[0] += __shfl_xor_sync(0xffffffffu, pv[0], off);
+        }
+      }
+      float* rb = red + ((j >> 1) & 1) * kFfnWarps * NV;
+      if ((lane & (32 / NV - 1)) == 0) rb[warp * NV + vi] = pv[0];
+      if (consumer_sync_or(!ok)) {  // a copy never arrived: all consumers stop
+        if (tid == 0) s_abort = 1;
+        break;
+      }
+      float t[NV];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) t[v] = 0.f;
+#pragma unroll
+      for (int w = 0; w < kFfnWarps; ++w) {
+        if (NV == 4) {
+          const float4 x4 = reinterpret_cast<const float4*>(rb)[w];
+          t[0] += x4.x; t[1] += x4.y; t[2 % NV] += x4.z; t[3 % NV] += x4.w;
+        } else {
+          const float2 x2 = reinterpret_cast<const float2*>(rb)[w];
+          t[0] += x2.x; t[1] += x2.y;
+        }
+      }
+      float hv0, hv1;
+      if (GATED) {
+        hv0 = (t[0] > 0.f ? t[0] : 0.f) * t[1];
+        hv1 = (t[2 % NV] > 0.f ? t[2 % NV] : 0.f) * t[3 % NV];
+      } else {
+        hv0 = t[0] > 0.f ? t[0] : 0.f;
+        hv1 = t[1] > 0.f ? t[1] : 0.f;
+      }
+      const float2 h0 = make_float2(hv0, hv0), h1 = make_float2(hv1, hv1);
+      const int dn = (NPROJ - 1) * NC;
+#pragma unroll
+      for (int k = 0; k < MAXC; ++k) {
+        const int c = tid + k * kFfnThreads;
+        if (c < NC) {
+          float2 f[P];
+          Pairs<T>::load(r0[dn + c], f);
+#pragma unroll
+          for (int q = 0; q < P; ++q) acc[k][q] = ffma2(h0, f[q], acc[k][q]);
+          if (two) {
+            Pairs<T>::load(r1[dn + c], f);
+#pragma unroll
+            for (int q = 0; q < P; ++q) acc[k][q] = ffma2(h1, f[q], acc[k][q]);
+          }
+        }
+      }
+      // this warp is done with both slots
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&empty[s0]);
+        if (two) mbar_arrive(&empty[s1]);
       }
     }
   }
-  if (aborted && tid == 0) {
+  __syncthreads();
+  if (s_abort && tid == kFfnThreads) {
     // drain copies still in flight before the CTA's shared memory goes away
-    const int first = issued_upto > n_stages ? issued_upto - n_stages : 0;
-    for (int j = first; j < issued_upto; ++j) mbar_wait(&bars[j % n_stages], (uint32_t)(j / n_stages) & 1u, nullptr);
+    atomicExch(a.err, kDevErrTimeout);
+    const int issued = s_issued;
+    const int first = issued > n_slots ? issued - n_slots : 0;
+    for (int j = first; j < issued; ++j) mbar_wait(&full[j % n_slots], (uint32_t)(j / n_slots) & 1u, nullptr);
   }
 
-  float* out = part + (size_t)blockIdx.x * D;
+  // ---- split-K: cluster reduction in distributed shared memory, then the
+  // last cluster per column slice
+  cg::cluster_group cl = cg::this_cluster();
+  const int CS = (int)cl.num_blocks();
+  const int crank = (int)cl.block_rank();
+  const int cid = (int)blockIdx.x / CS;
+  const int ncl = (int)gridDim.x / CS;
+  float* mine = reinterpret_cast<float*>(ring);  // every copy has landed: reuse the ring
 #pragma unroll
-  for (int k = 0; k < kMaxChunksPerThread; ++k) {
-    const int c = tid + k * kThreads;
-    if (c < NC) {
+  for (int k = 0; k < MAXC; ++k) {
+    const int c = tid + k * kFfnThreads;
+    if (tid < kFfnThreads && c < NC) {
 #pragma unroll
-      for (int e = 0; e < E; e += 4)
-        *reinterpret_cast<float4*>(out + c * E + e) = make_float4(acc[k][e], acc[k][e + 1], acc[k][e + 2], acc[k][e + 3]);
+      for (int q = 0; q < P; q += 2)
+        *reinterpret_cast<float4*>(mine + c * E + 2 * q) =
+            make_float4(acc[k][q].x, acc[k][q].y, acc[k][q + 1].x, acc[k][q + 1].y);
     }
   }
-}
-
-// y[j] = sum over CTAs b (in order) of part[b][j]; h_out = h_in + y; y_out = y.
-// Block: 256 threads = 8 warps over 32 columns; warp w sums partials w, w+8, ...
-__global__ void __launch_bounds__(256) ffn_finish_kernel(const float* __restrict__ part, int n_part, int D,
-                                                         const float* h_in, float* h_out, float* y_out) {
-  __shared__ float s[8][33];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int j = blockIdx.x * 32 + lane;
-  float v = 0.f;
-  if (j < D)
-    for (int b = warp; b < n_part; b += 8) v += part[(size_t)b * D + j];
-  s[warp][lane] = v;
+  cl.sync();
+  const int slice = (((D + CS - 1) / CS) + 3) & ~3;
+  const int lo = crank * slice;
+  const int hi = lo + slice < D ? lo + slice : D;
+  float* cpart = a.part + (size_t)cid * D;
+  for (int j = lo + tid * 4; j < hi; j += kFfnBlock * 4) {
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < CS; ++r) {
+      const float4 v = *reinterpret_cast<const float4*>(cl.map_shared_rank(mine, r) + j);
+      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+    }
+    *reinterpret_cast<float4*>(cpart + j) = sum;
+  }
+  cl.sync();  // no CTA leaves while its shared memory is being read
+  __threadfence();
   __syncthreads();
-  if (warp == 0 && j < D) {
-    float y = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) y += s[w][lane];
-    if (y_out) y_out[j] = y;
-    if (h_out) h_out[j] = h_in[j] + y;
+  __shared__ int s_last;
+  if (tid == 0) s_last = atomicAdd(&a.slice_cnt[crank], 1) == ncl - 1;
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    for (int j = lo + tid * 4; j < hi; j += kFfnBlock * 4) {
+      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+      int c = 0;
+      for (; c + 3 < ncl; c += 4) {  // four loads in flight, summed in cluster order
+        const float4 v0 = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)c * D + j));
+        const float4 v1 = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)(c + 1) * D + j));
+        const float4 v2 = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)(c + 2) * D + j));
+        const float4 v3 = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)(c + 3) * D + j));
+        y.x += v0.x; y.y += v0.y; y.z += v0.z; y.w += v0.w;
+        y.x += v1.x; y.y += v1.y; y.z += v1.z; y.w += v1.w;
+        y.x += v2.x; y.y += v2.y; y.z += v2.z; y.w += v2.w;
+        y.x += v3.x; y.y += v3.y; y.z += v3.z; y.w += v3.w;
+      }
+      for (; c < ncl; ++c) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)c * D + j));
+        y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+      }
+      if (a.y_out) *reinterpret_cast<float4*>(a.y_out + j) = y;
+      if (a.h_out) {
+        const float4 h = *reinterpret_cast<const float4*>(a.h_in + j);
+        *reinterpret_cast<float4*>(a.h_out + j) = make_float4(h.x + y.x, h.y + y.y, h.z + y.z, h.w + y.w);
+      }
+    }
+    if (tid == 0) a.slice_cnt[crank] = 0;
   }
 }
 
 template <typename T, bool GATED>
-static cudaError_t launch_rows_t(const FfnLaunch& a, cudaStream_t st) {
-  const size_t smem = ffn_smem_bytes(a.D, a.dtype_bytes, GATED ? 3 : 2, a.n_stages);
-  auto kern = ffn_rows_kernel<T, GATED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  kern<<<a.grid, kThreads, smem, st>>>(a.h_in, (const T*)a.w_gate, (const T*)a.w_up, (const T*)a.w_down, a.row_list,
-                                       a.n_rows_dev, a.n_rows_host, a.list_cap, a.row_limit, a.part, a.D, a.n_stages,
-                                       a.err);
-  return cudaGetLastError();
+static void* kernel_for(int maxc) {
+  switch (maxc) {
+    case 1: return reinterpret_cast<void*>(ffn_rows_kernel<T, GATED, 1>);
+    case 2: return reinterpret_cast<void*>(ffn_rows_kernel<T, GATED, 2>);
+    case 3: return reinterpret_cast<void*>(ffn_rows_kernel<T, GATED, 3>);
+    default: return reinterpret_cast<void*>(ffn_rows_kernel<T, GATED, 4>);
+  }
+}
+
+static int chunks_per_thread(int D, int dtype_bytes) {
+  const int nc = D * dtype_bytes / 16;
+  return (nc + kFfnThreads - 1) / kFfnThreads;
+}
+
+static void* pick_kernel(int dtype, bool gated, int D, int dtype_bytes) {
+  const int mc = chunks_per_thread(D, dtype_bytes);
+  if (gated) return dtype == 0 ? kernel_for<float, true>(mc) : dtype == 1 ? kernel_for<__half, true>(mc)
+                                                                         : kernel_for<__nv_bfloat16, true>(mc);
+  return dtype == 0 ? kernel_for<float, false>(mc) : dtype == 1 ? kernel_for<__half, false>(mc)
+                                                               : kernel_for<__nv_bfloat16, false>(mc);
 }
 
 size_t ffn_smem_bytes(int D, int dtype_bytes, int nproj, int n_stages) {
-  return 128 + (size_t)n_stages * nproj * D * dtype_bytes + (size_t)D * 4 + 64 * 4;
+  size_t ring = (size_t)n_stages * nproj * D * dtype_bytes;
+  if (ring < (size_t)D * 4) ring = (size_t)D * 4;  // the ring also parks the partial y
+  return 512 + ring + 64 * 4;
 }
 
-int ffn_pick_stages(int D, int dtype_bytes, int nproj, size_t smem_limit) {
-  int ns = 8;
-  while (ns > 2 && ffn_smem_bytes(D, dtype_bytes, nproj, ns) > smem_limit) --ns;
-  return ffn_smem_bytes(D, dtype_bytes, nproj, ns) <= smem_limit ? ns : 0;
+int ffn_max_chunks() { return kFfnThreads * 4; }
+size_t ffn_counter_bytes() { return 16 * sizeof(int); }
+
+cudaError_t ffn_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_optin, int n_sms, int* n_stages,
+                     int* cluster, int* grid) {
+  const int nproj = gated ? 3 : 2;
+  int ns = 16;  // one CTA per SM with as many ring slots (4..16) as fit
+  while (ns > 4 && ffn_smem_bytes(D, dtype_bytes, nproj, ns) > smem_optin) --ns;
+  if (ffn_smem_bytes(D, dtype_bytes, nproj, ns) > smem_optin) return cudaErrorInvalidValue;
+  void* k = pick_kernel(dtype, gated != 0, D, dtype_bytes);
+  const size_t smem = ffn_smem_bytes(D, dtype_bytes, nproj, ns);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  // the largest cluster that still keeps (nearly) every SM busy
+  int best_cs = 1, best_ctas = 0;
+  for (int cs : {8, 4, 2}) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs * ((n_sms + cs - 1) / cs), 1, 1);
+    cfg.blockDim = dim3(kFfnBlock, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = cs;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n * cs > best_ctas + n_sms / 16) {  // prefer larger clusters unless they idle >6% of SMs
+      best_ctas = n * cs;
+      best_cs = cs;
+    }
+  }
+  if (best_ctas == 0) return cudaErrorInvalidConfiguration;
+  *n_stages = ns;
+  *cluster = best_cs;
+  *grid = best_ctas;
+  return cudaSuccess;
 }
 
 cudaError_t launch_ffn_rows(const FfnLaunch& a, cudaStream_t st) {
-  if (a.gated) {
-    if (a.dtype == 0) return launch_rows_t<float, true>(a, st);
-    if (a.dtype == 1) return launch_rows_t<__half, true>(a, st);
-    return launch_rows_t<__nv_bfloat16, true>(a, st);
-  }
-  if (a.dtype == 0) return launch_rows_t<float, false>(a, st);
-  if (a.dtype == 1) return launch_rows_t<__half, false>(a, st);
-  return launch_rows_t<__nv_bfloat16, false>(a, st);
-}
-
-cudaError_t launch_ffn_finish(const float* part, int n_part, int D, const float* h_in, float* h_out, float* y_out,
-                              cudaStream_t st) {
-  ffn_finish_kernel<<<(D + 31) / 32, 256, 0, st>>>(part, n_part, D, h_in, h_out, y_out);
-  return cudaGetLastError();
+  void* k = pick_kernel(a.dtype, a.gated != 0, a.D, a.dtype_bytes);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid, 1, 1);
+  cfg.blockDim = dim3(kFfnBlock, 1, 1);
+  cfg.dynamicSmemBytes = ffn_smem_bytes(a.D, a.dtype_bytes, a.gated ? 3 : 2, a.n_stages);
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = a.cluster;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  FfnLaunch arg = a;
+  void* params[] = {&arg};
+  return cudaLaunchKernelExC(&cfg, k, params);
 }
 
 }  // namespace np

@@ -25,7 +25,11 @@ struct FfnLaunch {
   int n_rows_host;
   int list_cap;           // capacity of row_list (upper bound of the count)
   int row_limit;          // rows present in the weight buffers
-  float* part;            // [grid][D] per-CTA partial y
+  float* part;            // [grid / cluster][D] cluster partial sums
+  int* slice_cnt;         // [cluster] arrival counters, zero between launches
+  int cluster;            // CTAs per thread-block cluster (grid % cluster == 0)
+  float* h_out;           // h_in + y (may alias h_in), or null
+  float* y_out;           // y, or null
   int D;
   int dtype;              // 0 f32, 1 f16, 2 bf16
   int dtype_bytes;
@@ -35,10 +39,12 @@ struct FfnLaunch {
   int* err;
 };
 size_t ffn_smem_bytes(int D, int dtype_bytes, int nproj, int n_stages);
-int ffn_pick_stages(int D, int dtype_bytes, int nproj, size_t smem_limit);
+// Ring depth, cluster size and grid (one CTA per SM) of the FFN launch.
+cudaError_t ffn_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_optin, int n_sms, int* n_stages,
+                     int* cluster, int* grid);
+int ffn_max_chunks();        // 16-byte chunks per row the FFN supports
+size_t ffn_counter_bytes();  // bytes of slice-counter state
 cudaError_t launch_ffn_rows(const FfnLaunch& a, cudaStream_t st);
-cudaError_t launch_ffn_finish(const float* part, int n_part, int D, const float* h_in, float* h_out, float* y_out,
-                              cudaStream_t st);
 
 // ---- row dot products: predictor layers (np_pred.cu) ----------------------
 // out mode: 0 = relu(dot) -> out_f[row]; 1 = argmax key per head of C rows;
@@ -79,30 +85,35 @@ struct SetLaunch {
   int batch;
   int n_heads;
   int token;
-  const int* ids;         // [batch][n_heads] or null (fire mask mode)
+  const int* ids;         // [batch][n_heads] or null
+  const unsigned long long* keys;  // packed argmax keys [batch][n_heads] (used if ids null)
+  int* ids_out;           // with keys: CTA 0 also writes the decoded IDs here
   const uint32_t* fire;   // [n_layers_launch][words] or null
   const uint32_t* centroids;  // [S][2][C][words]
-  uint64_t cur_bits;      // bit s: committed state lives in buffer 1 (else 0)
-  // double-buffered state, each [2][S][...]
-  int* slotmap;           // [2][S][F]
-  int* inv;               // [2][S][K]
-  int* content;           // [2][S][K]
-  uint32_t* resbits;      // [2][S][words]
-  int* last_seen;         // [2][S][F] (window > 1)
+  // decode state, updated in place: [S][...]
+  int* slotmap;           // [S][F] slot of each neuron or -1
+  int* inv;               // [S][K] neuron in each slot or -1
+  int* content;           // [S][K] neuron whose rows the slot's bytes hold or -1
+  uint32_t* resbits;      // [S][words] resident set
+  int* last_seen;         // [S][F] last active token (window > 1)
   int S;
-  // outputs [S][...]
+  // delta lists [S][...]
   int* counts;            // [S][4]
   int* active;            // [S][K]
   int* active_slot;       // [S][K]
   int* din_n;             // [S][K]
   int* din_s;             // [S][K]
+  int* din_oldct;         // [S][K] previous content of each incoming slot
   int* dout_n;            // [S][K]
+  int* dout_s;            // [S][K] slot each outgoing neuron held
+  int* ls_old;            // [S][K] previous last use of each active neuron
   unsigned long long* totals;  // running sums: |A|, |D_in|, |D_out|, dropped
   int* err;
 };
 cudaError_t launch_set(const SetLaunch& a, cudaStream_t st);
-cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int* last_seen, int S, int F, int K,
-                               int words, cudaStream_t st);
+cudaError_t launch_rollback(const SetLaunch& a, cudaStream_t st);  // undo launch_set from its lists
+cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int S, int F, int K, int words,
+                               cudaStream_t st);
 
 // ---- host-link gather and deinterleave-scatter (np_scatter.cu) -----------
 struct MoveLaunch {
@@ -119,7 +130,7 @@ struct MoveLaunch {
   int chunk_cap;
   void* staging;            // [chunk_cap][rec_vec] device
   void* bufs_layer;         // [n_proj][K][row_vec] device
-  const int* content_old;   // restore: neuron whose bytes were in each slot (-1: zero)
+  const int* din_oldct;     // restore: neuron whose bytes each incoming slot held (-1: zero)
   int grid;
   int* err;
 };

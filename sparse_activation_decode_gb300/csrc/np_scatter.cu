@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kMoveThreads) fused_kernel(MoveLaunch a) {
 }
 
 // Put back what the assigned slots held before this delta: the record of
-// content_old[slot], or zeros for a slot that never held a row.
+// din_oldct[i], or zeros for a slot that never held a row.
 __global__ void __launch_bounds__(kMoveThreads) restore_kernel(MoveLaunch a) {
   const int end = chunk_end(a);
   const uint4* store = static_cast<const uint4*>(a.store_layer);
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kMoveThreads) restore_kernel(MoveLaunch a) {
   for (int i = a.chunk_begin + blockIdx.x; i < end; i += gridDim.x) {
     const int slot = a.din_s[i];
     if ((unsigned)slot >= (unsigned)a.K) continue;
-    const int n = a.content_old[slot];
+    const int n = a.din_oldct[i];
     for (int p = 0; p < a.n_proj; ++p) {
       uint4* dst = bufs + ((size_t)p * a.K + slot) * a.row_vec;
       if ((unsigned)n < (unsigned)a.F) {

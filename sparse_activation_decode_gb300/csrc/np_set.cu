@@ -14,9 +14,14 @@
 //     use first (ties: lowest ID first) while more than K_max remain.
 //  4. D_in = A \ R_prev, D_out = R_prev \ R_next.  Slots of R_prev ∩ R_next
 //     stay; the free slots in ascending order go to D_in in ascending ID
-//     order.  New slot map, inverse map and slot contents are written to the
-//     other half of the double-buffered state, which becomes the committed
-//     state once the rows have been scattered.
+//     order.
+//
+// The state (slot map S, inverse map inv, slot contents, resident bitmask,
+// last use) is updated in place and only where it changes; every value
+// overwritten is recorded in the delta lists so that rollback_kernel can put
+// the previous state back if the incoming rows cannot be read.  Slots are
+// derived from the inverse map (one coalesced pass over the K slots), so the
+// F-long slot map is only written, never read.
 #include "np_common.cuh"
 #include "np_kernels.h"
 
@@ -24,6 +29,7 @@ namespace np {
 
 constexpr int kSetThreads = 512;
 constexpr int kMaxKmax = 8192;
+constexpr int kMaxWords = kSetThreads;
 
 // Exclusive prefix sum of v over the 512-thread block; *total = sum.
 __device__ __forceinline__ int block_scan(int v, int* wsum, int* total) {
@@ -62,41 +68,63 @@ __device__ __forceinline__ uint32_t lowest_bits(uint32_t w, int m) {
   return r;
 }
 
+// rank of neuron n among the set bits of `words` (per-word exclusive counts in excl)
+__device__ __forceinline__ int bit_rank(const uint32_t* words, const int* excl, int n) {
+  const int w = n >> 5;
+  return excl[w] + __popc(words[w] & ((1u << (n & 31)) - 1u));
+}
+
 __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   __shared__ int wsum[32];
   __shared__ uint32_t occ[kMaxKmax / 32];
-  __shared__ int free_list[kMaxKmax];
   __shared__ int hist[33];
   __shared__ int cut_age, cut_need;
+  __shared__ uint32_t s_a[kMaxWords], s_out[kMaxWords], s_keep[kMaxWords];
+  __shared__ int s_ea[kMaxWords], s_eout[kMaxWords];
+  extern __shared__ int free_list[];  // [K]
 
   const int tid = threadIdx.x;
   const int s = a.first_sparse + blockIdx.x;
   const int layer = a.n_dense + s;
   const int F = a.F, K = a.K, W = a.words;
-  const int pb = (int)((a.cur_bits >> s) & 1ull), nb = pb ^ 1;
-  const size_t S = a.S;
-  const int* sm_prev = a.slotmap + ((size_t)pb * S + s) * F;
-  int* sm_next = a.slotmap + ((size_t)nb * S + s) * F;
-  int* inv_next = a.inv + ((size_t)nb * S + s) * K;
-  const int* ct_prev = a.content + ((size_t)pb * S + s) * K;
-  int* ct_next = a.content + ((size_t)nb * S + s) * K;
-  const uint32_t* res_prev = a.resbits + ((size_t)pb * S + s) * W;
-  uint32_t* res_next = a.resbits + ((size_t)nb * S + s) * W;
-  const int* ls_prev = a.window > 1 ? a.last_seen + ((size_t)pb * S + s) * F : nullptr;
-  int* ls_next = a.window > 1 ? a.last_seen + ((size_t)nb * S + s) * F : nullptr;
+  int* __restrict__ S = a.slotmap + (size_t)s * F;
+  int* __restrict__ inv = a.inv + (size_t)s * K;
+  int* __restrict__ ct = a.content + (size_t)s * K;
+  uint32_t* __restrict__ res = a.resbits + (size_t)s * W;
+  int* __restrict__ ls = a.window > 1 ? a.last_seen + (size_t)s * F : nullptr;
+  int* __restrict__ out_a = a.active + (size_t)s * K;
+  int* __restrict__ out_as = a.active_slot + (size_t)s * K;
+  int* __restrict__ out_in = a.din_n + (size_t)s * K;
+  int* __restrict__ out_ins = a.din_s + (size_t)s * K;
+  int* __restrict__ out_inct = a.din_oldct + (size_t)s * K;
+  int* __restrict__ out_out = a.dout_n + (size_t)s * K;
+  int* __restrict__ out_outs = a.dout_s + (size_t)s * K;
+  int* __restrict__ out_lsold = a.ls_old + (size_t)s * K;
+
+  if (a.keys && a.ids_out && blockIdx.x == 0)
+    for (int h = tid; h < a.batch * a.n_heads; h += kSetThreads)
+      a.ids_out[h] = (int)(0xFFFFFFFFu - (uint32_t)(a.keys[h] & 0xFFFFFFFFull));
 
   const int i = tid;
   const bool has_word = i < W;
   const uint32_t word_mask =
       (has_word && i == W - 1 && (F & 31)) ? ((1u << (F & 31)) - 1u) : (has_word ? 0xffffffffu : 0u);
 
-  // 1. active set words
+  // 1. active set words and resident words
   uint32_t aw = 0;
+  const uint32_t rw = has_word ? res[i] : 0u;
   if (has_word) {
-    if (a.ids) {
+    if (a.ids || a.keys) {
       for (int b = 0; b < a.batch; ++b) {
-        int ig = a.ids[b * a.n_heads + 2 * (layer - 1)];
-        int iu = a.ids[b * a.n_heads + 2 * (layer - 1) + 1];
+        const int hg = b * a.n_heads + 2 * (layer - 1);
+        int ig, iu;
+        if (a.keys) {  // packed argmax keys: low word = ~centroid index
+          ig = (int)(0xFFFFFFFFu - (uint32_t)(a.keys[hg] & 0xFFFFFFFFull));
+          iu = (int)(0xFFFFFFFFu - (uint32_t)(a.keys[hg + 1] & 0xFFFFFFFFull));
+        } else {
+          ig = a.ids[hg];
+          iu = a.ids[hg + 1];
+        }
         if ((unsigned)ig >= (unsigned)a.C || (unsigned)iu >= (unsigned)a.C) {
           atomicExch(a.err, kDevErrBounds);
           ig = iu = 0;
@@ -113,7 +141,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
 
   // 2. cap to the K lowest IDs
   int total;
-  int excl = block_scan(__popc(aw), wsum, &total);
+  const int excl = block_scan(__popc(aw), wsum, &total);
   const int dropped = total > K ? total - K : 0;
   if (total > K) {
     if (excl >= K) aw = 0;
@@ -121,17 +149,14 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   }
 
   // 3. resident set after this token
-  const uint32_t rw = has_word ? res_prev[i] : 0u;
   uint32_t nw = aw;
   if (a.window > 1) {
-    // candidates: A plus resident neurons used within the window
-    uint32_t old = rw & ~aw;  // resident, not active now
+    const uint32_t old = rw & ~aw;  // resident, not active now
     uint32_t keep_old = 0;
     for (uint32_t w = old; w;) {
       const int b = __ffs(w) - 1;
       w &= w - 1;
-      const int n = i * 32 + b;
-      const int age = a.token - ls_prev[n];
+      const int age = a.token - ls[i * 32 + b];
       if (age >= 0 && age < a.window) keep_old |= 1u << b;
     }
     uint32_t cand = aw | keep_old;
@@ -143,7 +168,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
       for (uint32_t w = keep_old; w;) {
         const int b = __ffs(w) - 1;
         w &= w - 1;
-        atomicAdd(&hist[a.token - ls_prev[i * 32 + b]], 1);
+        atomicAdd(&hist[a.token - ls[i * 32 + b]], 1);
       }
       __syncthreads();
       if (tid == 0) {
@@ -152,7 +177,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
           excess -= hist[age];
           --age;
         }
-        cut_age = age;    // evict all older than age, and `excess` lowest IDs of age
+        cut_age = age;  // evict all older than age, and `excess` lowest IDs of age
         cut_need = excess;
       }
       __syncthreads();
@@ -160,7 +185,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
       for (uint32_t w = keep_old; w;) {
         const int b = __ffs(w) - 1;
         w &= w - 1;
-        const int age = a.token - ls_prev[i * 32 + b];
+        const int age = a.token - ls[i * 32 + b];
         if (age > cut_age) older |= 1u << b;
         else if (age == cut_age) bucket |= 1u << b;
       }
@@ -174,17 +199,18 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   }
   const uint32_t dinw = aw & ~rw;
   const uint32_t doutw = rw & ~nw;
-  const uint32_t keptw = rw & nw;
 
-  // 4. compact A, D_in, D_out (ascending IDs)
+  // 4. ranks within A, D_in, D_out; the lists in ascending ID order
   int n_a, n_in, n_out;
   const int ea = block_scan(__popc(aw), wsum, &n_a);
   const int ein = block_scan(__popc(dinw), wsum, &n_in);
   const int eout = block_scan(__popc(doutw), wsum, &n_out);
-  int* out_a = a.active + (size_t)s * K;
-  int* out_in = a.din_n + (size_t)s * K;
-  int* out_out = a.dout_n + (size_t)s * K;
-  {
+  if (has_word) {
+    s_a[i] = aw;
+    s_out[i] = doutw;
+    s_keep[i] = rw & nw;
+    s_ea[i] = ea;
+    s_eout[i] = eout;
     int p = ea;
     for (uint32_t w = aw; w; w &= w - 1) out_a[p++] = i * 32 + __ffs(w) - 1;
     p = ein;
@@ -192,21 +218,26 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     p = eout;
     for (uint32_t w = doutw; w; w &= w - 1) out_out[p++] = i * 32 + __ffs(w) - 1;
   }
-
-  // 5. free slots = [0, K) minus the slots of kept neurons, ascending
   const int KW = (K + 31) / 32;
   if (tid < KW) occ[tid] = 0u;
   __syncthreads();
-  for (uint32_t w = keptw; w; w &= w - 1) {
-    const int n = i * 32 + __ffs(w) - 1;
-    const int slot = sm_prev[n];
-    if ((unsigned)slot >= (unsigned)K) {
-      atomicExch(a.err, kDevErrBounds);
-      continue;
+
+  // 5. one pass over the slots: occupied = holds a neuron that stays;
+  //    kept active neurons get their slot, outgoing neurons record theirs
+  for (int k = tid; k < K; k += kSetThreads) {
+    const int n = inv[k];
+    if ((unsigned)n >= (unsigned)F) continue;
+    const uint32_t bit = 1u << (n & 31);
+    const int w = n >> 5;
+    if (s_out[w] & bit) {
+      out_outs[bit_rank(s_out, s_eout, n)] = k;
+    } else if (s_keep[w] & bit) {
+      atomicOr(&occ[k >> 5], 1u << (k & 31));
+      if (s_a[w] & bit) out_as[bit_rank(s_a, s_ea, n)] = k;
     }
-    atomicOr(&occ[slot >> 5], 1u << (slot & 31));
   }
   __syncthreads();
+  // free slots in ascending order
   uint32_t fw = 0;
   if (tid < KW) {
     fw = ~occ[tid];
@@ -221,67 +252,32 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   __syncthreads();
   if (n_in > n_free && tid == 0) atomicExch(a.err, kDevErrBounds);
 
-  // 6. slot map of the next state; D_in slots
-  int* out_ins = a.din_s + (size_t)s * K;
-  if (has_word) {
-    for (int b = 0; b < 32; ++b) {
-      const int n = i * 32 + b;
-      if (n >= F) break;
-      const uint32_t bit = 1u << b;
-      int v = -1;
-      if (keptw & bit) {
-        v = sm_prev[n];
-      } else if (dinw & bit) {
-        const int r = ein + __popc(dinw & (bit - 1u));
-        v = r < n_free ? free_list[r] : 0;
-        out_ins[r] = v;
-      }
-      sm_next[n] = v;
-    }
-    res_next[i] = nw;
-    if (ls_next)
-      for (uint32_t w = nw; w; w &= w - 1) {
-        const int n = i * 32 + __ffs(w) - 1;
-        ls_next[n] = (aw >> (n & 31)) & 1u ? a.token : ls_prev[n];
-      }
-  }
-  // slots of the active neurons, in active-list order
-  {
-    int* out_as = a.active_slot + (size_t)s * K;
-    int p = ea;
-    for (uint32_t w = aw; w; w &= w - 1) {
-      const int b = __ffs(w) - 1;
-      const int n = i * 32 + b;
-      int v;
-      if ((rw >> b) & 1u) {
-        v = sm_prev[n];
-      } else {
-        const int r = ein + __popc(dinw & ((1u << b) - 1u));
-        v = r < n_free ? free_list[r] : 0;
-      }
-      out_as[p++] = v;
-    }
-  }
-  // inverse map and slot contents of the next state
-  for (int k = tid; k < K; k += kSetThreads) {
-    inv_next[k] = -1;
-    ct_next[k] = ct_prev[k];
+  // 6. outgoing neurons leave (before incoming ones may take their slots)
+  for (int r = tid; r < n_out; r += kSetThreads) {
+    const int n = out_out[r];
+    const int k = out_outs[r];
+    S[n] = -1;
+    if ((unsigned)k < (unsigned)K) inv[k] = -1;
   }
   __syncthreads();
-  for (uint32_t w = keptw; w; w &= w - 1) {
-    const int n = i * 32 + __ffs(w) - 1;
-    const int slot = sm_prev[n];
-    if ((unsigned)slot < (unsigned)K) inv_next[slot] = n;
+  // 7. incoming neurons take the free slots; remember what the slots held
+  for (int r = tid; r < n_in; r += kSetThreads) {
+    const int n = out_in[r];
+    const int k = r < n_free ? free_list[r] : 0;
+    out_ins[r] = k;
+    out_inct[r] = ct[k];
+    ct[k] = n;
+    inv[k] = n;
+    S[n] = k;
+    out_as[bit_rank(s_a, s_ea, n)] = k;
   }
-  for (uint32_t w = dinw; w; w &= w - 1) {
-    const int b = __ffs(w) - 1;
-    const int r = ein + __popc(dinw & ((1u << b) - 1u));
-    if (r < n_free) {
-      const int slot = free_list[r];
-      inv_next[slot] = i * 32 + b;
-      ct_next[slot] = i * 32 + b;
+  if (has_word) res[i] = nw;
+  if (ls)
+    for (int r = tid; r < n_a; r += kSetThreads) {
+      const int n = out_a[r];
+      out_lsold[r] = ls[n];
+      ls[n] = a.token;
     }
-  }
   if (tid == 0) {
     int* c = a.counts + (size_t)s * 4;
     c[0] = n_a;
@@ -297,6 +293,48 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   }
 }
 
+// Undo set_kernel for one layer per CTA from the recorded delta lists.
+__global__ void __launch_bounds__(kSetThreads) rollback_kernel(SetLaunch a) {
+  const int s = a.first_sparse + blockIdx.x;
+  const int F = a.F, K = a.K, W = a.words;
+  int* S = a.slotmap + (size_t)s * F;
+  int* inv = a.inv + (size_t)s * K;
+  int* ct = a.content + (size_t)s * K;
+  uint32_t* res = a.resbits + (size_t)s * W;
+  int* ls = a.window > 1 ? a.last_seen + (size_t)s * F : nullptr;
+  const int* c = a.counts + (size_t)s * 4;
+  const int n_a = c[0], n_in = c[1], n_out = c[2];
+  const int* din = a.din_n + (size_t)s * K;
+  const int* dins = a.din_s + (size_t)s * K;
+  const int* dinct = a.din_oldct + (size_t)s * K;
+  const int* dout = a.dout_n + (size_t)s * K;
+  const int* douts = a.dout_s + (size_t)s * K;
+  for (int r = threadIdx.x; r < n_in; r += kSetThreads) {
+    const int n = din[r], k = dins[r];
+    if ((unsigned)n >= (unsigned)F || (unsigned)k >= (unsigned)K) continue;
+    S[n] = -1;
+    inv[k] = -1;
+    ct[k] = dinct[r];
+    atomicAnd(&res[n >> 5], ~(1u << (n & 31)));
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < n_out; r += kSetThreads) {
+    const int n = dout[r], k = douts[r];
+    if ((unsigned)n >= (unsigned)F || (unsigned)k >= (unsigned)K) continue;
+    S[n] = k;
+    inv[k] = n;
+    atomicOr(&res[n >> 5], 1u << (n & 31));
+  }
+  if (ls) {
+    const int* act = a.active + (size_t)s * K;
+    const int* old = a.ls_old + (size_t)s * K;
+    for (int r = threadIdx.x; r < n_a; r += kSetThreads) {
+      const int n = act[r];
+      if ((unsigned)n < (unsigned)F) ls[n] = old[r];
+    }
+  }
+}
+
 __global__ void reset_state_kernel(int* slotmap, int* inv, uint32_t* resbits, size_t n_sm, size_t n_inv,
                                    size_t n_res) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -306,15 +344,22 @@ __global__ void reset_state_kernel(int* slotmap, int* inv, uint32_t* resbits, si
 }
 
 cudaError_t launch_set(const SetLaunch& a, cudaStream_t st) {
-  if (a.words > kSetThreads || a.K > kMaxKmax) return cudaErrorInvalidValue;
-  set_kernel<<<a.n_layers_launch, kSetThreads, 0, st>>>(a);
+  if (a.words > kMaxWords || a.K > kMaxKmax) return cudaErrorInvalidValue;
+  const size_t dyn = (size_t)a.K * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(set_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  set_kernel<<<a.n_layers_launch, kSetThreads, dyn, st>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int* last_seen, int S, int F, int K,
-                               int words, cudaStream_t st) {
-  (void)last_seen;
-  reset_state_kernel<<<256, 256, 0, st>>>(slotmap, inv, resbits, 2ull * S * F, 2ull * S * K, 2ull * S * words);
+cudaError_t launch_rollback(const SetLaunch& a, cudaStream_t st) {
+  rollback_kernel<<<a.n_layers_launch, kSetThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int S, int F, int K, int words,
+                               cudaStream_t st) {
+  reset_state_kernel<<<256, 256, 0, st>>>(slotmap, inv, resbits, (size_t)S * F, (size_t)S * K, (size_t)S * words);
   return cudaGetLastError();
 }
 

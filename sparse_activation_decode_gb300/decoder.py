@@ -227,6 +227,16 @@ class SparseDecoder:
         L.check(self.lib.np_get_profile(self.model, ms, n, b), "np_get_profile")
         return {k: {"ms": ms[i], "launches": n[i], "bytes": b[i]} for i, k in enumerate(L.KIND_NAMES)}
 
+    def timeline(self, max_entries: int = 65536):
+        """[(kind, start_ms, end_ms)] of the launches timed since the last
+        profile() call, in issue order."""
+        kinds = (ctypes.c_int32 * max_entries)()
+        a = (ctypes.c_float * max_entries)()
+        b = (ctypes.c_float * max_entries)()
+        n = ctypes.c_int32()
+        L.check(self.lib.np_get_timeline(self.model, kinds, a, b, max_entries, ctypes.byref(n)), "np_get_timeline")
+        return [(L.KIND_NAMES[kinds[i]], a[i], b[i]) for i in range(n.value)]
+
     def launch_count(self) -> int:
         return int(self.lib.np_launch_count(self.model))
 
