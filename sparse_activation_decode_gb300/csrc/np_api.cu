@@ -71,6 +71,7 @@ struct np_model {
   size_t row_bytes = 0, rec_bytes = 0;
   cudaStream_t main = nullptr, side = nullptr;  // side = gather stream G0
   cudaStream_t g1 = nullptr, xs = nullptr;        // gather stream G1, scatter stream X
+  cudaStream_t fs = nullptr;                      // sparse-FFN stream
   const unsigned char* store_dev = nullptr;
   // device allocations
   void* bufs = nullptr;
@@ -97,7 +98,8 @@ struct np_model {
   uint64_t pending_bits = 0, committed_since_token = 0;
   int64_t token = 0;
   int64_t launches = 0;
-  cudaEvent_t ev_set = nullptr, ev_side_done = nullptr, ev_j[3] = {nullptr, nullptr, nullptr};
+  cudaEvent_t ev_set = nullptr, ev_side_done = nullptr, ev_j[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t ev_pre = nullptr, ev_ffn = nullptr;
   std::vector<cudaEvent_t> ev_g, ev_layer;  // per sparse layer: gathered, ready
   // profiling
   bool prof = false;
@@ -195,9 +197,9 @@ const unsigned char* layer_bufs(const np_model* m, int s) {
 }
 
 // FFN over a row list followed by the partial-sum finish.
-np_status enqueue_ffn(np_model* m, int kind, const unsigned char* base, size_t proj_stride, const int* rows,
-                      const int* n_dev, int n_host, int list_cap, int row_limit, int stages, const float* h_in,
-                      float* h_out, float* y_out, int64_t fixed_bytes) {
+np_status enqueue_ffn(np_model* m, cudaStream_t st, int kind, const unsigned char* base, size_t proj_stride,
+                      const int* rows, const int* n_dev, int n_host, int list_cap, int row_limit, int stages,
+                      const float* h_in, float* h_out, float* y_out, int64_t fixed_bytes) {
   FfnLaunch a{};
   a.h_in = h_in;
   int p = 0;
@@ -221,22 +223,30 @@ np_status enqueue_ffn(np_model* m, int kind, const unsigned char* base, size_t p
   a.n_stages = stages;
   a.grid = m->ffn_grid;
   a.err = m->err;
-  cudaStream_t st = m->main;
   return launch(m, kind, st, fixed_bytes, [&] { return launch_ffn_rows(a, st); });
 }
 
-np_status enqueue_dense(np_model* m, int layer, const float* h_in, float* h_out, float* y_out) {
+np_status enqueue_dense_on(np_model* m, cudaStream_t st, int layer, const float* h_in, float* h_out,
+                           float* y_out) {
   const size_t proj_stride = (size_t)m->F * m->row_bytes;
   const unsigned char* base =
       static_cast<const unsigned char*>(m->d.dense_w) + (size_t)layer * m->nproj * proj_stride;
-  return enqueue_ffn(m, NP_KIND_DENSE, base, proj_stride, nullptr, nullptr, m->F, m->F, m->F, m->ffn_stages_dense,
-                     h_in, h_out, y_out, (int64_t)m->nproj * m->F * m->row_bytes);
+  return enqueue_ffn(m, st, NP_KIND_DENSE, base, proj_stride, nullptr, nullptr, m->F, m->F, m->F,
+                     m->ffn_stages_dense, h_in, h_out, y_out, (int64_t)m->nproj * m->F * m->row_bytes);
+}
+
+np_status enqueue_dense(np_model* m, int layer, const float* h_in, float* h_out, float* y_out) {
+  return enqueue_dense_on(m, m->main, layer, h_in, h_out, y_out);
+}
+
+np_status enqueue_sparse_on(np_model* m, cudaStream_t st, int s, const float* h_in, float* h_out, float* y_out) {
+  const size_t proj_stride = (size_t)m->K * m->row_bytes;
+  return enqueue_ffn(m, st, NP_KIND_FFN, layer_bufs(m, s), proj_stride, m->active_slot + (size_t)s * m->K,
+                     m->counts + (size_t)s * 4, 0, m->K, m->K, m->ffn_stages, h_in, h_out, y_out, 0);
 }
 
 np_status enqueue_sparse(np_model* m, int s, const float* h_in, float* h_out, float* y_out) {
-  const size_t proj_stride = (size_t)m->K * m->row_bytes;
-  return enqueue_ffn(m, NP_KIND_FFN, layer_bufs(m, s), proj_stride, m->active_slot + (size_t)s * m->K,
-                     m->counts + (size_t)s * 4, 0, m->K, m->K, m->ffn_stages, h_in, h_out, y_out, 0);
+  return enqueue_sparse_on(m, m->main, s, h_in, h_out, y_out);
 }
 
 np_status enqueue_rowdot(np_model* m, const void* W, int n_rows, int len, const float* vec, int rms, int mode,
@@ -264,6 +274,19 @@ np_status enqueue_rowdot(np_model* m, const void* W, int n_rows, int len, const 
   a.err = m->err;
   cudaStream_t st = m->main;
   return launch(m, NP_KIND_PRED, st, (int64_t)n_rows * len * m->esz, [&] { return launch_rowdot(a, st); });
+}
+
+// Second predictor product for heads [h0, h1) only (shared predictor).
+np_status enqueue_pred_heads(np_model* m, int h0, int h1) {
+  if (h1 <= h0) return NP_OK;
+  const unsigned char* w2 = static_cast<const unsigned char*>(m->d.pred_w2) + (size_t)h0 * m->C * m->H * m->esz;
+  return enqueue_rowdot(m, w2, (h1 - h0) * m->C, m->H, m->z, 0, 1, nullptr, nullptr, m->keys + h0, m->C, nullptr,
+                        nullptr, 0, m->rps2, m->ns2);
+}
+
+np_status enqueue_pred_hidden(np_model* m, const float* h) {
+  return enqueue_rowdot(m, m->d.pred_w1, m->H, m->D, h, 1, 0, nullptr, m->z, nullptr, 0, nullptr,
+                        reinterpret_cast<uint32_t*>(m->keys), 2 * m->NH, m->rps1, m->ns1);
 }
 
 np_status enqueue_predict(np_model* m, int layer, const float* h, bool want_ids = true) {
@@ -322,8 +345,8 @@ cudaStream_t gather_stream(const np_model* m, int s) { return (s & 1) ? m->g1 : 
 
 // Make `st` wait for all work queued so far on the gather and scatter streams.
 np_status join_side(np_model* m, cudaStream_t st) {
-  const cudaStream_t src[3] = {m->side, m->g1, m->xs};
-  for (int k = 0; k < 3; ++k) {
+  const cudaStream_t src[4] = {m->side, m->g1, m->xs, m->fs};
+  for (int k = 0; k < 4; ++k) {
     CUDA_TRY(cudaEventRecord(m->ev_j[k], src[k]));
     CUDA_TRY(cudaStreamWaitEvent(st, m->ev_j[k], 0));
   }
@@ -466,6 +489,7 @@ np_status sync_model(np_model* m) {
   CUDA_TRY(cudaStreamSynchronize(m->side));
   CUDA_TRY(cudaStreamSynchronize(m->g1));
   CUDA_TRY(cudaStreamSynchronize(m->xs));
+  CUDA_TRY(cudaStreamSynchronize(m->fs));
   CUDA_TRY(cudaStreamSynchronize(m->main));
   return NP_OK;
 }
@@ -673,7 +697,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
   e = cudaEventCreateWithFlags(&m->ev_side_done, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
-  for (int k = 0; k < 3; ++k) {
+  for (int k = 0; k < 4; ++k) {
     e = cudaEventCreateWithFlags(&m->ev_j[k], cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
   }
@@ -692,6 +716,9 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     const int pr = env_int("NP_TUNE_SIDE_PRIORITY", 1) == 1 ? hi : lo;
     e = cudaStreamCreateWithPriority(&m->g1, cudaStreamNonBlocking, pr);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&m->xs, cudaStreamNonBlocking, pr);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->fs, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_pre, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_ffn, cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(cuda_fail(e, "cudaStreamCreate"));
   }
   e = cudaDeviceSynchronize();
@@ -707,8 +734,12 @@ np_status np_free_model(np_model* m) {
   if (m->g1) cudaStreamSynchronize(m->g1);
   if (m->xs) cudaStreamSynchronize(m->xs);
   cudaDeviceSynchronize();
+  if (m->fs) cudaStreamSynchronize(m->fs);
   if (m->g1) cudaStreamDestroy(m->g1);
   if (m->xs) cudaStreamDestroy(m->xs);
+  if (m->fs) cudaStreamDestroy(m->fs);
+  if (m->ev_pre) cudaEventDestroy(m->ev_pre);
+  if (m->ev_ffn) cudaEventDestroy(m->ev_ffn);
   for (cudaEvent_t ev : m->ev_j)
     if (ev) cudaEventDestroy(ev);
   for (cudaEvent_t ev : m->ev_g)
@@ -858,40 +889,72 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
   }
   const int64_t token = m->token;
   const bool shared = m->d.pred_kind == NP_PRED_SHARED_ARGMAX;
-  for (int l = 0; l < m->dn; ++l) {
-    NP_TRY(enqueue_dense(m, l, h_dev, h_dev, nullptr));
-    if (l == 0 && shared && m->S > 0) {
-      NP_TRY(enqueue_predict(m, 0, h_dev, false));
-      NP_TRY(enqueue_set(m, 0, m->S, nullptr, nullptr, m->keys));
-      m->pending_bits = all_layers(m);
-      std::vector<int> layers(m->S);
-      for (int s = 0; s < m->S; ++s) layers[s] = s;
+  if (shared && m->S > 0) {
+    // main: dense layer 0, the predictor's hidden layer, then per layer
+    // group the group's predictor heads, its set kernel and its reads on the
+    // gather streams, so that transfers start after the first small group.
+    // The FFN stream runs dense layers 1..d-1 (once the predictor has read
+    // h) and then the sparse FFNs, each after its own rows have arrived.
+    NP_TRY(enqueue_dense(m, 0, h_dev, h_dev, nullptr));
+    NP_TRY(enqueue_pred_hidden(m, h_dev));
+    CUDA_TRY(cudaEventRecord(m->ev_pre, m->main));
+    CUDA_TRY(cudaStreamWaitEvent(m->fs, m->ev_pre, 0));
+    for (int l = 1; l < m->dn; ++l) NP_TRY(enqueue_dense_on(m, m->fs, l, h_dev, h_dev, nullptr));
+    m->pending_bits = all_layers(m);
+    std::vector<int> moved;
+    int s0 = 0;
+    for (int g = 1; s0 < m->S; g *= 2) {
+      const int cnt = g < m->S - s0 ? g : m->S - s0;
+      const bool last = s0 + cnt == m->S;
+      const int l0 = m->dn + s0;
+      NP_TRY(enqueue_pred_heads(m, 2 * (l0 - 1), 2 * (l0 - 1 + cnt)));
+      if (last) NP_TRY(enqueue_pred_heads(m, 0, 2 * (m->dn - 1)));  // heads of dense layers 1..d-1
+      SetLaunch sa = set_args(m, s0, cnt);
+      sa.keys = m->keys;
+      sa.ids_out = last ? m->ids : nullptr;
+      cudaStream_t st = m->main;
+      NP_TRY(launch(m, NP_KIND_SET, st, (int64_t)cnt * m->W * 8, [&] { return launch_set(sa, st); }));
+      CUDA_TRY(cudaEventRecord(m->ev_set, st));
+      std::vector<int> layers;
+      for (int s = s0; s < s0 + cnt; ++s) layers.push_back(s);
       size_t n_moved = 0;
       const np_status rs = move_layers(m, layers, &n_moved);
+      for (size_t q = 0; q < n_moved; ++q) moved.push_back(layers[q]);
       if (rs != NP_OK) {
-        NP_TRY(abort_pending(m, std::vector<int>(layers.begin(), layers.begin() + n_moved)));
-        return rs;
-      }
-    }
-  }
-  for (int s = 0; s < m->S; ++s) {
-    if (!shared) {
-      NP_TRY(enqueue_predict(m, m->dn + s, h_dev));
-      NP_TRY(enqueue_set(m, s, 1, nullptr, m->fire));
-      m->pending_bits |= 1ull << s;
-      size_t n_moved = 0;
-      const np_status rs = move_layers(m, std::vector<int>{s}, &n_moved);
-      if (rs != NP_OK) {
-        // earlier layers of this token already hold their new rows: put the
-        // previous contents back and undo the whole token's delta
-        std::vector<int> moved;
-        for (int q = 0; q < s; ++q) moved.push_back(q);
+        // layers of later groups have no delta yet
+        for (int s = s0 + cnt; s < m->S; ++s) m->pending_bits &= ~(1ull << s);
         NP_TRY(abort_pending(m, moved));
         return rs;
       }
+      s0 += cnt;
     }
-    CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_layer[s], 0));
-    NP_TRY(enqueue_sparse(m, s, h_dev, h_dev, nullptr));
+    for (int s = 0; s < m->S; ++s) {
+      CUDA_TRY(cudaStreamWaitEvent(m->fs, m->ev_layer[s], 0));
+      NP_TRY(enqueue_sparse_on(m, m->fs, s, h_dev, h_dev, nullptr));
+    }
+    CUDA_TRY(cudaEventRecord(m->ev_ffn, m->fs));
+    CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_ffn, 0));
+  } else {
+    for (int l = 0; l < m->dn; ++l) NP_TRY(enqueue_dense(m, l, h_dev, h_dev, nullptr));
+    for (int s = 0; s < m->S; ++s) {
+      if (!shared) {
+        NP_TRY(enqueue_predict(m, m->dn + s, h_dev));
+        NP_TRY(enqueue_set(m, s, 1, nullptr, m->fire));
+        m->pending_bits |= 1ull << s;
+        size_t n_moved = 0;
+        const np_status rs = move_layers(m, std::vector<int>{s}, &n_moved);
+        if (rs != NP_OK) {
+          // earlier layers of this token already hold their new rows: put the
+          // previous contents back and undo the whole token's delta
+          std::vector<int> moved;
+          for (int q = 0; q < s; ++q) moved.push_back(q);
+          NP_TRY(abort_pending(m, moved));
+          return rs;
+        }
+      }
+      CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_layer[s], 0));
+      NP_TRY(enqueue_sparse(m, s, h_dev, h_dev, nullptr));
+    }
   }
   if (m->S > 0) {
     m->committed_since_token = 0;

@@ -42,8 +42,6 @@ constexpr int kFfnThreads = 256;                 // consumer threads
 constexpr int kFfnWarps = kFfnThreads / 32;      // consumer warps
 constexpr int kFfnBlock = kFfnThreads + 32;      // plus one producer warp
 constexpr int kRowCache = 64;                    // row indices cached per CTA
-constexpr int kSliceCols = 16;                      // columns per reduction slice
-constexpr int kSliceGroups = kFfnThreads / kSliceCols;  // partial groups per slice
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   uint64_t d;
