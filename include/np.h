@@ -270,6 +270,26 @@ np_status np_get_timeline(np_model* m, int32_t* kinds, float* start_ms, float* e
 np_status np_host_register(void* ptr, size_t bytes);
 np_status np_host_unregister(void* ptr);
 
+/* Allocation-free FFN over caller-provided rows (no counterpart on the
+ * pages: an addition for callers that cannot allocate device memory, e.g. a
+ * serving loop whose allocator owns a fixed memory budget, or a
+ * latency-critical path where cudaMalloc would synchronize the device).
+ * Computes y = sum over the listed rows r of relu(g_r . x)(u_r . x) d_r
+ * (relu(u_r . x) d_r when has_gate = 0) with x = rmsnorm(h) — the kernel of
+ * np_sparse_mlp — and writes y_dev [d_model].  Rows: rows_dev[0..n_rows) are
+ * row indices into w_gate/w_up/w_down ([row_limit][d_model] each), or NULL
+ * for rows 0..n_rows-1.  All pointers are device pointers, 16-byte aligned;
+ * dtype NP_F32/NP_F16/NP_BF16; d_model in [8, 8192], rows a multiple of 16
+ * bytes.  Enqueued on `stream` (cudaStream_t); the call allocates nothing:
+ * its scratch (at most 1 MiB of partial sums plus 64 counters) is a
+ * file-scope device array whose address the first call on each device looks
+ * up, so make that first call before any stream capture.  All calls share
+ * the array: calls that overlap on the GPU race.  Errors: NP_ERR_ARG for
+ * sizes or pointers out of range, NP_ERR_CUDA if a launch fails. */
+np_status np_ffn_rows_noalloc(const float* h_dev, const void* w_gate, const void* w_up, const void* w_down,
+                              const int32_t* rows_dev, int32_t n_rows, int32_t row_limit, int32_t d_model,
+                              int32_t dtype, int32_t has_gate, float* y_dev, void* stream);
+
 /* Number of kernel launches the model has issued since creation. */
 int64_t np_launch_count(np_model* m);
 

@@ -1,0 +1,115 @@
+// Allocation-free FFN entry point (np_ffn_rows_noalloc).
+//
+// Some callers cannot call cudaMalloc: a serving loop that runs under a
+// fixed, pre-planned memory budget owned by its own allocator, or code on a
+// latency-critical path where a device allocation would implicitly
+// synchronize the device.  For them this entry point runs the same FFN
+// kernel as np_sparse_mlp / np_dense_mlp on caller-provided weights, row
+// list, input and output, with its split-K scratch (cluster partial sums,
+// per-slice arrival counters, error word) in one file-scope __device__
+// array of fixed size instead of model-owned device allocations.
+//
+// The array is a host-side stand-in in host code: its device address is
+// looked up once per device with cudaGetSymbolAddress while that device is
+// current (the first call on a device does this, so that first call should
+// come before any stream capture), and only that address is passed to the
+// kernel.  Every call on a device shares the array and it keeps the last
+// call's contents; the counters and the error word are cleared on the
+// caller's stream before each launch.  Calls whose kernels overlap on the
+// GPU race on the array: serialize them (one stream, or events).
+#include <mutex>
+
+#include "np.h"
+#include "np_kernels.h"
+
+namespace np {
+
+constexpr int kNoallocMaxDevices = 64;
+constexpr size_t kNoallocPartialFloats = 256 * 1024;  // 1 MiB of cluster partials
+constexpr size_t kNoallocCounters = 64;               // slice counters + error word
+
+struct NoallocScratch {
+  float partial[kNoallocPartialFloats];
+  int counters[kNoallocCounters];
+};
+
+static __device__ __align__(256) NoallocScratch g_noalloc_scratch;
+
+static std::mutex g_noalloc_mu;
+static NoallocScratch* g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+static cudaError_t noalloc_scratch_for_current_device(NoallocScratch** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<NoallocScratch*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace np
+
+extern "C" np_status np_ffn_rows_noalloc(const float* h_dev, const void* w_gate, const void* w_up,
+                                         const void* w_down, const int32_t* rows_dev, int32_t n_rows,
+                                         int32_t row_limit, int32_t d_model, int32_t dtype, int32_t has_gate,
+                                         float* y_dev, void* stream) {
+  using namespace np;
+  if (!h_dev || !w_up || !w_down || !y_dev || (has_gate && !w_gate)) return NP_ERR_ARG;
+  if (dtype < NP_F32 || dtype > NP_BF16 || (has_gate != 0 && has_gate != 1)) return NP_ERR_ARG;
+  const int esz = dtype == NP_F32 ? 4 : 2;
+  if (d_model < 8 || d_model > 8192 || (d_model * esz) % 16 != 0 || d_model / (16 / esz) > ffn_max_chunks())
+    return NP_ERR_ARG;
+  if (n_rows < 0 || row_limit < 1 || (!rows_dev && n_rows > row_limit)) return NP_ERR_ARG;
+  const uintptr_t align_or = reinterpret_cast<uintptr_t>(h_dev) | reinterpret_cast<uintptr_t>(y_dev) |
+                             reinterpret_cast<uintptr_t>(w_gate) | reinterpret_cast<uintptr_t>(w_up) |
+                             reinterpret_cast<uintptr_t>(w_down);
+  if (align_or & 15u) return NP_ERR_ARG;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  NoallocScratch* scratch = nullptr;
+  if (noalloc_scratch_for_current_device(&scratch) != cudaSuccess) return NP_ERR_CUDA;
+  int dev = 0, sms = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NP_ERR_CUDA;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  int n_stages = 0, cluster = 1, grid = 0;
+  if (ffn_plan(dtype, has_gate, d_model, esz, (size_t)optin - 1024, sms, &n_stages, &cluster, &grid) != cudaSuccess)
+    return NP_ERR_CUDA;
+  // the cluster partials must fit the fixed scratch: shrink the grid if needed
+  const int max_clusters = (int)(kNoallocPartialFloats / (size_t)d_model);
+  if (grid / cluster > max_clusters) grid = max_clusters * cluster;
+  if (grid < cluster || cluster + 1 > (int)kNoallocCounters) return NP_ERR_ARG;
+  int* err_word = scratch->counters + kNoallocCounters - 1;
+  if (cudaMemsetAsync(scratch->counters, 0, sizeof(scratch->counters), st) != cudaSuccess) return NP_ERR_CUDA;
+
+  FfnLaunch a{};
+  a.h_in = h_dev;
+  a.w_gate = has_gate ? w_gate : nullptr;
+  a.w_up = w_up;
+  a.w_down = w_down;
+  a.row_list = rows_dev;
+  a.n_rows_dev = nullptr;
+  a.n_rows_host = n_rows;
+  a.list_cap = rows_dev ? n_rows : row_limit;
+  a.row_limit = row_limit;
+  a.part = scratch->partial;
+  a.slice_cnt = scratch->counters;
+  a.h_out = nullptr;
+  a.y_out = y_dev;
+  a.cluster = cluster;
+  a.D = d_model;
+  a.dtype = dtype;
+  a.dtype_bytes = esz;
+  a.gated = has_gate;
+  a.n_stages = n_stages;
+  a.grid = grid;
+  a.err = err_word;
+  return launch_ffn_rows(a, st) == cudaSuccess ? NP_OK : NP_ERR_CUDA;
+}

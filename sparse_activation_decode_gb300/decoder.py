@@ -263,3 +263,19 @@ def decoder_for(wl, *, h2d_mode: str = "staged", staging_rows: int | None = None
         window=cfg.window if cfg.residency == "window" else 1, batch=cfg.batch,
         staging_rows=cfg.staging_rows if staging_rows is None else staging_rows, h2d_mode=h2d_mode,
         read_hook=read_hook, **kw)
+
+
+def ffn_rows_noalloc(h: torch.Tensor, w_gate: torch.Tensor | None, w_up: torch.Tensor, w_down: torch.Tensor,
+                     rows: torch.Tensor | None, n_rows: int, y: torch.Tensor | None = None) -> torch.Tensor:
+    """np_ffn_rows_noalloc: the FFN over listed rows without any device
+    allocation by the library (its scratch is a fixed device array); for
+    callers that cannot allocate.  Enqueued on torch's current stream."""
+    lib = L.load()
+    if y is None:
+        y = torch.empty_like(h)
+    L.check(lib.np_ffn_rows_noalloc(h.data_ptr(), None if w_gate is None else w_gate.data_ptr(), w_up.data_ptr(),
+                                    w_down.data_ptr(), None if rows is None else rows.data_ptr(), int(n_rows),
+                                    int(w_up.shape[0]), int(h.numel()), _DTYPES[w_up.dtype],
+                                    int(w_gate is not None), y.data_ptr(), torch.cuda.current_stream().cuda_stream),
+            "np_ffn_rows_noalloc")
+    return y
