@@ -44,7 +44,7 @@ class SparseDecoder:
                  dense_w: torch.Tensor | None = None, centroids: torch.Tensor | None = None,
                  pred_hidden: int, pred_kind: str = "shared_argmax", has_gate: bool = True,
                  combine: str = "union", residency: str = "slotmap", window: int = 1, batch: int = 1,
-                 staging_rows: int = 0, h2d_mode: str = "staged",
+                 staging_rows: int = 0, h2d_mode: str = "fused",
                  main_stream: torch.cuda.Stream | None = None, side_stream: torch.cuda.Stream | None = None,
                  read_hook=None):
         self.lib = L.load()
@@ -229,7 +229,8 @@ class SparseDecoder:
 
     def timeline(self, max_entries: int = 65536):
         """[(kind, start_ms, end_ms)] of the launches timed since the last
-        profile() call, in issue order."""
+        profile() call, in issue order.  The library keeps at most the most
+        recent 16384 launches (older ones only enter the profile() sums)."""
         kinds = (ctypes.c_int32 * max_entries)()
         a = (ctypes.c_float * max_entries)()
         b = (ctypes.c_float * max_entries)()
@@ -241,7 +242,7 @@ class SparseDecoder:
         return int(self.lib.np_launch_count(self.model))
 
 
-def decoder_for(wl, *, h2d_mode: str = "staged", staging_rows: int | None = None, read_hook=None,
+def decoder_for(wl, *, h2d_mode: str = "fused", staging_rows: int | None = None, read_hook=None,
                 centroids_dev: torch.Tensor | None = None, **kw) -> SparseDecoder:
     """Build a SparseDecoder from an object carrying a `cfg` (shapes) and the
     weight tensors (dense_w, store, pred_w1, pred_w2, pred_b2, centroids)."""
