@@ -36,9 +36,9 @@ design notes):
   the predictor;
 * argmax ties go to the lowest centroid index; the per-layer predictor fires
   when its logit is strictly positive (sigmoid > 0.5);
-* batched decoding rounds the normalised input to bf16 before every dot
-  product (the GPU's tensor-core operands) and takes the union of the
-  sequences' active sets.
+* batched decoding takes the union of the sequences' active sets; every
+  sequence's FFN runs over that union, on the same (unrounded) normalised
+  input as a single sequence.
 
 Functions without an external pin say so in their docstring ("parity
 unpinned"); all others are pinned by the CPU tests against closed forms, brute
@@ -62,12 +62,6 @@ def f64(a) -> np.ndarray:
     if isinstance(a, torch.Tensor):
         return a.detach().to("cpu", torch.float64).numpy()
     return np.asarray(a, dtype=np.float64)
-
-
-def round_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float64 values to the nearest bf16 (ties to even), via torch."""
-    return torch.from_numpy(np.asarray(x, dtype=np.float64)).to(torch.float32) \
-        .to(torch.bfloat16).to(torch.float64).numpy()
 
 
 def rmsnorm(h: np.ndarray) -> np.ndarray:
@@ -289,7 +283,6 @@ class OracleDecoder:
             instead of logit > 0 (per-layer predictor, staged parity)."""
         cfg, wl = self.cfg, self.wl
         B = cfg.batch
-        rnd = round_bf16 if B > 1 else (lambda v: v)
         h = f64(x).reshape(B, cfg.d_model).copy()
         rec = TokenRecord()
         # Dense prefix (NeuroPrefetcher "System Overview": the first d layers
@@ -299,7 +292,7 @@ class OracleDecoder:
             rec.h_in_dense.append(h.copy())
             yd = np.zeros((B, cfg.d_model))
             for b in range(B):
-                yd[b], _ = ffn_rows(g, u, dt, rnd(rmsnorm(h[b])))
+                yd[b], _ = ffn_rows(g, u, dt, rmsnorm(h[b]))
                 h[b] += yd[b]
             rec.y_dense.append(yd)
             if layer == 0:
@@ -348,7 +341,7 @@ class OracleDecoder:
             rec.h_in.append(h.copy())
             ys = np.zeros((B, cfg.d_model))
             for b in range(B):
-                ys[b], _ = ffn_rows(g, u, dt, rnd(rmsnorm(h[b])))
+                ys[b], _ = ffn_rows(g, u, dt, rmsnorm(h[b]))
                 h[b] += ys[b]
             rec.y.append(ys)
         rec.h = h
@@ -358,9 +351,8 @@ class OracleDecoder:
     def _predict_shared(self, h, rec, ids_override):
         cfg = self.cfg
         w1, w2, _ = self._pred()
-        rnd = round_bf16 if cfg.batch > 1 else (lambda v: v)
         for b in range(cfg.batch):
-            xs = rnd(rmsnorm(h[b]))
+            xs = rmsnorm(h[b])
             lg = predictor_logits(w1, w2, None, xs)
             rec.pred_xhat.append(xs)
             rec.logits.append(lg)

@@ -428,3 +428,32 @@ def test_batched_union_over_sequences():
             u = _bits_by_loop(wl.centroids[s, 1, rec.ids[b][2 * (layer - 1) + 1]], cfg.d_ff)
             want |= set(g) | set(u)
         assert rec.active[s] == sorted(want)[:cfg.k_max]
+
+
+def test_batched_ffn_equals_dense_masked_ffn_per_sequence():
+    # Each sequence of a batch runs the FFN over the union set: its output
+    # equals the dense FFN (a torch float64 matmul) with every neuron outside
+    # the union zeroed, on that sequence's own normalised input; and the
+    # sequences do not mix (permuting the batch permutes the outputs).
+    cfg = SMALL_BATCHED
+    wl = make_workload(cfg)
+    dec = OracleDecoder(wl, materialize_buffers=False)
+    rec = dec.step(wl.x[0].numpy())
+    for s in range(cfg.n_sparse):
+        st = torch.from_numpy(oracle.f64(wl.store[s]))      # [F][3][D]
+        hin = torch.from_numpy(rec.h_in[s])                # [B][D]
+        xh = hin / torch.sqrt((hin * hin).mean(dim=1, keepdim=True) + 1e-6)
+        a = xh @ st[:, 0].T                                # [B][F]
+        b = xh @ st[:, 1].T
+        mask = torch.zeros(cfg.d_ff, dtype=torch.bool)
+        mask[rec.active[s]] = True
+        hn = torch.where(mask & (a > 0), a * b, torch.zeros_like(a))
+        y = hn @ st[:, 2]                                  # [B][D]
+        for bb in range(cfg.batch):
+            assert oracle.rel_l2(rec.y[s][bb], y[bb].numpy()) < 1e-12
+    perm = np.arange(cfg.batch)[::-1]
+    dec2 = OracleDecoder(wl, materialize_buffers=False)
+    rec2 = dec2.step(wl.x[0].numpy()[perm])
+    assert rec2.active == rec.active
+    for s in range(cfg.n_sparse):
+        assert np.array_equal(rec2.y[s], rec.y[s][perm])
