@@ -251,8 +251,12 @@ class OracleDecoder:
         return f64(wl.pred_w1[layer]), f64(wl.pred_w2[layer]), f64(wl.pred_b2[layer])
 
     def _dense_rows(self, layer: int):
+        """Gate, up and down^T rows of a dense layer (no gate rows when the
+        model has none, as in its sparse records)."""
         w = f64(self.wl.dense_w[layer])
-        return w[0], w[1], w[2]
+        if self.cfg.has_gate:
+            return w[0], w[1], w[2]
+        return None, w[0], w[1]
 
     def _sparse_rows(self, s: int, ids: list[int]):
         """Rows of the active neurons, read through the slot map from the

@@ -230,7 +230,7 @@ class Workload:
     the host weight store, which is always CPU memory (the storage tier)."""
 
     cfg: Config
-    dense_w: torch.Tensor | None      # [d][3][F][D]  (gate, up, down^T)
+    dense_w: torch.Tensor | None      # [d][n_proj][F][D]  (gate, up, down^T; no gate rows without a gate)
     store: torch.Tensor                # [S][F][n_proj][D]  record layout, CPU
     centroids: np.ndarray | None       # uint32 [S][2][C][words]
     pred_w1: torch.Tensor              # [H][D]       or [L][H][D]  (per layer)
@@ -259,9 +259,9 @@ def make_workload(cfg: Config, device: str | torch.device = "cpu",
     # ---- FFN weights: dense prefix on `device`, sparse layers into the store
     dense_w = None
     if d > 0:
-        dense_w = torch.empty((d, 3, F, D), dtype=tdt, device=dev)
+        dense_w = torch.empty((d, cfg.n_proj, F, D), dtype=tdt, device=dev)
         for layer in range(d):
-            dense_w[layer] = _torch_normal((3, F, D), cfg.weight_std, tdt, dev,
+            dense_w[layer] = _torch_normal((cfg.n_proj, F, D), cfg.weight_std, tdt, dev,
                                            cfg.seed * 1000 + layer)
     if store_out is None:
         store = torch.empty((S, F, cfg.n_proj, D), dtype=tdt)
