@@ -19,7 +19,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libnp.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["np_api.cu", "np_ffn.cu", "np_pred.cu", "np_set.cu", "np_scatter.cu", "np_noalloc.cu"]
+SOURCES = ["np_api.cu", "np_ffn.cu", "np_pred.cu", "np_set.cu", "np_scatter.cu", "np_noalloc.cu", "np_mma.cu"]
 
 
 def _nvcc() -> str:

@@ -89,6 +89,15 @@ struct np_model {
   float* logits = nullptr;
   float* part = nullptr;
   int* slice_cnt = nullptr;
+  // batched (B > 1) tensor-core path: tensor maps over the weight blocks,
+  // launch plans, residual bases [2][B][D], y accumulators [3][B][D], the
+  // predictor hidden layer as hi/lo 16-bit operands [16][H]
+  bool tc = false;
+  CUtensorMap map_bufs{}, map_dense{}, map_w1{}, map_w2{};
+  MmaPlan plan_ffn{}, plan_hid{}, plan_heads{};
+  float* hbase = nullptr;
+  float* yacc = nullptr;
+  uint16_t* zhl = nullptr;
   std::vector<void*> allocs;
   // launch shapes
   int ffn_grid = 0, ffn_cluster = 1, ffn_stages = 0, ffn_stages_dense = 0;
@@ -249,6 +258,92 @@ np_status enqueue_sparse(np_model* m, int s, const float* h_in, float* h_out, fl
   return enqueue_sparse_on(m, m->main, s, h_in, h_out, y_out);
 }
 
+// ---- batched path (tensor cores) -------------------------------------------
+float* tc_hbase(np_model* m, int i) { return m->hbase + (size_t)(i & 1) * m->B * m->D; }
+float* tc_y(np_model* m, int i) { return m->yacc + (size_t)(i % 3) * m->B * m->D; }
+
+np_status enqueue_mma(np_model* m, cudaStream_t st, int kind, int mode, const CUtensorMap& map, const MmaPlan& p,
+                      MmaArgs& a, int64_t fixed_bytes) {
+  a.B = m->B;
+  a.err = m->err;
+  const int bf16 = m->d.dtype == NP_BF16;
+  return launch(m, kind, st, fixed_bytes, [&] { return launch_mma_rows(mode, bf16, map, a, p, st); });
+}
+
+// FFN of layer l for all sequences: x = rmsnorm(hb + yprev), y added into
+// y_acc; hb + yprev stored into hb_out and y_zero cleared (both optional).
+np_status enqueue_tc_ffn(np_model* m, cudaStream_t st, int l, const float* hb, const float* yprev, float* hb_out,
+                         float* y_acc, float* y_zero) {
+  MmaArgs a{};
+  a.Kdim = m->D;
+  a.hb = hb;
+  a.yprev = yprev;
+  a.hb_out = hb_out;
+  a.y_acc = y_acc;
+  a.y_zero = y_zero;
+  const int g = m->d.has_gate ? 1 : 0;
+  const int mode = g ? kMmaFfnGated : kMmaFfnUp;
+  if (l < m->dn) {
+    const int base = l * m->nproj * m->F;
+    a.row_base0 = base;
+    a.row_base1 = base + m->F;
+    a.row_base2 = base + (1 + g) * m->F;
+    a.n_rows_host = m->F;
+    a.row_cap = m->F;
+    a.row_limit = m->F;
+    a.oob_row = m->dn * m->nproj * m->F;
+    return enqueue_mma(m, st, NP_KIND_DENSE, mode, m->map_dense, m->plan_ffn, a,
+                       (int64_t)m->nproj * m->F * m->row_bytes);
+  }
+  const int s = l - m->dn;
+  const int base = s * m->nproj * m->K;
+  a.row_base0 = base;
+  a.row_base1 = base + m->K;
+  a.row_base2 = base + (1 + g) * m->K;
+  a.row_list = m->active_slot + (size_t)s * m->K;
+  a.n_rows_dev = m->counts + (size_t)s * 4;
+  a.row_cap = m->K;
+  a.row_limit = m->K;
+  a.oob_row = m->S * m->nproj * m->K;
+  return enqueue_mma(m, st, NP_KIND_FFN, mode, m->map_bufs, m->plan_ffn, a, 0);
+}
+
+// Predictor hidden layer for all sequences (x = rmsnorm(hb + yprev)); the
+// argmax keys are cleared for the heads that follow.
+np_status enqueue_tc_hidden(np_model* m, const float* hb, const float* yprev) {
+  MmaArgs a{};
+  a.Kdim = m->D;
+  a.hb = hb;
+  a.yprev = yprev;
+  a.n_rows_host = m->H;
+  a.row_cap = m->H;
+  a.row_limit = m->H;
+  a.oob_row = m->H;
+  a.zout = m->zhl;
+  a.zout_stride = m->H;
+  a.keys_zero = m->keys;
+  a.n_keys_zero = m->B * m->NH;
+  return enqueue_mma(m, m->main, NP_KIND_PRED, kMmaHidden, m->map_w1, m->plan_hid, a,
+                     (int64_t)m->H * m->D * m->esz);
+}
+
+np_status enqueue_tc_heads(np_model* m, int h0, int h1) {
+  if (h1 <= h0) return NP_OK;
+  MmaArgs a{};
+  a.Kdim = m->H;
+  a.row_base0 = h0 * m->C;
+  a.n_rows_host = (h1 - h0) * m->C;
+  a.row_cap = a.n_rows_host;
+  a.row_limit = a.n_rows_host;
+  a.oob_row = m->NH * m->C;
+  a.zin = m->zhl;
+  a.keys = m->keys;
+  a.n_heads = m->NH;
+  a.C = m->C;
+  return enqueue_mma(m, m->main, NP_KIND_PRED, kMmaHeads, m->map_w2, m->plan_heads, a,
+                     (int64_t)(h1 - h0) * m->C * m->H * m->esz);
+}
+
 np_status enqueue_rowdot(np_model* m, const void* W, int n_rows, int len, const float* vec, int rms, int mode,
                          const void* bias, float* out_f, unsigned long long* keys, int C, uint32_t* fire,
                          uint32_t* zero_ptr, int zero_words, int rps, int ns) {
@@ -278,6 +373,7 @@ np_status enqueue_rowdot(np_model* m, const void* W, int n_rows, int len, const 
 
 // Second predictor product for heads [h0, h1) only (shared predictor).
 np_status enqueue_pred_heads(np_model* m, int h0, int h1) {
+  if (m->tc) return enqueue_tc_heads(m, h0, h1);
   if (h1 <= h0) return NP_OK;
   const unsigned char* w2 = static_cast<const unsigned char*>(m->d.pred_w2) + (size_t)h0 * m->C * m->H * m->esz;
   return enqueue_rowdot(m, w2, (h1 - h0) * m->C, m->H, m->z, 0, 1, nullptr, nullptr, m->keys + h0, m->C, nullptr,
@@ -290,6 +386,13 @@ np_status enqueue_pred_hidden(np_model* m, const float* h) {
 }
 
 np_status enqueue_predict(np_model* m, int layer, const float* h, bool want_ids = true) {
+  if (m->tc) {
+    NP_TRY(enqueue_tc_hidden(m, h, nullptr));
+    NP_TRY(enqueue_tc_heads(m, 0, m->NH));
+    if (!want_ids) return NP_OK;
+    cudaStream_t st = m->main;
+    return launch(m, NP_KIND_PRED, st, 0, [&] { return launch_keys_to_ids(m->keys, m->B * m->NH, m->ids, st); });
+  }
   if (m->d.pred_kind == NP_PRED_SHARED_ARGMAX) {
     NP_TRY(enqueue_rowdot(m, m->d.pred_w1, m->H, m->D, h, 1, 0, nullptr, m->z, nullptr, 0, nullptr,
                           reinterpret_cast<uint32_t*>(m->keys), 2 * m->NH, m->rps1, m->ns1));
@@ -556,7 +659,13 @@ static np_status validate(const np_model_desc* d) {
   if (d->combine != NP_COMBINE_INTERSECT && d->combine != NP_COMBINE_UNION) return arg_fail("bad combine");
   if (d->residency != NP_RES_SLOTMAP && d->residency != NP_RES_WINDOW) return arg_fail("bad residency");
   if (d->residency == NP_RES_WINDOW && (d->window < 1 || d->window > 32)) return arg_fail("window must be 1..32");
-  if (d->batch != 1) return arg_fail("batch must be 1");
+  if (d->batch < 1 || d->batch > 8) return arg_fail("batch must be in 1..8");
+  if (d->batch > 1) {
+    if (d->dtype == NP_F32) return arg_fail("batched decoding needs f16 or bf16 weights");
+    if (d->pred_kind != NP_PRED_SHARED_ARGMAX) return arg_fail("batched decoding uses the shared predictor");
+    if (d->d_model % 128 != 0) return arg_fail("batched decoding needs d_model a multiple of 128");
+    if (d->pred_hidden % 64 != 0) return arg_fail("batched decoding needs pred_hidden a multiple of 64");
+  }
   if (d->staging_rows < 0 || d->staging_rows > d->k_max) return arg_fail("staging_rows must be in [0, k_max]");
   if (d->h2d_mode != NP_H2D_STAGED && d->h2d_mode != NP_H2D_FUSED) return arg_fail("bad h2d_mode");
   if (d->pred_hidden < 1 || (d->pred_hidden * esz) % 16 != 0 ||
@@ -692,6 +801,34 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if ((st = dev_alloc(m, &m->part, (size_t)(m->ffn_grid / m->ffn_cluster) * m->B * m->D)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, reinterpret_cast<unsigned char**>(&m->slice_cnt), ffn_counter_bytes())) != NP_OK)
     return fail(st);
+
+  if (m->B > 1) {
+    // tensor-core path: maps over every weight block the gathers read
+    m->tc = true;
+    const int dt = m->d.dtype;
+    const size_t optin = m->smem_optin - 1024;
+    const int want = env_int("NP_TUNE_MMA_CLUSTERS", 0);
+    const int ffn_mode = m->d.has_gate ? kMmaFfnGated : kMmaFfnUp;
+    if ((e = mma_plan(ffn_mode, dt == NP_BF16, m->D, optin, m->sms, want, &m->plan_ffn)) != cudaSuccess ||
+        (e = mma_plan(kMmaHidden, dt == NP_BF16, m->D, optin, m->sms, want, &m->plan_hid)) != cudaSuccess ||
+        (e = mma_plan(kMmaHeads, dt == NP_BF16, m->H, optin, m->sms, want, &m->plan_heads)) != cudaSuccess)
+      return fail(cuda_fail(e, "mma_plan"));
+    if (m->S > 0 && (e = make_row_map(&m->map_bufs, m->bufs, dt, (uint64_t)m->S * m->nproj * K, m->D)) != cudaSuccess)
+      return fail(cuda_fail(e, "tensor map of the resident rows"));
+    if (m->dn > 0 &&
+        (e = make_row_map(&m->map_dense, m->d.dense_w, dt, (uint64_t)m->dn * m->nproj * F, m->D)) != cudaSuccess)
+      return fail(cuda_fail(e, "tensor map of the dense layers"));
+    if ((e = make_row_map(&m->map_w1, m->d.pred_w1, dt, (uint64_t)m->H, m->D)) != cudaSuccess ||
+        (e = make_row_map(&m->map_w2, m->d.pred_w2, dt, (uint64_t)m->NH * m->C, m->H)) != cudaSuccess)
+      return fail(cuda_fail(e, "tensor map of the predictor"));
+    if ((st = dev_alloc(m, &m->hbase, 2 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
+    if ((st = dev_alloc(m, &m->yacc, 3 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
+    if ((st = dev_alloc(m, &m->zhl, 16 * (size_t)m->H)) != NP_OK) return fail(st);
+    if (env_int("NP_TUNE_VERBOSE", 0) == 1)
+      std::fprintf(stderr, "np: tensor-core ffn %d clusters x %d, %d stages; hidden %d x %d; heads %d x %d\n",
+                   m->plan_ffn.n_clusters, m->plan_ffn.cs, m->plan_ffn.n_stages, m->plan_hid.n_clusters,
+                   m->plan_hid.cs, m->plan_heads.n_clusters, m->plan_heads.cs);
+  }
 
   e = cudaEventCreateWithFlags(&m->ev_set, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
@@ -869,6 +1006,10 @@ np_status np_sparse_mlp(np_model* m, int32_t layer, const float* h_dev, float* y
   if (!aligned16(h_dev) || !aligned16(y_dev)) return arg_fail("h_dev and y_dev must be 16-byte aligned");
   if (layer < m->dn || layer >= m->L) return arg_fail("layer is not a sparse layer");
   if (h_dev == y_dev) return arg_fail("y_dev may not alias h_dev");
+  if (m->tc) {
+    CUDA_TRY(cudaMemsetAsync(y_dev, 0, sizeof(float) * m->B * m->D, m->main));
+    return enqueue_tc_ffn(m, m->main, layer, h_dev, nullptr, nullptr, y_dev, nullptr);
+  }
   return enqueue_sparse(m, layer - m->dn, h_dev, nullptr, y_dev);
 }
 
@@ -877,6 +1018,10 @@ np_status np_dense_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_
   if (!aligned16(h_dev) || !aligned16(y_dev)) return arg_fail("h_dev and y_dev must be 16-byte aligned");
   if (layer < 0 || layer >= m->dn) return arg_fail("layer is not a dense layer");
   if (h_dev == y_dev) return arg_fail("y_dev may not alias h_dev");
+  if (m->tc) {
+    CUDA_TRY(cudaMemsetAsync(y_dev, 0, sizeof(float) * m->B * m->D, m->main));
+    return enqueue_tc_ffn(m, m->main, layer, h_dev, nullptr, nullptr, y_dev, nullptr);
+  }
   return enqueue_dense(m, layer, h_dev, nullptr, y_dev);
 }
 
@@ -895,11 +1040,27 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
     // gather streams, so that transfers start after the first small group.
     // The FFN stream runs dense layers 1..d-1 (once the predictor has read
     // h) and then the sparse FFNs, each after its own rows have arrived.
-    NP_TRY(enqueue_dense(m, 0, h_dev, h_dev, nullptr));
-    NP_TRY(enqueue_pred_hidden(m, h_dev));
+    // Batched: layer l reads base(l) + y(l-1) and adds its y into y(l) (three
+    // rotating accumulators, two rotating bases); the last add is a finish.
+    auto tc_layer = [&](cudaStream_t st, int l) -> np_status {
+      const float* hb = l <= 1 ? h_dev : tc_hbase(m, l - 1);
+      const float* yp = l == 0 ? nullptr : tc_y(m, l - 1);
+      return enqueue_tc_ffn(m, st, l, hb, yp, l >= 1 ? tc_hbase(m, l) : nullptr, tc_y(m, l), tc_y(m, l + 1));
+    };
+    if (m->tc) {
+      CUDA_TRY(cudaMemsetAsync(tc_y(m, 0), 0, sizeof(float) * m->B * m->D, m->main));
+      NP_TRY(tc_layer(m->main, 0));
+      NP_TRY(enqueue_tc_hidden(m, h_dev, tc_y(m, 0)));
+    } else {
+      NP_TRY(enqueue_dense(m, 0, h_dev, h_dev, nullptr));
+      NP_TRY(enqueue_pred_hidden(m, h_dev));
+    }
     CUDA_TRY(cudaEventRecord(m->ev_pre, m->main));
     CUDA_TRY(cudaStreamWaitEvent(m->fs, m->ev_pre, 0));
-    for (int l = 1; l < m->dn; ++l) NP_TRY(enqueue_dense_on(m, m->fs, l, h_dev, h_dev, nullptr));
+    for (int l = 1; l < m->dn; ++l) {
+      if (m->tc) NP_TRY(tc_layer(m->fs, l));
+      else NP_TRY(enqueue_dense_on(m, m->fs, l, h_dev, h_dev, nullptr));
+    }
     m->pending_bits = all_layers(m);
     std::vector<int> moved;
     int s0 = 0;
@@ -930,7 +1091,15 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
     }
     for (int s = 0; s < m->S; ++s) {
       CUDA_TRY(cudaStreamWaitEvent(m->fs, m->ev_layer[s], 0));
-      NP_TRY(enqueue_sparse_on(m, m->fs, s, h_dev, h_dev, nullptr));
+      if (m->tc) NP_TRY(tc_layer(m->fs, m->dn + s));
+      else NP_TRY(enqueue_sparse_on(m, m->fs, s, h_dev, h_dev, nullptr));
+    }
+    if (m->tc) {
+      const int l = m->L - 1;
+      const float* hb = l == 0 ? h_dev : tc_hbase(m, l);  // layer l stored its input h_l there
+      cudaStream_t st = m->fs;
+      NP_TRY(launch(m, NP_KIND_FINISH, st, 0,
+                    [&] { return launch_add(h_dev, hb, tc_y(m, l), m->B * m->D, st); }));
     }
     CUDA_TRY(cudaEventRecord(m->ev_ffn, m->fs));
     CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_ffn, 0));

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace np {
@@ -138,5 +139,52 @@ cudaError_t launch_gather(const MoveLaunch& a, cudaStream_t st);    // host stor
 cudaError_t launch_scatter(const MoveLaunch& a, cudaStream_t st);   // staging -> buffers
 cudaError_t launch_fused(const MoveLaunch& a, cudaStream_t st);     // host store -> buffers
 cudaError_t launch_restore(const MoveLaunch& a, cudaStream_t st);   // previous slot contents back
+
+
+// ---- batched row products on the tensor cores (np_mma.cu) ----------------
+// Modes: FFN with gate (gate, up, down^T), FFN without gate (up, down^T),
+// predictor hidden layer (relu, written as hi/lo 16-bit operands), predictor
+// heads (argmax keys per head of C rows).
+enum { kMmaFfnGated = 0, kMmaFfnUp = 1, kMmaHidden = 2, kMmaHeads = 3 };
+struct MmaArgs {
+  int Kdim;                 // contraction length (d_model, or the hidden width for the heads)
+  int ks_len, cs, n_clusters, B;  // column slice per CTA, cluster size, clusters, sequences (<= 8)
+  const int* row_list;      // row ids (slots) or null for 0..n-1
+  const int* n_rows_dev;    // device row count, or null to use n_rows_host
+  int n_rows_host;
+  int row_cap;              // upper bound of the row count
+  int row_limit;            // row ids must be below this
+  int row_base0, row_base1, row_base2;  // tensor-map row of id 0 for each projection
+  int oob_row;              // a tensor-map row past the end (reads as zeros)
+  const float* hb;          // [B][Kdim] residual base (FFN, hidden)
+  const float* yprev;       // [B][Kdim] previous layer's y, or null
+  float* hb_out;            // hb + yprev is stored here (cluster 0), or null
+  float* y_acc;             // FFN: y is added here, [B][Kdim]
+  float* y_zero;            // cleared by cluster 0 (the next layer's accumulator), or null
+  const uint16_t* zin;      // heads: [16][Kdim] hi/lo input operand
+  uint16_t* zout;           // hidden: [16][zout_stride] hi/lo output
+  int zout_stride;
+  unsigned long long* keys; // heads: [B][n_heads] packed argmax keys
+  int n_heads, C;
+  unsigned long long* keys_zero;  // hidden: cleared before the heads run
+  int n_keys_zero;
+  int n_stages;
+  uint32_t stage_bytes;
+  int* err;
+};
+struct MmaPlan {
+  int cs, ks_len, n_clusters, n_stages;
+  uint32_t stage_bytes;
+  size_t smem;
+};
+// 2-D tensor map over [rows][cols] 16-bit values with a {64, 1} box and
+// 128-byte swizzle (dtype 1 = f16, 2 = bf16).
+cudaError_t make_row_map(CUtensorMap* out, const void* base, int dtype, uint64_t rows, uint64_t cols);
+size_t mma_smem_bytes(int mode, int ks_len, int n_stages);
+cudaError_t mma_plan(int mode, int bf16, int Kdim, size_t smem_optin, int n_sms, int want_clusters, MmaPlan* p);
+cudaError_t launch_mma_rows(int mode, int bf16, const CUtensorMap& map, const MmaArgs& a, const MmaPlan& p,
+                            cudaStream_t st);
+// out[i] = x[i] + y[i] (the residual stream after the last layer)
+cudaError_t launch_add(float* out, const float* x, const float* y, int n, cudaStream_t st);
 
 }  // namespace np

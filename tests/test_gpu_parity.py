@@ -8,8 +8,8 @@ import torch
 import oracle
 from oracle import OracleDecoder
 from tests.parity import FFN_TOL, build_decoder, run_and_compare
-from workloads import (LLAMA7B, LLAMA13B, OPT67B, SMALL_BF16, SMALL_F16, SMALL_OPT, TINY,
-                       make_workload)
+from workloads import (BATCHED7B, LLAMA7B, LLAMA13B, OPT67B, SMALL_BATCHED, SMALL_BF16, SMALL_F16, SMALL_OPT,
+                       TINY, make_workload)
 
 pytestmark = pytest.mark.gpu
 
@@ -31,6 +31,11 @@ SMALL_CASES = {
     "small-f16-staging3": (SMALL_F16, {"staging_rows": 3}),
     "small-bf16-staging7": (SMALL_BF16, {"staging_rows": 7}),
     "small-opt-capped": (SMALL_OPT.replace(k_max=150), {}),
+    # batched decoding on the tensor cores (union of the sequences' sets)
+    "small-batched": (SMALL_BATCHED, {}),
+    "small-batched-fused": (SMALL_BATCHED, {"h2d_mode": "fused"}),
+    "small-batched-b3-f16": (SMALL_BATCHED.replace(batch=3, dtype="f16", k_max=700), {}),
+    "small-batched-nogate": (SMALL_BATCHED.replace(has_gate=False), {}),
 }
 
 
@@ -43,6 +48,15 @@ def test_decode_parity_small(name):
     wl = make_workload(cfg)
     summ = run_and_compare(wl, **kw)
     assert summ["tokens"] == cfg.n_tokens
+    assert summ["max_h_rel"] < FFN_TOL
+
+
+def test_batched_multi_tile(monkeypatch):
+    # one cluster per launch: every product runs several 128-row tiles through
+    # the same cluster (exchange buffers and accumulators reused across tiles)
+    monkeypatch.setenv("NP_TUNE_MMA_CLUSTERS", "1")
+    wl = make_workload(SMALL_BATCHED)
+    summ = run_and_compare(wl, 4)
     assert summ["max_h_rel"] < FFN_TOL
 
 
@@ -195,8 +209,8 @@ def test_read_failure_restores_committed_state():
 # Full-size shapes: every integer output compared in full, buffer bytes on
 # sampled slots, FFN outputs per layer.
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("cfg,tokens", [(LLAMA7B, 3), (LLAMA13B, 2), (OPT67B, 2)],
-                         ids=["llama2-7b", "llama2-13b", "opt-6.7b"])
+@pytest.mark.parametrize("cfg,tokens", [(LLAMA7B, 3), (LLAMA13B, 2), (OPT67B, 2), (BATCHED7B, 2)],
+                         ids=["llama2-7b", "llama2-13b", "opt-6.7b", "llama2-7b-batch8"])
 def test_full_size_sampled(cfg, tokens):
     wl = make_workload(cfg.replace(n_warm=0, n_decode=tokens), device="cuda")
     summ = run_and_compare(wl, tokens, check_buffers=False, sample_slots=64, check_layer_y=True)
