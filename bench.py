@@ -49,12 +49,17 @@ def parse():
     p.add_argument("--warmup", type=int, default=128)
     p.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     p.add_argument("--config", default="llama2-7b-relu")
+    p.add_argument("--persistence", type=float, default=None,
+                   help="override the workload's token-to-token mask persistence (batched sweep)")
     p.add_argument("--h2d-mode", default="fused", choices=["staged", "fused"])
     p.add_argument("--cpu-sample-tokens", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--profile-case", action="store_true",
-                   help="run the small capture case used for ncu (8-token 7B workload, standalone calls) and exit")
+                   help="run the small capture case used for ncu (8-token workload of --config, 3 decode steps, "
+                        "then standalone calls) and exit")
+    p.add_argument("--layers", type=int, default=None,
+                   help="with --profile-case: keep only this many layers (same shapes per layer)")
     return p.parse_args()
 
 
@@ -188,7 +193,7 @@ def isolated_kernels(dec, torch, cfg, reps=5):
     """Standalone launches (no concurrent host-link traffic), events on the
     launching stream: sparse FFN over every sparse layer, dense layer 0, and
     the predictor, each with its algorithmic bytes."""
-    h = torch.randn(cfg.d_model, device="cuda")
+    h = torch.randn(cfg.batch * cfg.d_model, device="cuda")
     out = {}
     st = dec.main_stream
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -222,15 +227,18 @@ def isolated_kernels(dec, torch, cfg, reps=5):
     return out
 
 
-def profile_case():
-    """Small capture case for ncu: 8-token 7B workload, 3 decoded tokens,
-    then standalone calls of every kernel kind."""
+def profile_case(args):
+    """Small capture case for ncu: 8-step workload of --config (optionally
+    cut to --layers layers), 3 decoded steps, then standalone calls of every
+    kernel kind: two sparse FFNs, dense layer 0, predictor, delta, scatter."""
     import torch
     from sparse_activation_decode_gb300 import decoder_for
     from sparse_activation_decode_gb300.build import build
-    from workloads import LLAMA7B, make_workload
+    from workloads import CONFIGS, make_workload
     build()
-    cfg = LLAMA7B.replace(n_warm=0, n_decode=8)
+    cfg = CONFIGS[args.config].replace(n_warm=0, n_decode=8)
+    if args.layers:
+        cfg = cfg.replace(n_layers=args.layers)
     wl = make_workload(cfg, device="cuda")
     dec = decoder_for(wl)
     xs = wl.x.cuda()
@@ -238,8 +246,9 @@ def profile_case():
         dec.decode_token(xs[t].clone())
     torch.cuda.synchronize()
     h = xs[4].reshape(-1).clone()
-    dec.sparse_mlp(7, h)
-    dec.sparse_mlp(8, h)
+    l1, l2 = (7, 8) if cfg.n_layers > 8 else (cfg.n_dense + 1, cfg.n_dense + 2)
+    dec.sparse_mlp(l1, h)
+    dec.sparse_mlp(l2, h)
     dec.dense_mlp(0, h)
     ids = dec.predict(h)
     dec.delta(ids, -1)
@@ -271,8 +280,12 @@ def run_cuda(args):
     peaks = load_peaks()
     W, K = args.warmup, args.steps
     base = CONFIGS[args.config]
-    T = min(W + 3 * K, base.n_centroids - 24 if base.n_centroids else 10 ** 9)
+    if args.persistence is not None:
+        base = base.replace(persistence=args.persistence)
+    span = (base.batch - 1) * base.phase_step + 24
+    T = min(W + 3 * K, base.n_centroids - span if base.n_centroids else 10 ** 9)
     cfg = base.replace(n_warm=0, n_decode=T, seed=base.seed + 7919 * rank)
+    B = cfg.batch
     t0 = time.time()
     wl = make_workload(cfg, device="cuda")
     gen_s = time.time() - t0
@@ -302,12 +315,15 @@ def run_cuda(args):
         torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
     launches = dec.launch_count() - n0
+    # the host link is shared with other tenants of the machine: measure it
+    # again right after the timed region
+    h2d_after = h2d_peak_gbs(torch) if rank == 0 else None
     ms_t = torch.tensor([ms], device="cuda")
     if world > 1:
         dist.barrier()
         dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
     ms_max = float(ms_t.item())
-    value = world * K / (ms_max * 1e-3)
+    value = world * K * B / (ms_max * 1e-3)     # tokens: sequences x steps
 
     # live per-kernel durations (events on each kernel's own stream); few
     # enough tokens that the library keeps every launch in its timeline
@@ -318,6 +334,8 @@ def run_cuda(args):
     for k in range(KP):
         dec.decode_token(hs2[k])
     timeline = dec.timeline()
+    counts = dec.counts()
+    union_density = float(sum(c[0] for c in counts)) / (len(counts) * cfg.d_ff) if counts else None
     prof = dec.profile()
     dec.set_profiling(False)
     table = kernel_table(prof, peaks, h2d_peak or 0.0)
@@ -340,7 +358,7 @@ def run_cuda(args):
         ev1.record(main)
         torch.cuda.synchronize()
         ms_e = ev0.elapsed_time(ev1)
-        e2e = {"value": round(world * K / (ms_e * 1e-3), 2), "unit": "tok/s",
+        e2e = {"value": round(world * K * B / (ms_e * 1e-3), 2), "unit": "tok/s",
                "h2d_bytes_per_step": B * D * 4, "d2h_bytes_per_step": B * D * 4}
     dec.close()
 
@@ -383,16 +401,17 @@ def run_cuda(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16 weights, f32 accumulate", "data": "synthetic (seeded; shapes of the pages' workloads)",
+        "dtype": f"{cfg.dtype} weights, f32 accumulate", "data": "synthetic (seeded; shapes of the pages' workloads)",
         "config": {"workload": cfg.name, "layers": cfg.n_layers, "dense_prefix": cfg.n_dense,
                    "d_model": cfg.d_model, "d_ff": cfg.d_ff, "k_max": cfg.k_max, "centroids": cfg.n_centroids,
                    "combine": cfg.combine, "persistence": cfg.persistence, "batch": cfg.batch,
+                   "density": cfg.density, "ffn": "tcgen05 tensor cores" if cfg.batch > 1 else "CUDA cores",
                    "h2d_mode": args.h2d_mode, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (per-token weights ~2 GB > 129 MB)"},
         "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": table,
-        "h2d_peak_gbs": round(h2d_peak, 1), "host_link_busy_ms_per_token": round(link_ms / KP, 4),
+        "h2d_peak_gbs": round(h2d_peak, 1), "h2d_peak_after_gbs": round(h2d_after, 1), "host_link_busy_ms_per_token": round(link_ms / KP, 4),
         "profiled_tokens": KP,
-        "gpu_launches": launches,
+        "gpu_launches": launches, "active_density_last_step": round(union_density, 4) if union_density else None,
         "clocks": clk.summary(), "e2e": e2e, "workload_gen_s": round(gen_s, 1),
     }
     return line, wl
@@ -425,7 +444,7 @@ def cores_used():
 def main():
     args = parse()
     if args.profile_case:
-        return profile_case()
+        return profile_case(args)
     if args.impl == "reference":
         return run_reference(args)
     res = run_cuda(args)
@@ -434,9 +453,11 @@ def main():
     line, wl = res
     if not args.no_cpu_baseline and args.gpus == 1 and int(os.environ.get("WORLD_SIZE", "1")) == 1:
         n, sec = run_oracle_tokens(wl, args.cpu_sample_tokens, budget_s=45)
-        line["cpu_baseline"] = {"value": round(n / sec, 4), "unit": "tok/s", "cores": cores_used(),
+        nb = wl.cfg.batch
+        line["cpu_baseline"] = {"value": round(n * nb / sec, 4), "unit": "tok/s", "cores": cores_used(),
                                 "kind": "oracle",
-                                "sample": f"{n} tokens of {wl.cfg.name} after a cold-start token, fp64 numpy"}
+                                "sample": f"{n} steps x {nb} sequences of {wl.cfg.name} after a cold-start step, "
+                                          "fp64 numpy"}
     print(json.dumps(line), flush=True)
 
 
@@ -449,6 +470,8 @@ def run_reference(args):
     if rank != 0:
         return
     base = CONFIGS[args.config]
+    if args.persistence is not None:
+        base = base.replace(persistence=args.persistence)
     n_tok = max(1, min(args.steps, 8))
     cfg = base.replace(n_warm=0, n_decode=n_tok + 1)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
@@ -456,13 +479,13 @@ def run_reference(args):
     wl.dense_w = wl.dense_w.cpu() if wl.dense_w is not None else None
     wl.pred_w1, wl.pred_w2 = wl.pred_w1.cpu(), wl.pred_w2.cpu()
     n, sec = run_oracle_tokens(wl, n_tok, budget_s=120)
-    v = n / sec
+    v = n * cfg.batch / sec
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tok/s", "n_gpus": args.gpus,
             "steps": n, "warmup": 1, "ms_per_step": round(1e3 * sec / n, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": cfg.name},
             "cpu_baseline": {"value": round(v, 4), "unit": "tok/s", "cores": cores_used(), "kind": "oracle",
-                             "sample": f"{n} tokens of {cfg.name} after a cold-start token"},
+                             "sample": f"{n} steps x {cfg.batch} sequences of {cfg.name} after a cold-start step"},
             "e2e": {"value": round(v, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

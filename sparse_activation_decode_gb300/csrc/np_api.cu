@@ -93,7 +93,8 @@ struct np_model {
   // launch plans, residual bases [2][B][D], y accumulators [3][B][D], the
   // predictor hidden layer as hi/lo 16-bit operands [16][H]
   bool tc = false;
-  CUtensorMap map_bufs{}, map_dense{}, map_w1{}, map_w2{};
+  RowMaps map_bufs{}, map_dense{}, map_w1{}, map_w2{};
+  int* slot_hw = nullptr;  // [S] one past the highest occupied slot
   MmaPlan plan_ffn{}, plan_hid{}, plan_heads{};
   float* hbase = nullptr;
   float* yacc = nullptr;
@@ -262,7 +263,7 @@ np_status enqueue_sparse(np_model* m, int s, const float* h_in, float* h_out, fl
 float* tc_hbase(np_model* m, int i) { return m->hbase + (size_t)(i & 1) * m->B * m->D; }
 float* tc_y(np_model* m, int i) { return m->yacc + (size_t)(i % 3) * m->B * m->D; }
 
-np_status enqueue_mma(np_model* m, cudaStream_t st, int kind, int mode, const CUtensorMap& map, const MmaPlan& p,
+np_status enqueue_mma(np_model* m, cudaStream_t st, int kind, int mode, const RowMaps& map, const MmaPlan& p,
                       MmaArgs& a, int64_t fixed_bytes) {
   a.B = m->B;
   a.err = m->err;
@@ -290,8 +291,6 @@ np_status enqueue_tc_ffn(np_model* m, cudaStream_t st, int l, const float* hb, c
     a.row_base2 = base + (1 + g) * m->F;
     a.n_rows_host = m->F;
     a.row_cap = m->F;
-    a.row_limit = m->F;
-    a.oob_row = m->dn * m->nproj * m->F;
     return enqueue_mma(m, st, NP_KIND_DENSE, mode, m->map_dense, m->plan_ffn, a,
                        (int64_t)m->nproj * m->F * m->row_bytes);
   }
@@ -300,11 +299,10 @@ np_status enqueue_tc_ffn(np_model* m, cudaStream_t st, int l, const float* hb, c
   a.row_base0 = base;
   a.row_base1 = base + m->K;
   a.row_base2 = base + (1 + g) * m->K;
-  a.row_list = m->active_slot + (size_t)s * m->K;
-  a.n_rows_dev = m->counts + (size_t)s * 4;
+  // slot order over [0, high-water mark); free slots are skipped
+  a.occ_inv = m->inv + (size_t)s * m->K;
+  a.n_rows_dev = m->slot_hw + s;
   a.row_cap = m->K;
-  a.row_limit = m->K;
-  a.oob_row = m->S * m->nproj * m->K;
   return enqueue_mma(m, st, NP_KIND_FFN, mode, m->map_bufs, m->plan_ffn, a, 0);
 }
 
@@ -317,8 +315,6 @@ np_status enqueue_tc_hidden(np_model* m, const float* hb, const float* yprev) {
   a.yprev = yprev;
   a.n_rows_host = m->H;
   a.row_cap = m->H;
-  a.row_limit = m->H;
-  a.oob_row = m->H;
   a.zout = m->zhl;
   a.zout_stride = m->H;
   a.keys_zero = m->keys;
@@ -334,8 +330,6 @@ np_status enqueue_tc_heads(np_model* m, int h0, int h1) {
   a.row_base0 = h0 * m->C;
   a.n_rows_host = (h1 - h0) * m->C;
   a.row_cap = a.n_rows_host;
-  a.row_limit = a.n_rows_host;
-  a.oob_row = m->NH * m->C;
   a.zin = m->zhl;
   a.keys = m->keys;
   a.n_heads = m->NH;
@@ -529,6 +523,7 @@ SetLaunch set_args(np_model* m, int first_sparse, int n_layers) {
   a.dout_s = m->dout_s;
   a.ls_old = m->ls_old;
   a.totals = m->totals;
+  a.slot_hw = m->slot_hw;
   a.err = m->err;
   return a;
 }
@@ -813,14 +808,15 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
         (e = mma_plan(kMmaHidden, dt == NP_BF16, m->D, optin, m->sms, want, &m->plan_hid)) != cudaSuccess ||
         (e = mma_plan(kMmaHeads, dt == NP_BF16, m->H, optin, m->sms, want, &m->plan_heads)) != cudaSuccess)
       return fail(cuda_fail(e, "mma_plan"));
-    if (m->S > 0 && (e = make_row_map(&m->map_bufs, m->bufs, dt, (uint64_t)m->S * m->nproj * K, m->D)) != cudaSuccess)
+    if (m->S > 0 && (e = make_row_maps(&m->map_bufs, m->bufs, dt, (uint64_t)m->S * m->nproj * K, m->D)) != cudaSuccess)
       return fail(cuda_fail(e, "tensor map of the resident rows"));
     if (m->dn > 0 &&
-        (e = make_row_map(&m->map_dense, m->d.dense_w, dt, (uint64_t)m->dn * m->nproj * F, m->D)) != cudaSuccess)
+        (e = make_row_maps(&m->map_dense, m->d.dense_w, dt, (uint64_t)m->dn * m->nproj * F, m->D)) != cudaSuccess)
       return fail(cuda_fail(e, "tensor map of the dense layers"));
-    if ((e = make_row_map(&m->map_w1, m->d.pred_w1, dt, (uint64_t)m->H, m->D)) != cudaSuccess ||
-        (e = make_row_map(&m->map_w2, m->d.pred_w2, dt, (uint64_t)m->NH * m->C, m->H)) != cudaSuccess)
+    if ((e = make_row_maps(&m->map_w1, m->d.pred_w1, dt, (uint64_t)m->H, m->D)) != cudaSuccess ||
+        (e = make_row_maps(&m->map_w2, m->d.pred_w2, dt, (uint64_t)m->NH * m->C, m->H)) != cudaSuccess)
       return fail(cuda_fail(e, "tensor map of the predictor"));
+    if ((st = dev_alloc(m, &m->slot_hw, Sa)) != NP_OK) return fail(st);
     if ((st = dev_alloc(m, &m->hbase, 2 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
     if ((st = dev_alloc(m, &m->yacc, 3 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
     if ((st = dev_alloc(m, &m->zhl, 16 * (size_t)m->H)) != NP_OK) return fail(st);

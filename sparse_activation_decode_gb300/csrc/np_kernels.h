@@ -109,6 +109,7 @@ struct SetLaunch {
   int* dout_s;            // [S][K] slot each outgoing neuron held
   int* ls_old;            // [S][K] previous last use of each active neuron
   unsigned long long* totals;  // running sums: |A|, |D_in|, |D_out|, dropped
+  int* slot_hw;           // [S] one past the highest occupied slot (an upper bound), or null
   int* err;
 };
 cudaError_t launch_set(const SetLaunch& a, cudaStream_t st);
@@ -149,12 +150,11 @@ enum { kMmaFfnGated = 0, kMmaFfnUp = 1, kMmaHidden = 2, kMmaHeads = 3 };
 struct MmaArgs {
   int Kdim;                 // contraction length (d_model, or the hidden width for the heads)
   int ks_len, cs, n_clusters, B;  // column slice per CTA, cluster size, clusters, sequences (<= 8)
-  const int* row_list;      // row ids (slots) or null for 0..n-1
-  const int* n_rows_dev;    // device row count, or null to use n_rows_host
+  const int* occ_inv;       // row r is used only if occ_inv[r] >= 0 (slot occupancy), or null: all rows
+  const int* n_rows_dev;    // device row count (rows 0..n-1), or null to use n_rows_host
   int n_rows_host;
   int row_cap;              // upper bound of the row count
-  int row_limit;            // row ids must be below this
-  int row_base0, row_base1, row_base2;  // tensor-map row of id 0 for each projection
+  int row_base0, row_base1, row_base2;  // tensor-map row of row 0 for each projection
   int oob_row;              // a tensor-map row past the end (reads as zeros)
   const float* hb;          // [B][Kdim] residual base (FFN, hidden)
   const float* yprev;       // [B][Kdim] previous layer's y, or null
@@ -177,12 +177,15 @@ struct MmaPlan {
   uint32_t stage_bytes;
   size_t smem;
 };
-// 2-D tensor map over [rows][cols] 16-bit values with a {64, 1} box and
-// 128-byte swizzle (dtype 1 = f16, 2 = bf16).
-cudaError_t make_row_map(CUtensorMap* out, const void* base, int dtype, uint64_t rows, uint64_t cols);
+// Two 2-D tensor maps over [rows][cols] 16-bit values with 128-byte swizzle
+// and boxes of {64, 32} and {64, 8} (dtype 1 = f16, 2 = bf16).
+struct RowMaps {
+  CUtensorMap m32, m8;
+};
+cudaError_t make_row_maps(RowMaps* out, const void* base, int dtype, uint64_t rows, uint64_t cols);
 size_t mma_smem_bytes(int mode, int ks_len, int n_stages);
 cudaError_t mma_plan(int mode, int bf16, int Kdim, size_t smem_optin, int n_sms, int want_clusters, MmaPlan* p);
-cudaError_t launch_mma_rows(int mode, int bf16, const CUtensorMap& map, const MmaArgs& a, const MmaPlan& p,
+cudaError_t launch_mma_rows(int mode, int bf16, const RowMaps& maps, const MmaArgs& a, const MmaPlan& p,
                             cudaStream_t st);
 // out[i] = x[i] + y[i] (the residual stream after the last layer)
 cudaError_t launch_add(float* out, const float* x, const float* y, int n, cudaStream_t st);

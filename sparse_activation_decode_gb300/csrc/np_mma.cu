@@ -17,9 +17,12 @@
 // Work split: thread-block clusters of CS CTAs; the clusters split the row
 // list evenly; inside a cluster CTA r owns the column slice
 // [r*Kdim/CS, (r+1)*Kdim/CS) of every row.  For each tile of 128 rows:
-//   1. a producer warp gathers the tile's rows of the slice, 64 columns at a
-//      time, with tensor-map gather loads (four arbitrary rows per copy,
-//      rows past the list's end read as zeros) into a shared-memory ring;
+//   1. a producer warp loads the tile's rows of the slice, 64 columns at a
+//      time, with 2-D tensor-map boxes of 32 and 8 rows (4 KB / 1 KB per
+//      copy: the copy engine's cost is per request, so requests stay large)
+//      into a shared-memory ring.  Sparse layers are walked in slot order,
+//      over slots [0, high-water mark) of the resident buffers, and a slot
+//      whose inverse map entry is -1 (free) contributes nothing;
 //   2. one thread issues the MMAs of the slice for gate and up;
 //   3. four epilogue warps read the partial dot products from tensor memory
 //      and send them to the CTA of the cluster that owns the row (remote
@@ -53,13 +56,25 @@ constexpr int kMmaThreads = 192;     // warp 0 producer, warp 1 MMA, warps 2-5 e
 constexpr int kTileRows = 128;
 constexpr uint32_t kTmemCols = 256;
 constexpr int kMaxStages = 16;
-constexpr uint32_t kSmemHeader = 14336;  // barriers, rows, exchange buffers, activation operand
+constexpr uint32_t kSmemHeader = 18432;  // barriers, exchange buffers, activation operand, y staging
 
 // barrier slots
 constexpr int kBarFull = 0, kBarEmpty = 16, kBarAccFull = 32, kBarAccEmpty = 33, kBarXReady = 34, kBarRed = 35,
-              kBarXFree = 36, kBarHFull = 37, kBarYFull = 38, kBarDone = 39;
+              kBarXFree = 36, kBarHFull = 37, kBarYFull = 38, kBarDone = 39, kBarSS = 40;
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// AND of a flag over the 128 epilogue threads (all of them must arrive).
+__device__ __forceinline__ bool epi_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, 1, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
 
 template <bool BF16> __device__ __forceinline__ uint16_t to16(float v);
 template <> __device__ __forceinline__ uint16_t to16<true>(float v) {
@@ -93,7 +108,8 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 template <int MODE, bool BF16>
-__global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_constant__ CUtensorMap tmap,
+__global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_constant__ CUtensorMap tmap32,
+                                                                  const __grid_constant__ CUtensorMap tmap8,
                                                                   const MmaArgs a) {
   constexpr bool kFfn = MODE == kMmaFfnGated || MODE == kMmaFfnUp;
   constexpr bool kGated = MODE == kMmaFfnGated;
@@ -107,7 +123,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
   unsigned char* sm = smem_raw + (sbase - raw);
   volatile int* misc = reinterpret_cast<volatile int*>(sm + 512);  // [0] tmem base, [1] abort
   float* ssred = reinterpret_cast<float*>(sm + 512 + 64);          // [4 warps][8]
-  int* rows_s = reinterpret_cast<int*>(sm + 1024);                 // [128]
+  const uint32_t ssx_a = sbase + 512 + 256;                        // [cs][8] slice sums of squares
+  const float* ssx = reinterpret_cast<const float*>(sm + 512 + 256);
+  float* ystage = reinterpret_cast<float*>(sm + 14336);            // [8][128] y of one M tile
   float* recv = reinterpret_cast<float*>(sm + 2048);               // [128][16]
   const uint32_t recv_a = sbase + 2048;
   const uint32_t hbuf_a = sbase + 10240;                           // 4 KB activation operand
@@ -134,11 +152,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
     mbar_init(b + kBarAccFull, 1);
     mbar_init(b + kBarAccEmpty, 128);
     mbar_init(b + kBarXReady, 128);
-    mbar_init(b + kBarRed, 128);
-    mbar_init(b + kBarXFree, 128);
-    mbar_init(b + kBarHFull, 128);
+    // cross-CTA barriers count one arrive per epilogue warp of the cluster
+    // that writes (each warp's 32 rows have a single owner)
+    mbar_init(b + kBarRed, 4);
+    mbar_init(b + kBarXFree, 4);
+    mbar_init(b + kBarHFull, 4);
     mbar_init(b + kBarYFull, 1);
     mbar_init(b + kBarDone, 1);
+    mbar_init(b + kBarSS, (uint32_t)a.cs);
     misc[1] = 0;
     fence_barrier_init();
   }
@@ -168,67 +189,49 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
     for (int tile = 0; tile < n_tiles && ok; ++tile) {
       const int t0 = r_begin + tile * kTileRows;
       const int nr = min(kTileRows, r_end - t0);
-      __syncwarp();
-      for (int j = lane; j < kTileRows; j += 32) {
-        int id = -1;
-        if (j < nr) {
-          id = a.row_list ? a.row_list[t0 + j] : t0 + j;
-          if ((unsigned)id >= (unsigned)a.row_limit) {
-            atomicExch(a.err, kDevErrBounds);
-            id = -1;
-          }
-        }
-        rows_s[j] = id;
-      }
-      __syncwarp();
-      const int ng4 = (nr + 3) >> 2;
+      // boxes: n32 of 32 rows, then 8-row boxes up to a multiple of 8 rows
+      // (first product) or of 16 rows (down projection: whole MMA K steps)
+      const int n32 = nr >> 5;
+      const int nb_gu = n32 + ((((nr + 7) & ~7) - 32 * n32) >> 3);
+      const int rows_gu = 32 * n32 + 8 * (nb_gu - n32);
       for (int kb = 0; kb < n_kb && ok; ++kb) {
         const int s = (int)(it % (uint32_t)NS);
         int w = 1;
         if (lane == 0) {
           w = wait_phase(bar(kBarEmpty + s), ((it / NS) & 1u) ^ 1u, abort, a.err);
-          if (w) mbar_arrive_expect_tx_a(bar(kBarFull + s), (uint32_t)(kProj * ng4 * 512));
+          if (w) mbar_arrive_expect_tx_a(bar(kBarFull + s), (uint32_t)(kProj * rows_gu * 128));
         }
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
         if (!ok) break;
         const uint32_t dst0 = ring_a + (uint32_t)s * stage_bytes;
         const int x = slice0 + kb * 64;
-        for (int q = lane; q < kProj * ng4; q += 32) {
-          const int p = q / ng4, g = q - p * ng4;
-          const int rb = p == 0 ? a.row_base0 : a.row_base1;
-          int rr[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int id = rows_s[4 * g + u];
-            rr[u] = id >= 0 ? rb + id : a.oob_row;
-          }
-          tma_gather4(dst0 + (uint32_t)p * 16384u + (uint32_t)g * 512u, &tmap, x, rr[0], rr[1], rr[2], rr[3],
+        for (int q = lane; q < kProj * nb_gu; q += 32) {
+          const int p = q / nb_gu, b = q - p * nb_gu;
+          const int rb = (p == 0 ? a.row_base0 : a.row_base1) + t0;
+          const int r = b < n32 ? 32 * b : 32 * n32 + 8 * (b - n32);
+          tma_load_2d(dst0 + (uint32_t)p * 16384u + (uint32_t)r * 128u, b < n32 ? &tmap32 : &tmap8, x, rb + r,
                       bar(kBarFull + s), pol);
         }
         ++it;
       }
       if (kFfn) {
-        const int ng16 = ((nr + 15) >> 4) * 4;  // 4-row groups covering the 16-row K steps
+        const int nb_dt = n32 + ((((nr + 15) & ~15) - 32 * n32) >> 3);
+        const int rows_dt = 32 * n32 + 8 * (nb_dt - n32);
         for (int mt = 0; mt < n_mt && ok; ++mt) {
           const int s = (int)(it % (uint32_t)NS);
           int w = 1;
           if (lane == 0) {
             w = wait_phase(bar(kBarEmpty + s), ((it / NS) & 1u) ^ 1u, abort, a.err);
-            if (w) mbar_arrive_expect_tx_a(bar(kBarFull + s), (uint32_t)(2 * ng16 * 512));
+            if (w) mbar_arrive_expect_tx_a(bar(kBarFull + s), (uint32_t)(2 * rows_dt * 128));
           }
           ok = __shfl_sync(0xffffffffu, w, 0) != 0;
           if (!ok) break;
           const uint32_t dst0 = ring_a + (uint32_t)s * stage_bytes;
-          for (int q = lane; q < 2 * ng16; q += 32) {
-            const int grp = q / ng16, g = q - grp * ng16;
-            int rr[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int id = rows_s[4 * g + u];
-              rr[u] = id >= 0 ? a.row_base2 + id : a.oob_row;
-            }
-            tma_gather4(dst0 + (uint32_t)grp * 16384u + (uint32_t)g * 512u, &tmap, slice0 + mt * 128 + grp * 64,
-                        rr[0], rr[1], rr[2], rr[3], bar(kBarFull + s), pol);
+          for (int q = lane; q < 2 * nb_dt; q += 32) {
+            const int grp = q / nb_dt, b = q - grp * nb_dt;
+            const int r = b < n32 ? 32 * b : 32 * n32 + 8 * (b - n32);
+            tma_load_2d(dst0 + (uint32_t)grp * 16384u + (uint32_t)r * 128u, b < n32 ? &tmap32 : &tmap8,
+                        slice0 + mt * 128 + grp * 64, a.row_base2 + t0 + r, bar(kBarFull + s), pol);
           }
           ++it;
         }
@@ -311,70 +314,106 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
 
     // prologue: input operand of this CTA's column slice
     if (MODE == kMmaHeads) {
-      const int half = ks / 2;
-      for (int idx = e; idx < 16 * half; idx += 128) {
-        const int nn = idx / half, kp = idx - nn * half;
-        const uint32_t wv = reinterpret_cast<const uint32_t*>(a.zin + (size_t)nn * Kd + slice0)[kp];
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(xb_a + kmajor_off(nn, 2 * kp, 16)), "r"(wv) : "memory");
+      uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kSmemHeader);
+      const int q4 = ks / 8;  // 16-byte chunks per operand row
+      for (int idx = e; idx < 16 * q4; idx += 128) {
+        const int nn = idx / q4, c = idx - nn * q4;
+        const uint4 wv = reinterpret_cast<const uint4*>(a.zin + (size_t)nn * Kd + slice0)[c];
+        *reinterpret_cast<uint4*>(xw + (kmajor_off(nn, 8 * c, 16) >> 2)) = wv;
       }
     } else {
+      // sum of squares of h = hb + yprev over this CTA's slice; the CTAs of
+      // the cluster cover every column once, so the slice sums are exchanged
+      // and added in rank order
       float ss[8];
 #pragma unroll
       for (int b = 0; b < 8; ++b) ss[b] = 0.f;
-      const int K4 = Kd / 4;
+      const int S4 = ks / 4;
+      for (int i = e; i < S4; i += 128) {
+        float4 v[8];
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        if (b < B) {
-          const float4* hb4 = reinterpret_cast<const float4*>(a.hb + (size_t)b * Kd);
-          const float4* yp4 = a.yprev ? reinterpret_cast<const float4*>(a.yprev + (size_t)b * Kd) : nullptr;
-          float acc = 0.f;
-          for (int i = e; i < K4; i += 128) {
-            float4 v = hb4[i];
-            if (yp4) {
-              const float4 w = yp4[i];
-              v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+        for (int b = 0; b < 8; ++b) {
+          v[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (b < B) v[b] = reinterpret_cast<const float4*>(a.hb + (size_t)b * Kd + slice0)[i];
+        }
+        if (a.yprev) {
+#pragma unroll
+          for (int b = 0; b < 8; ++b)
+            if (b < B) {
+              const float4 w = reinterpret_cast<const float4*>(a.yprev + (size_t)b * Kd + slice0)[i];
+              v[b].x += w.x; v[b].y += w.y; v[b].z += w.z; v[b].w += w.w;
             }
-            acc = fmaf(v.x, v.x, acc);
-            acc = fmaf(v.y, v.y, acc);
-            acc = fmaf(v.z, v.z, acc);
-            acc = fmaf(v.w, v.w, acc);
-          }
-          ss[b] = warp_sum(acc);
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          ss[b] = fmaf(v[b].x, v[b].x, ss[b]);
+          ss[b] = fmaf(v[b].y, v[b].y, ss[b]);
+          ss[b] = fmaf(v[b].z, v[b].z, ss[b]);
+          ss[b] = fmaf(v[b].w, v[b].w, ss[b]);
         }
       }
+#pragma unroll
+      for (int b = 0; b < 8; ++b) ss[b] = warp_sum(ss[b]);
       if (lane == 0)
 #pragma unroll
         for (int b = 0; b < 8; ++b) ssred[ew * 8 + b] = ss[b];
       epi_sync();
+      if (e == 0) {
+        float part[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) part[b] = ssred[b] + ssred[8 + b] + ssred[16 + b] + ssred[24 + b];
+        for (int dst = 0; dst < cs; ++dst) {
+          const uint32_t ra = cluster_map(ssx_a + rank * 32u, (uint32_t)dst);
+          st_cluster_f4(ra, part[0], part[1], part[2], part[3]);
+          st_cluster_f4(ra + 16, part[4], part[5], part[6], part[7]);
+        }
+        fence_acq_rel_cluster();
+        for (int dst = 0; dst < cs; ++dst) mbar_arrive_cluster_relaxed(cluster_map(bar(kBarSS), (uint32_t)dst));
+      }
+      const bool ss_ok = wait_phase(bar(kBarSS), 0, abort, a.err);
       float inv[8];
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
-        const float tot = ssred[b] + ssred[8 + b] + ssred[16 + b] + ssred[24 + b];
-        inv[b] = rsqrtf(tot / (float)Kd + 1e-6f);
+        float tot = 0.f;
+        for (int r = 0; r < cs; ++r) tot += ssx[r * 8 + b];
+        inv[b] = ss_ok ? rsqrtf(tot / (float)Kd + 1e-6f) : 0.f;
       }
-      const int half = ks / 2;
-      for (int idx = e; idx < 16 * half; idx += 128) {
-        const int nn = idx / half, kp = idx - nn * half;
-        const int b = nn & 7;
-        uint32_t wv = 0u;
-        if (b < B) {
-          const int d = slice0 + 2 * kp;
-          float2 v = *reinterpret_cast<const float2*>(a.hb + (size_t)b * Kd + d);
-          if (a.yprev) {
-            const float2 w = *reinterpret_cast<const float2*>(a.yprev + (size_t)b * Kd + d);
-            v.x += w.x;
-            v.y += w.y;
-          }
-          if (nn < 8 && cid == 0) {
-            if (a.hb_out) *reinterpret_cast<float2*>(a.hb_out + (size_t)b * Kd + d) = v;
-            if (a.y_zero) *reinterpret_cast<float2*>(a.y_zero + (size_t)b * Kd + d) = make_float2(0.f, 0.f);
-          }
-          uint16_t h0, l0, h1, l1;
-          split16<BF16>(v.x * inv[b], h0, l0);
-          split16<BF16>(v.y * inv[b], h1, l1);
-          wv = nn < 8 ? ((uint32_t)h0 | ((uint32_t)h1 << 16)) : ((uint32_t)l0 | ((uint32_t)l1 << 16));
+      // x = h * inv as hi/lo operand rows (row b = hi, row 8 + b = lo), four
+      // columns per step; cluster 0 also stores h and clears the next y
+      uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kSmemHeader);
+      for (int i = e; i < S4; i += 128) {
+        const int k = 4 * i, d = slice0 + k;
+        float4 v[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          v[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (b < B) v[b] = *reinterpret_cast<const float4*>(a.hb + (size_t)b * Kd + d);
         }
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(xb_a + kmajor_off(nn, 2 * kp, 16)), "r"(wv) : "memory");
+        if (a.yprev) {
+#pragma unroll
+          for (int b = 0; b < 8; ++b)
+            if (b < B) {
+              const float4 w = *reinterpret_cast<const float4*>(a.yprev + (size_t)b * Kd + d);
+              v[b].x += w.x; v[b].y += w.y; v[b].z += w.z; v[b].w += w.w;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (cid == 0 && b < B) {
+            if (a.hb_out) *reinterpret_cast<float4*>(a.hb_out + (size_t)b * Kd + d) = v[b];
+            if (a.y_zero) *reinterpret_cast<float4*>(a.y_zero + (size_t)b * Kd + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          uint16_t hi[4], lo[4];
+          split16<BF16>(v[b].x * inv[b], hi[0], lo[0]);
+          split16<BF16>(v[b].y * inv[b], hi[1], lo[1]);
+          split16<BF16>(v[b].z * inv[b], hi[2], lo[2]);
+          split16<BF16>(v[b].w * inv[b], hi[3], lo[3]);
+          // columns k..k+3 share one 16-byte chunk of their operand row
+          xw[kmajor_off(b, k, 16) >> 2] = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
+          xw[kmajor_off(b, k + 2, 16) >> 2] = (uint32_t)hi[2] | ((uint32_t)hi[3] << 16);
+          xw[kmajor_off(8 + b, k, 16) >> 2] = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
+          xw[kmajor_off(8 + b, k + 2, 16) >> 2] = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);
+        }
       }
       if (MODE == kMmaHidden && a.keys_zero && blockIdx.x == 0)
         for (int i = e; i < a.n_keys_zero; i += 128) a.keys_zero[i] = 0ull;
@@ -399,7 +438,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
       tc_fence_before();
       mbar_arrive_local(bar(kBarAccEmpty));
       if (tile > 0) {
-        ok = wait_phase(bar(kBarXFree), (uint32_t)(tile - 1) & 1u, abort, a.err);
+        // the owner has read this CTA's previous partials: it broadcast h
+        // after reading them (FFN), or released the buffer (other modes)
+        ok = wait_phase(bar(kFfn ? kBarHFull : kBarXFree), (uint32_t)(tile - 1) & 1u, abort, a.err);
         if (!ok) break;
       }
       {
@@ -410,7 +451,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
           st_cluster_f4(dst + 32, u[0] + u[8], u[1] + u[9], u[2] + u[10], u[3] + u[11]);
           st_cluster_f4(dst + 48, u[4] + u[12], u[5] + u[13], u[6] + u[14], u[7] + u[15]);
         }
-        mbar_arrive_cluster(cluster_map(bar(kBarRed), owner));
+        __syncwarp();
+        if (lane == 0) {
+          fence_acq_rel_cluster();
+          mbar_arrive_cluster_relaxed(cluster_map(bar(kBarRed), owner));
+        }
       }
       if (!reducer) continue;
       ok = wait_phase(bar(kBarRed), (uint32_t)tile & 1u, abort, a.err);
@@ -426,8 +471,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
           if (kGated) bv[j] += r[8 + j];
         }
       }
-      for (int src = 0; src < cs; ++src) mbar_arrive_cluster(cluster_map(bar(kBarXFree), (uint32_t)src));
-      const bool valid = t < nr;
+      if (!kFfn) {
+        __syncwarp();
+        if (lane == 0) {
+          fence_acq_rel_cluster();
+          for (int src = 0; src < cs; ++src) mbar_arrive_cluster_relaxed(cluster_map(bar(kBarXFree), (uint32_t)src));
+        }
+      }
+      const bool valid = t < nr && (a.occ_inv == nullptr || a.occ_inv[t0 + t] >= 0);
       if (kFfn) {
         uint16_t v16[16];
 #pragma unroll
@@ -436,27 +487,31 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
           if (valid && j < B) hv = kGated ? fmaxf(av[j], 0.f) * bv[j] : fmaxf(av[j], 0.f);
           split16<BF16>(hv, v16[j], v16[8 + j]);
         }
-        // rows t and t^1 share 32-bit words: the even lane writes the hi
-        // columns of the pair, the odd lane the lo columns
-        const bool odd = lane & 1;
-        uint32_t wv[8];
+        // write this row's 16 operand values into the local buffer, then copy
+        // the warp's 64 16-byte chunks (16 operand rows x 4 groups of 8 tile
+        // rows) to the same place in every other CTA of the cluster
+        uint16_t* hw16 = reinterpret_cast<uint16_t*>(sm + 10240);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t mine_hi = v16[j], mine_lo = v16[8 + j];
-          const uint32_t give = odd ? mine_hi : mine_lo;
-          const uint32_t got = __shfl_xor_sync(0xffffffffu, give, 1);
-          wv[j] = odd ? (got | (mine_lo << 16)) : (mine_hi | (got << 16));
-        }
-        const int k0 = t & ~1;
-        for (int dst = 0; dst < cs; ++dst) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int nn = odd ? 8 + j : j;
-            st_cluster_u32(cluster_map(hbuf_a + kmajor_off(nn, k0, 16), (uint32_t)dst), wv[j]);
+        for (int nn = 0; nn < 16; ++nn) hw16[kmajor_off(nn, t, 16) >> 1] = v16[nn];
+        __syncwarp();
+        for (int c = lane; c < 64; c += 32) {
+          const int nn = c >> 2, kr = 32 * Q + 8 * (c & 3);
+          const uint32_t off = kmajor_off(nn, kr, 16);
+          const uint4 val = *reinterpret_cast<const uint4*>(sm + 10240 + off);
+          for (int dst = 0; dst < cs; ++dst) {
+            if (dst == (int)rank) continue;
+            const uint32_t ra = cluster_map(hbuf_a + off, (uint32_t)dst);
+            asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "r"(val.x), "r"(val.y),
+                         "r"(val.z), "r"(val.w)
+                         : "memory");
           }
         }
         fence_proxy_async_cluster();
-        for (int dst = 0; dst < cs; ++dst) mbar_arrive_cluster(cluster_map(bar(kBarHFull), (uint32_t)dst));
+        __syncwarp();
+        if (lane == 0) {
+          fence_acq_rel_cluster();
+          for (int dst = 0; dst < cs; ++dst) mbar_arrive_cluster_relaxed(cluster_map(bar(kBarHFull), (uint32_t)dst));
+        }
       } else if (MODE == kMmaHidden) {
         if (valid) {
           const int row = t0 + t;
@@ -486,15 +541,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
         }
       }
     }
-    if (kFfn && ok && n_tiles > 0) {
-      ok = wait_phase(bar(kBarYFull), 0, abort, a.err);
+    if (kFfn && n_tiles > 0) {
+      if (ok) ok = wait_phase(bar(kBarYFull), 0, abort, a.err);
+      ok = epi_and(ok);  // the stores below synchronise all 128 threads
       if (ok) {
         tc_fence_after();
         for (int mt = 0; mt < n_mt; ++mt) {
           float v[16];
           tmem_ld16(tbase + ((uint32_t)(32 * Q) << 16) + 32u + 16u * (uint32_t)mt, v);
-          const int d = slice0 + mt * 128 + t;
-          for (int j = 0; j < B; ++j) atomicAdd(a.y_acc + (size_t)j * Kd + d, v[j] + v[8 + j]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ystage[j * 128 + t] = v[j] + v[8 + j];
+          epi_sync();
+          // four consecutive columns of one sequence per vector atomic
+          for (int idx = e; idx < B * 32; idx += 128) {
+            const int j = idx >> 5, q = idx & 31;
+            const float4 y4 = *reinterpret_cast<const float4*>(ystage + j * 128 + 4 * q);
+            atomicAdd(reinterpret_cast<float4*>(a.y_acc + (size_t)j * Kd + slice0 + mt * 128 + 4 * q), y4);
+          }
+          epi_sync();
         }
       }
     }
@@ -509,7 +573,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
 }
 
 template <int MODE, bool BF16>
-cudaError_t launch_mode(const CUtensorMap& map, const MmaArgs& a, size_t smem, cudaStream_t st) {
+cudaError_t launch_mode(const RowMaps& maps, const MmaArgs& a, size_t smem, cudaStream_t st) {
   auto kern = mma_rows_kernel<MODE, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -525,7 +589,7 @@ cudaError_t launch_mode(const CUtensorMap& map, const MmaArgs& a, size_t smem, c
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, map, a);
+  return cudaLaunchKernelEx(&cfg, kern, maps.m32, maps.m8, a);
 }
 
 template <int MODE, bool BF16>
@@ -577,22 +641,27 @@ cudaError_t launch_add(float* out, const float* x, const float* y, int n, cudaSt
   return cudaGetLastError();
 }
 
-cudaError_t make_row_map(CUtensorMap* out, const void* base, int dtype, uint64_t rows, uint64_t cols) {
+cudaError_t make_row_maps(RowMaps* out, const void* base, int dtype, uint64_t rows, uint64_t cols) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   if (dtype != 1 && dtype != 2) return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(base) & 15u) || cols % 64 || rows == 0 || rows >= (1ull << 31))
     return cudaErrorInvalidValue;
-  std::memset(out, 0, sizeof(*out));
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, 1};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r =
-      fn(out, dtype == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  const cuuint32_t heights[2] = {32, 8};
+  CUtensorMap* maps[2] = {&out->m32, &out->m8};
+  for (int i = 0; i < 2; ++i) {
+    std::memset(maps[i], 0, sizeof(CUtensorMap));
+    const cuuint32_t box[2] = {64, heights[i]};
+    const CUresult r =
+        fn(maps[i], dtype == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
 }
 
 size_t mma_smem_bytes(int mode, int ks_len, int n_stages) {
@@ -644,7 +713,7 @@ cudaError_t mma_plan(int mode, int bf16, int Kdim, size_t smem_optin, int n_sms,
   return cudaSuccess;
 }
 
-cudaError_t launch_mma_rows(int mode, int bf16, const CUtensorMap& map, const MmaArgs& a_in, const MmaPlan& p,
+cudaError_t launch_mma_rows(int mode, int bf16, const RowMaps& map, const MmaArgs& a_in, const MmaPlan& p,
                             cudaStream_t st) {
   MmaArgs a = a_in;
   a.cs = p.cs;

@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   __shared__ int wsum[32];
   __shared__ uint32_t occ[kMaxKmax / 32];
   __shared__ int hist[33];
-  __shared__ int cut_age, cut_need;
+  __shared__ int cut_age, cut_need, s_hw;
   __shared__ uint32_t s_a[kMaxWords], s_out[kMaxWords], s_keep[kMaxWords];
   __shared__ int s_ea[kMaxWords], s_eout[kMaxWords];
   extern __shared__ int free_list[];  // [K]
@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   }
   const int KW = (K + 31) / 32;
   if (tid < KW) occ[tid] = 0u;
+  if (tid == 0) s_hw = 0;
   __syncthreads();
 
   // 5. one pass over the slots: occupied = holds a neuron that stays;
@@ -249,8 +250,17 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     int p = efree;
     for (uint32_t w = fw; w; w &= w - 1) free_list[p++] = tid * 32 + __ffs(w) - 1;
   }
+  if (tid < KW && occ[tid]) atomicMax(&s_hw, tid * 32 + 32 - __clz(occ[tid]));
   __syncthreads();
   if (n_in > n_free && tid == 0) atomicExch(a.err, kDevErrBounds);
+  // one past the highest occupied slot after this delta (kept slots, and the
+  // free slots handed out in ascending order)
+  if (tid == 0 && a.slot_hw) {
+    const int na = n_in < n_free ? n_in : n_free;
+    int hw = s_hw;
+    if (na > 0 && free_list[na - 1] + 1 > hw) hw = free_list[na - 1] + 1;
+    a.slot_hw[s] = hw;
+  }
 
   // 6. outgoing neurons leave (before incoming ones may take their slots)
   for (int r = tid; r < n_out; r += kSetThreads) {
@@ -309,6 +319,7 @@ __global__ void __launch_bounds__(kSetThreads) rollback_kernel(SetLaunch a) {
   const int* dinct = a.din_oldct + (size_t)s * K;
   const int* dout = a.dout_n + (size_t)s * K;
   const int* douts = a.dout_s + (size_t)s * K;
+  if (threadIdx.x == 0 && a.slot_hw) a.slot_hw[s] = K;  // an upper bound is always safe
   for (int r = threadIdx.x; r < n_in; r += kSetThreads) {
     const int n = din[r], k = dins[r];
     if ((unsigned)n >= (unsigned)F || (unsigned)k >= (unsigned)K) continue;

@@ -16,16 +16,14 @@
 namespace np {
 
 // ---- tensor-map loads -------------------------------------------------------
-// Four rows (r0..r3) of a 2-D tensor map with a box of {64 columns, 1 row},
-// starting at column x, into dst (512 bytes, rows 128 bytes apart, swizzled).
-// Rows at or past the tensor's end read as zeros.  Completion is counted on
-// `bar` (512 bytes).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2,
-                                            int r3, uint32_t bar, uint64_t policy) {
+// One box of a 2-D tensor map at (column x, row y) into dst; rows past the
+// tensor's end read as zeros.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                            uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -63,6 +61,15 @@ __device__ __forceinline__ void cluster_sync_all() {
 // Arrive (release, cluster scope) on an mbarrier of any CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Cluster-scope fence: this thread's earlier writes (and those it has
+// observed) are ordered before its later relaxed arrives.
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// Arrive without ordering (pair with fence_acq_rel_cluster before it).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, float c, float d) {
