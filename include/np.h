@@ -215,6 +215,15 @@ np_status np_sparse_mlp(np_model* m, int32_t layer, const float* h_dev, float* y
 /* Full FFN of dense layer `layer` < n_dense, same formula over all F neurons. */
 np_status np_dense_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_dev);
 
+/* FFNs of layers first .. first+count-1 (dense or sparse) for every
+ * sequence on the committed resident rows, one after another, with the
+ * residual stream h_dev [batch][D] float32 updated in place: for each layer
+ * h += FFN(rmsnorm(h)) — the FFN part of np_decode_token, without the
+ * prediction and transfer steps (for callers that run np_predict, np_delta
+ * and np_scatter themselves).  Errors: NP_ERR_ARG for a bad range,
+ * NP_ERR_STATE if a delta is pending for a layer in the range. */
+np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev);
+
 /* One decode step for all sequences: dense prefix, predictor, delta,
  * host-link gather and scatter on the side stream overlapped with the FFNs on
  * the main stream (each sparse layer waits only for its own rows), sparse
@@ -281,11 +290,12 @@ np_status np_host_unregister(void* ptr);
  * for rows 0..n_rows-1.  All pointers are device pointers, 16-byte aligned;
  * dtype NP_F32/NP_F16/NP_BF16; d_model in [8, 8192], rows a multiple of 16
  * bytes.  Enqueued on `stream` (cudaStream_t); the call allocates nothing:
- * its scratch (at most 1 MiB of partial sums plus 64 counters) is a
- * file-scope device array whose address the first call on each device looks
- * up, so make that first call before any stream capture.  All calls share
- * the array: calls that overlap on the GPU race.  Errors: NP_ERR_ARG for
- * sizes or pointers out of range, NP_ERR_CUDA if a launch fails. */
+ * y_dev is cleared on the stream and then accumulated into, and the
+ * kernel's error word lives in a file-scope device array (256 bytes) whose
+ * address the first call on each device looks up, so make that first call
+ * before any stream capture.  All calls share the array: calls that overlap
+ * on the GPU race.  Errors: NP_ERR_ARG for sizes or pointers out of range,
+ * NP_ERR_CUDA if a launch fails. */
 np_status np_ffn_rows_noalloc(const float* h_dev, const void* w_gate, const void* w_up, const void* w_down,
                               const int32_t* rows_dev, int32_t n_rows, int32_t row_limit, int32_t d_model,
                               int32_t dtype, int32_t has_gate, float* y_dev, void* stream);

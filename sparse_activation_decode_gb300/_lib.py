@@ -60,6 +60,7 @@ SIGNATURES = {
     "np_scatter": (_I32, [_P, _I32]),
     "np_sparse_mlp": (_I32, [_P, _I32, _P, _P]),
     "np_dense_mlp": (_I32, [_P, _I32, _P, _P]),
+    "np_ffn_layers": (_I32, [_P, _I32, _I32, _P]),
     "np_decode_token": (_I32, [_P, _P, ctypes.POINTER(Stats)]),
     "np_get_state": (_I32, [_P, _I32, _P, _P]),
     "np_resident_rows": (_I32, [_P, _I32, _I32, ctypes.POINTER(_P)]),

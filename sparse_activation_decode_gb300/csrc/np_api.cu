@@ -87,8 +87,6 @@ struct np_model {
   int* ids = nullptr;
   uint32_t* fire = nullptr;
   float* logits = nullptr;
-  float* part = nullptr;
-  int* slice_cnt = nullptr;
   // batched (B > 1) tensor-core path: tensor maps over the weight blocks,
   // launch plans, residual bases [2][B][D], y accumulators [3][B][D], the
   // predictor hidden layer as hi/lo 16-bit operands [16][H]
@@ -96,12 +94,13 @@ struct np_model {
   RowMaps map_bufs{}, map_dense{}, map_w1{}, map_w2{};
   int* slot_hw = nullptr;  // [S] one past the highest occupied slot
   MmaPlan plan_ffn{}, plan_hid{}, plan_heads{};
+  uint16_t* zhl = nullptr;
+  // residual chaining (every batch size): bases [2][B][D], accumulators [3][B][D]
   float* hbase = nullptr;
   float* yacc = nullptr;
-  uint16_t* zhl = nullptr;
   std::vector<void*> allocs;
   // launch shapes
-  int ffn_grid = 0, ffn_cluster = 1, ffn_stages = 0, ffn_stages_dense = 0;
+  int ffn_grid = 0, ffn_stages = 0;
   int gather_grid = 0, scatter_grid = 0, pred_grid = 0;
   int rps1 = 1, rps2 = 1, ns1 = 2, ns2 = 2;
   // state
@@ -206,12 +205,18 @@ const unsigned char* layer_bufs(const np_model* m, int s) {
   return static_cast<const unsigned char*>(m->bufs) + (size_t)s * m->nproj * m->K * m->row_bytes;
 }
 
-// FFN over a row list followed by the partial-sum finish.
+// FFN over a row list: x = rmsnorm(hb + yprev), y added into y_acc; CTA 0
+// stores hb + yprev into hb_out and clears y_zero (both optional).
 np_status enqueue_ffn(np_model* m, cudaStream_t st, int kind, const unsigned char* base, size_t proj_stride,
-                      const int* rows, const int* n_dev, int n_host, int list_cap, int row_limit, int stages,
-                      const float* h_in, float* h_out, float* y_out, int64_t fixed_bytes) {
+                      const int* rows, const int* n_dev, int n_host, int list_cap, int row_limit,
+                      const float* hb, const float* yprev, float* hb_out, float* y_acc, float* y_zero,
+                      int64_t fixed_bytes) {
   FfnLaunch a{};
-  a.h_in = h_in;
+  a.h_in = hb;
+  a.yprev = yprev;
+  a.hb_out = hb_out;
+  a.y_acc = y_acc;
+  a.y_zero = y_zero;
   int p = 0;
   a.w_gate = m->d.has_gate ? base + (p++) * proj_stride : nullptr;
   a.w_up = base + (p++) * proj_stride;
@@ -221,47 +226,44 @@ np_status enqueue_ffn(np_model* m, cudaStream_t st, int kind, const unsigned cha
   a.n_rows_host = n_host;
   a.list_cap = list_cap;
   a.row_limit = row_limit;
-  a.part = m->part;
-  a.slice_cnt = m->slice_cnt;
-  a.cluster = m->ffn_cluster;
-  a.h_out = h_out;
-  a.y_out = y_out;
   a.D = m->D;
   a.dtype = m->d.dtype;
   a.dtype_bytes = m->esz;
   a.gated = m->d.has_gate;
-  a.n_stages = stages;
+  a.n_stages = m->ffn_stages;
   a.grid = m->ffn_grid;
   a.err = m->err;
   return launch(m, kind, st, fixed_bytes, [&] { return launch_ffn_rows(a, st); });
 }
 
-np_status enqueue_dense_on(np_model* m, cudaStream_t st, int layer, const float* h_in, float* h_out,
-                           float* y_out) {
-  const size_t proj_stride = (size_t)m->F * m->row_bytes;
-  const unsigned char* base =
-      static_cast<const unsigned char*>(m->d.dense_w) + (size_t)layer * m->nproj * proj_stride;
-  return enqueue_ffn(m, st, NP_KIND_DENSE, base, proj_stride, nullptr, nullptr, m->F, m->F, m->F,
-                     m->ffn_stages_dense, h_in, h_out, y_out, (int64_t)m->nproj * m->F * m->row_bytes);
-}
+np_status enqueue_tc_ffn(np_model* m, cudaStream_t st, int l, const float* hb, const float* yprev, float* hb_out,
+                         float* y_acc, float* y_zero);
 
-np_status enqueue_dense(np_model* m, int layer, const float* h_in, float* h_out, float* y_out) {
-  return enqueue_dense_on(m, m->main, layer, h_in, h_out, y_out);
-}
-
-np_status enqueue_sparse_on(np_model* m, cudaStream_t st, int s, const float* h_in, float* h_out, float* y_out) {
+// FFN of layer l (dense or sparse) for every sequence, on the kernel that
+// fits the batch: x = rmsnorm(hb + yprev), y added into y_acc.
+np_status enqueue_layer_ffn(np_model* m, cudaStream_t st, int l, const float* hb, const float* yprev,
+                            float* hb_out, float* y_acc, float* y_zero) {
+  if (m->tc) return enqueue_tc_ffn(m, st, l, hb, yprev, hb_out, y_acc, y_zero);
+  if (l < m->dn) {
+    const size_t proj_stride = (size_t)m->F * m->row_bytes;
+    const unsigned char* base =
+        static_cast<const unsigned char*>(m->d.dense_w) + (size_t)l * m->nproj * proj_stride;
+    return enqueue_ffn(m, st, NP_KIND_DENSE, base, proj_stride, nullptr, nullptr, m->F, m->F, m->F, hb, yprev,
+                       hb_out, y_acc, y_zero, (int64_t)m->nproj * m->F * m->row_bytes);
+  }
+  const int s = l - m->dn;
   const size_t proj_stride = (size_t)m->K * m->row_bytes;
   return enqueue_ffn(m, st, NP_KIND_FFN, layer_bufs(m, s), proj_stride, m->active_slot + (size_t)s * m->K,
-                     m->counts + (size_t)s * 4, 0, m->K, m->K, m->ffn_stages, h_in, h_out, y_out, 0);
+                     m->counts + (size_t)s * 4, 0, m->K, m->K, hb, yprev, hb_out, y_acc, y_zero, 0);
 }
 
-np_status enqueue_sparse(np_model* m, int s, const float* h_in, float* h_out, float* y_out) {
-  return enqueue_sparse_on(m, m->main, s, h_in, h_out, y_out);
-}
+// Residual chaining across layers: layer l reads base(l) + y(l-1), adds its
+// y into y(l) and stores its input h_l as base(l+1); y(l+1) is cleared by
+// layer l.  Two bases and three accumulators rotate.
+float* chain_base(np_model* m, int i) { return m->hbase + (size_t)(i & 1) * m->B * m->D; }
+float* chain_y(np_model* m, int i) { return m->yacc + (size_t)(i % 3) * m->B * m->D; }
 
 // ---- batched path (tensor cores) -------------------------------------------
-float* tc_hbase(np_model* m, int i) { return m->hbase + (size_t)(i & 1) * m->B * m->D; }
-float* tc_y(np_model* m, int i) { return m->yacc + (size_t)(i % 3) * m->B * m->D; }
 
 np_status enqueue_mma(np_model* m, cudaStream_t st, int kind, int mode, const RowMaps& map, const MmaPlan& p,
                       MmaArgs& a, int64_t fixed_bytes) {
@@ -340,9 +342,10 @@ np_status enqueue_tc_heads(np_model* m, int h0, int h1) {
 
 np_status enqueue_rowdot(np_model* m, const void* W, int n_rows, int len, const float* vec, int rms, int mode,
                          const void* bias, float* out_f, unsigned long long* keys, int C, uint32_t* fire,
-                         uint32_t* zero_ptr, int zero_words, int rps, int ns) {
+                         uint32_t* zero_ptr, int zero_words, int rps, int ns, const float* vec2 = nullptr) {
   RowdotLaunch a{};
   a.W = W;
+  a.vec2 = vec2;
   a.n_rows = n_rows;
   a.len = len;
   a.vec = vec;
@@ -374,12 +377,14 @@ np_status enqueue_pred_heads(np_model* m, int h0, int h1) {
                         nullptr, 0, m->rps2, m->ns2);
 }
 
-np_status enqueue_pred_hidden(np_model* m, const float* h) {
+// Hidden layer of the shared predictor on x = rmsnorm(h + h2) (h2 may be null).
+np_status enqueue_pred_hidden(np_model* m, const float* h, const float* h2) {
+  if (m->tc) return enqueue_tc_hidden(m, h, h2);
   return enqueue_rowdot(m, m->d.pred_w1, m->H, m->D, h, 1, 0, nullptr, m->z, nullptr, 0, nullptr,
-                        reinterpret_cast<uint32_t*>(m->keys), 2 * m->NH, m->rps1, m->ns1);
+                        reinterpret_cast<uint32_t*>(m->keys), 2 * m->NH, m->rps1, m->ns1, h2);
 }
 
-np_status enqueue_predict(np_model* m, int layer, const float* h, bool want_ids = true) {
+np_status enqueue_predict(np_model* m, int layer, const float* h, bool want_ids = true, const float* h2 = nullptr) {
   if (m->tc) {
     NP_TRY(enqueue_tc_hidden(m, h, nullptr));
     NP_TRY(enqueue_tc_heads(m, 0, m->NH));
@@ -401,7 +406,7 @@ np_status enqueue_predict(np_model* m, int layer, const float* h, bool want_ids 
       static_cast<const unsigned char*>(m->d.pred_w2) + (size_t)layer * m->F * m->H * m->esz;
   const unsigned char* b2 = static_cast<const unsigned char*>(m->d.pred_b2) + (size_t)layer * m->F * m->esz;
   NP_TRY(enqueue_rowdot(m, w1, m->H, m->D, h, 1, 0, nullptr, m->z, nullptr, 0, nullptr, m->fire, m->W, m->rps1,
-                        m->ns1));
+                        m->ns1, h2));
   return enqueue_rowdot(m, w2, m->F, m->H, m->z, 0, 2, b2, m->logits, nullptr, 0, m->fire, nullptr, 0, m->rps2,
                         m->ns2);
 }
@@ -740,16 +745,22 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   // launch shapes: two streaming CTAs per SM
   const size_t per_cta = m->smem_optin > 2048 ? (m->smem_optin / 2) - 1024 : m->smem_optin;
   {
-    e = ffn_plan(m->d.dtype, m->d.has_gate, m->D, m->esz, m->smem_optin - 1024, m->sms, &m->ffn_stages,
-                 &m->ffn_cluster, &m->ffn_grid);
+    int smem_sm = 0;
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    e = ffn_plan(m->d.dtype, m->d.has_gate, m->D, m->esz, (size_t)smem_sm, m->sms, &m->ffn_stages, &m->ffn_grid);
     if (e != cudaSuccess) return fail(cuda_fail(e, "ffn_plan"));
-    m->ffn_stages_dense = m->ffn_stages;
-    // NP_TUNE_FFN_CTAS caps the FFN grid (rounded down to whole clusters)
-    const int cap = env_int("NP_TUNE_FFN_CTAS", 0);
-    if (cap > 0 && cap < m->ffn_grid) m->ffn_grid = (cap / m->ffn_cluster > 0 ? cap / m->ffn_cluster : 1) * m->ffn_cluster;
-    if (env_int("NP_TUNE_VERBOSE", 0) == 1)
-      std::fprintf(stderr, "np: ffn grid %d cluster %d ring %d slots; gather %d scatter %d CTAs\n", m->ffn_grid,
-                   m->ffn_cluster, m->ffn_stages, m->gather_grid, m->scatter_grid);
+    // NP_TUNE_FFN_SLOTS sets the ring depth (one CTA per SM fits up to the
+    // per-block limit), NP_TUNE_FFN_CTAS the grid
+    const int slots = env_int("NP_TUNE_FFN_SLOTS", 0);
+    if (slots > 0) {
+      if (slots > 16 || ffn_smem_bytes(m->D, m->esz, m->nproj, slots) > m->smem_optin - 1024)
+        return fail(arg_fail("NP_TUNE_FFN_SLOTS does not fit in shared memory"));
+      m->ffn_stages = slots;
+      if ((e = ffn_set_smem(m->d.dtype, m->d.has_gate, m->D, m->esz, slots)) != cudaSuccess)
+        return fail(cuda_fail(e, "ffn_set_smem"));
+    }
+    const int ctas = env_int("NP_TUNE_FFN_CTAS", 0);
+    if (ctas > 0) m->ffn_grid = ctas;
   }
   // Host-link gathers need only a few MB in flight to fill the link; keeping
   // their grids small leaves the SMs to the FFN running beside them.
@@ -757,6 +768,9 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   m->gather_grid = env_int("NP_TUNE_GATHER_CTAS", 32);
   m->scatter_grid = env_int("NP_TUNE_SCATTER_CTAS", 4 * m->sms);
   m->pred_grid = 2 * m->sms;
+  if (env_int("NP_TUNE_VERBOSE", 0) == 1)
+    std::fprintf(stderr, "np: ffn grid %d, ring %d slots; gather %d scatter %d CTAs\n", m->ffn_grid, m->ffn_stages,
+                 m->gather_grid, m->scatter_grid);
   m->rps1 = pick_rps(m->row_bytes);
   m->rps2 = pick_rps((size_t)m->H * m->esz);
   m->ns1 = pick_stages(m->rps1 * m->row_bytes, rowdot_smem_bytes(m->D, m->esz, m->rps1, 0), per_cta);
@@ -793,9 +807,8 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if ((st = dev_alloc(m, &m->ids, (size_t)m->B * (m->NH > 0 ? m->NH : 1))) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->fire, (size_t)m->W)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->logits, F)) != NP_OK) return fail(st);
-  if ((st = dev_alloc(m, &m->part, (size_t)(m->ffn_grid / m->ffn_cluster) * m->B * m->D)) != NP_OK) return fail(st);
-  if ((st = dev_alloc(m, reinterpret_cast<unsigned char**>(&m->slice_cnt), ffn_counter_bytes())) != NP_OK)
-    return fail(st);
+  if ((st = dev_alloc(m, &m->hbase, 2 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->yacc, 3 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
 
   if (m->B > 1) {
     // tensor-core path: maps over every weight block the gathers read
@@ -817,8 +830,6 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
         (e = make_row_maps(&m->map_w2, m->d.pred_w2, dt, (uint64_t)m->NH * m->C, m->H)) != cudaSuccess)
       return fail(cuda_fail(e, "tensor map of the predictor"));
     if ((st = dev_alloc(m, &m->slot_hw, Sa)) != NP_OK) return fail(st);
-    if ((st = dev_alloc(m, &m->hbase, 2 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
-    if ((st = dev_alloc(m, &m->yacc, 3 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
     if ((st = dev_alloc(m, &m->zhl, 16 * (size_t)m->H)) != NP_OK) return fail(st);
     if (env_int("NP_TUNE_VERBOSE", 0) == 1)
       std::fprintf(stderr, "np: tensor-core ffn %d clusters x %d, %d stages; hidden %d x %d; heads %d x %d\n",
@@ -1002,11 +1013,8 @@ np_status np_sparse_mlp(np_model* m, int32_t layer, const float* h_dev, float* y
   if (!aligned16(h_dev) || !aligned16(y_dev)) return arg_fail("h_dev and y_dev must be 16-byte aligned");
   if (layer < m->dn || layer >= m->L) return arg_fail("layer is not a sparse layer");
   if (h_dev == y_dev) return arg_fail("y_dev may not alias h_dev");
-  if (m->tc) {
-    CUDA_TRY(cudaMemsetAsync(y_dev, 0, sizeof(float) * m->B * m->D, m->main));
-    return enqueue_tc_ffn(m, m->main, layer, h_dev, nullptr, nullptr, y_dev, nullptr);
-  }
-  return enqueue_sparse(m, layer - m->dn, h_dev, nullptr, y_dev);
+  CUDA_TRY(cudaMemsetAsync(y_dev, 0, sizeof(float) * m->B * m->D, m->main));
+  return enqueue_layer_ffn(m, m->main, layer, h_dev, nullptr, nullptr, y_dev, nullptr);
 }
 
 np_status np_dense_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_dev) {
@@ -1014,11 +1022,30 @@ np_status np_dense_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_
   if (!aligned16(h_dev) || !aligned16(y_dev)) return arg_fail("h_dev and y_dev must be 16-byte aligned");
   if (layer < 0 || layer >= m->dn) return arg_fail("layer is not a dense layer");
   if (h_dev == y_dev) return arg_fail("y_dev may not alias h_dev");
-  if (m->tc) {
-    CUDA_TRY(cudaMemsetAsync(y_dev, 0, sizeof(float) * m->B * m->D, m->main));
-    return enqueue_tc_ffn(m, m->main, layer, h_dev, nullptr, nullptr, y_dev, nullptr);
+  CUDA_TRY(cudaMemsetAsync(y_dev, 0, sizeof(float) * m->B * m->D, m->main));
+  return enqueue_layer_ffn(m, m->main, layer, h_dev, nullptr, nullptr, y_dev, nullptr);
+}
+
+np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev) {
+  if (!m || !h_dev) return arg_fail("null argument");
+  if (!aligned16(h_dev)) return arg_fail("h_dev must be 16-byte aligned");
+  if (first < 0 || count < 1 || first + count > m->L) return arg_fail("layer range out of bounds");
+  for (int l = first; l < first + count; ++l)
+    if (l >= m->dn && (m->pending_bits & (1ull << (l - m->dn)))) {
+      g_last_err = "a delta is pending for a layer in the range";
+      return NP_ERR_STATE;
+    }
+  // the same chaining as np_decode_token, relative to `first`
+  cudaStream_t st = m->main;
+  CUDA_TRY(cudaMemsetAsync(chain_y(m, 0), 0, sizeof(float) * m->B * m->D, st));
+  for (int i = 0; i < count; ++i) {
+    const float* hb = i <= 1 ? h_dev : chain_base(m, i - 1);
+    NP_TRY(enqueue_layer_ffn(m, st, first + i, hb, i == 0 ? nullptr : chain_y(m, i - 1),
+                             i >= 1 ? chain_base(m, i) : nullptr, chain_y(m, i), chain_y(m, i + 1)));
   }
-  return enqueue_dense(m, layer, h_dev, nullptr, y_dev);
+  const float* hb = count == 1 ? h_dev : chain_base(m, count - 1);
+  return launch(m, NP_KIND_FINISH, st, 0,
+                [&] { return launch_add(h_dev, hb, chain_y(m, count - 1), m->B * m->D, st); });
 }
 
 np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
@@ -1030,33 +1057,27 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
   }
   const int64_t token = m->token;
   const bool shared = m->d.pred_kind == NP_PRED_SHARED_ARGMAX;
+  // Residual chaining: layer l reads base(l) + y(l-1) and adds its y into
+  // y(l); the residual stream after the last layer is written back by a
+  // final add.  y(0) starts cleared; layer l clears y(l+1).
+  auto base_of = [&](int l) -> const float* { return l <= 1 ? h_dev : chain_base(m, l - 1); };
+  auto ffn_layer = [&](cudaStream_t st, int l) -> np_status {
+    return enqueue_layer_ffn(m, st, l, base_of(l), l == 0 ? nullptr : chain_y(m, l - 1),
+                             l >= 1 ? chain_base(m, l) : nullptr, chain_y(m, l), chain_y(m, l + 1));
+  };
+  CUDA_TRY(cudaMemsetAsync(chain_y(m, 0), 0, sizeof(float) * m->B * m->D, m->main));
+  cudaStream_t fin = m->main;
   if (shared && m->S > 0) {
     // main: dense layer 0, the predictor's hidden layer, then per layer
     // group the group's predictor heads, its set kernel and its reads on the
     // gather streams, so that transfers start after the first small group.
     // The FFN stream runs dense layers 1..d-1 (once the predictor has read
     // h) and then the sparse FFNs, each after its own rows have arrived.
-    // Batched: layer l reads base(l) + y(l-1) and adds its y into y(l) (three
-    // rotating accumulators, two rotating bases); the last add is a finish.
-    auto tc_layer = [&](cudaStream_t st, int l) -> np_status {
-      const float* hb = l <= 1 ? h_dev : tc_hbase(m, l - 1);
-      const float* yp = l == 0 ? nullptr : tc_y(m, l - 1);
-      return enqueue_tc_ffn(m, st, l, hb, yp, l >= 1 ? tc_hbase(m, l) : nullptr, tc_y(m, l), tc_y(m, l + 1));
-    };
-    if (m->tc) {
-      CUDA_TRY(cudaMemsetAsync(tc_y(m, 0), 0, sizeof(float) * m->B * m->D, m->main));
-      NP_TRY(tc_layer(m->main, 0));
-      NP_TRY(enqueue_tc_hidden(m, h_dev, tc_y(m, 0)));
-    } else {
-      NP_TRY(enqueue_dense(m, 0, h_dev, h_dev, nullptr));
-      NP_TRY(enqueue_pred_hidden(m, h_dev));
-    }
+    NP_TRY(ffn_layer(m->main, 0));
+    NP_TRY(enqueue_pred_hidden(m, h_dev, chain_y(m, 0)));
     CUDA_TRY(cudaEventRecord(m->ev_pre, m->main));
     CUDA_TRY(cudaStreamWaitEvent(m->fs, m->ev_pre, 0));
-    for (int l = 1; l < m->dn; ++l) {
-      if (m->tc) NP_TRY(tc_layer(m->fs, l));
-      else NP_TRY(enqueue_dense_on(m, m->fs, l, h_dev, h_dev, nullptr));
-    }
+    for (int l = 1; l < m->dn; ++l) NP_TRY(ffn_layer(m->fs, l));
     m->pending_bits = all_layers(m);
     std::vector<int> moved;
     int s0 = 0;
@@ -1087,23 +1108,15 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
     }
     for (int s = 0; s < m->S; ++s) {
       CUDA_TRY(cudaStreamWaitEvent(m->fs, m->ev_layer[s], 0));
-      if (m->tc) NP_TRY(tc_layer(m->fs, m->dn + s));
-      else NP_TRY(enqueue_sparse_on(m, m->fs, s, h_dev, h_dev, nullptr));
+      NP_TRY(ffn_layer(m->fs, m->dn + s));
     }
-    if (m->tc) {
-      const int l = m->L - 1;
-      const float* hb = l == 0 ? h_dev : tc_hbase(m, l);  // layer l stored its input h_l there
-      cudaStream_t st = m->fs;
-      NP_TRY(launch(m, NP_KIND_FINISH, st, 0,
-                    [&] { return launch_add(h_dev, hb, tc_y(m, l), m->B * m->D, st); }));
-    }
-    CUDA_TRY(cudaEventRecord(m->ev_ffn, m->fs));
-    CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_ffn, 0));
+    fin = m->fs;
   } else {
-    for (int l = 0; l < m->dn; ++l) NP_TRY(enqueue_dense(m, l, h_dev, h_dev, nullptr));
+    for (int l = 0; l < m->dn; ++l) NP_TRY(ffn_layer(m->main, l));
     for (int s = 0; s < m->S; ++s) {
+      const int l = m->dn + s;
       if (!shared) {
-        NP_TRY(enqueue_predict(m, m->dn + s, h_dev));
+        NP_TRY(enqueue_predict(m, l, base_of(l), true, l == 0 ? nullptr : chain_y(m, l - 1)));
         NP_TRY(enqueue_set(m, s, 1, nullptr, m->fire));
         m->pending_bits |= 1ull << s;
         size_t n_moved = 0;
@@ -1118,8 +1131,18 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
         }
       }
       CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_layer[s], 0));
-      NP_TRY(enqueue_sparse(m, s, h_dev, h_dev, nullptr));
+      NP_TRY(ffn_layer(m->main, l));
     }
+  }
+  if (m->L > 0) {
+    const int l = m->L - 1;
+    const float* hb = l == 0 ? h_dev : chain_base(m, l);  // layer l stored its input h_l there
+    NP_TRY(launch(m, NP_KIND_FINISH, fin, 0,
+                  [&] { return launch_add(h_dev, hb, chain_y(m, l), m->B * m->D, fin); }));
+  }
+  if (fin != m->main) {
+    CUDA_TRY(cudaEventRecord(m->ev_ffn, fin));
+    CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_ffn, 0));
   }
   if (m->S > 0) {
     m->committed_since_token = 0;

@@ -137,11 +137,13 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
-// x_hat = h / sqrt(mean(h^2) + 1e-6) into shared memory (fp32, D values).
-__device__ __forceinline__ void rmsnorm_to_smem(const float* __restrict__ h, float* xs, int D, float* red) {
+// x_hat = h / sqrt(mean(h^2) + 1e-6) into shared memory (fp32, D values),
+// with h = h1 + h2 (h2 may be null).
+__device__ __forceinline__ void rmsnorm_to_smem(const float* __restrict__ h, const float* __restrict__ h2, float* xs,
+                                                int D, float* red) {
   float ss = 0.f;
   for (int j = threadIdx.x; j < D; j += kThreads) {
-    const float v = h[j];
+    const float v = h2 ? h[j] + h2[j] : h[j];
     xs[j] = v;
     ss = fmaf(v, v, ss);
   }

@@ -4,37 +4,37 @@
 // neuron of a dense layer):
 //     h_r = relu(g_r . x) * (u_r . x)      (or relu(u_r . x) without a gate)
 //     y  += h_r * d_r
-// with x = rmsnorm(h_in), then h_out = h_in + y (NeuroPrefetcher full text,
-// delta runtime: row i of the gate, up and down^T projections serves active
-// neuron i; ReLU-fied form of the activation).
+// with x = rmsnorm(h), h = h_base + y_prev (NeuroPrefetcher full text, delta
+// runtime: row i of the gate, up and down^T projections serves active neuron
+// i; ReLU-fied form of the activation).  Consecutive layers chain through the
+// residual stream as base + previous y: the CTA that reads first stores h for
+// the next layer and clears the accumulator after next, so no separate
+// residual-add kernel runs between layers.
 //
 // Design (HBM-bound: 2 flops per weight element):
-//  * one CTA per SM, grouped in thread-block clusters; warp-specialized:
-//    warp 8 is the producer, warps 0-7 consume;
+//  * one CTA per SM per launch, sized so that two fit: consecutive launches
+//    in a stream overlap (see below); warp-specialized: warp 8 is the
+//    producer, warps 0-7 consume;
 //  * whole neuron records (gate|up|down^T rows) stream into a shared-memory
 //    ring through 1-D bulk copies (TMA engine); a "full" mbarrier per slot
 //    counts the bytes in, an "empty" mbarrier per slot counts the consumer
 //    warps done with it, so the producer refills a slot the moment it frees
 //    up and keeps the whole ring in flight;
+//  * programmatic dependent launch: the weights do not depend on the previous
+//    layer, so the producer starts streaming as soon as the CTA is resident,
+//    while the previous kernel in the stream may still be finishing; only the
+//    consumers wait for it (griddepcontrol.wait) before reading h;
 //  * thread t owns 16-byte column chunks t, t+256, ... of every row and keeps
 //    the matching x values and y accumulators in registers; products use
 //    packed FP32x2 FMAs.  Rows are consumed two at a time: the four dot
 //    products of a pair are reduce-scattered across each warp (6 shuffles),
 //    one block barrier combines the warps, and the down projection needs no
 //    reduction at all;
-//  * split-K over CTAs without any grid-wide wait: each CTA parks its
-//    partial y in shared memory, CTA r of a cluster sums column slice r over
-//    the cluster through distributed shared memory and writes one cluster
-//    partial; the last cluster to report slice r (an atomic counter per
-//    slice) sums the cluster partials in cluster order, writes h_out / y_out
-//    and resets the counter.  The summation order is fixed, so the result is
-//    bitwise reproducible.
-#include <cooperative_groups.h>
-
+//  * split-K over CTAs: each CTA adds its partial y to the layer's
+//    accumulator with vector atomics (fp32; the order of the CTAs' additions
+//    is not fixed).
 #include "np_common.cuh"
 #include "np_kernels.h"
-
-namespace cg = cooperative_groups;
 
 namespace np {
 
@@ -101,8 +101,13 @@ __device__ __forceinline__ bool consumer_sync_or(bool pred) {
   return r != 0;
 }
 
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <typename T, bool GATED, int MAXC>
-__global__ void __launch_bounds__(kFfnBlock, 1) ffn_rows_kernel(FfnLaunch a) {
+__global__ void __launch_bounds__(kFfnBlock, 2) ffn_rows_kernel(FfnLaunch a) {
   constexpr int P = Pairs<T>::N;      // float pairs per 16-byte chunk
   constexpr int E = 2 * P;            // elements per chunk
   constexpr int NPROJ = GATED ? 3 : 2;
@@ -120,6 +125,7 @@ __global__ void __launch_bounds__(kFfnBlock, 1) ffn_rows_kernel(FfnLaunch a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int NC = D / E;
 
+  grid_dependents_launch();  // the next layer may start prefetching its weights
   int n = a.n_rows_dev ? *a.n_rows_dev : a.n_rows_host;
   if (n > a.list_cap) n = a.list_cap;
   if (n < 0) n = 0;
@@ -174,7 +180,10 @@ __global__ void __launch_bounds__(kFfnBlock, 1) ffn_rows_kernel(FfnLaunch a) {
     }
   } else {
     // ------------------------------------------------------------ consumers
-    // x = rmsnorm(h_in): each thread reads its own chunks of h.
+    // x = rmsnorm(h_in + yprev): each thread reads its own chunks of h, once
+    // the previous kernel's writes are visible.  CTA 0 stores h for the next
+    // layer and clears the accumulator after next.
+    grid_dependency_wait();
     float2 xr[MAXC][P];
     float ss = 0.f;
 #pragma unroll
@@ -183,7 +192,18 @@ __global__ void __launch_bounds__(kFfnBlock, 1) ffn_rows_kernel(FfnLaunch a) {
 #pragma unroll
       for (int q = 0; q < P; ++q) {
         float2 v = make_float2(0.f, 0.f);
-        if (c < NC) v = *reinterpret_cast<const float2*>(a.h_in + c * E + 2 * q);
+        if (c < NC) {
+          v = *reinterpret_cast<const float2*>(a.h_in + c * E + 2 * q);
+          if (a.yprev) {
+            const float2 w = *reinterpret_cast<const float2*>(a.yprev + c * E + 2 * q);
+            v.x += w.x;
+            v.y += w.y;
+          }
+          if (blockIdx.x == 0) {
+            if (a.hb_out) *reinterpret_cast<float2*>(a.hb_out + c * E + 2 * q) = v;
+            if (a.y_zero) *reinterpret_cast<float2*>(a.y_zero + c * E + 2 * q) = make_float2(0.f, 0.f);
+          }
+        }
         xr[k][q] = v;
         ss = fmaf(v.x, v.x, fmaf(v.y, v.y, ss));
       }
@@ -323,69 +343,18 @@ __global__ void __launch_bounds__(kFfnBlock, 1) ffn_rows_kernel(FfnLaunch a) {
     for (int j = first; j < issued; ++j) mbar_wait(&full[j % n_slots], (uint32_t)(j / n_slots) & 1u, nullptr);
   }
 
-  // ---- split-K: cluster reduction in distributed shared memory, then the
-  // last cluster per column slice
-  cg::cluster_group cl = cg::this_cluster();
-  const int CS = (int)cl.num_blocks();
-  const int crank = (int)cl.block_rank();
-  const int cid = (int)blockIdx.x / CS;
-  const int ncl = (int)gridDim.x / CS;
-  float* mine = reinterpret_cast<float*>(ring);  // every copy has landed: reuse the ring
+  // ---- split-K: this CTA's partial y into the layer's accumulator
+  if (tid < kFfnThreads && !s_abort) {
 #pragma unroll
-  for (int k = 0; k < MAXC; ++k) {
-    const int c = tid + k * kFfnThreads;
-    if (tid < kFfnThreads && c < NC) {
+    for (int k = 0; k < MAXC; ++k) {
+      const int c = tid + k * kFfnThreads;
+      if (c < NC) {
 #pragma unroll
-      for (int q = 0; q < P; q += 2)
-        *reinterpret_cast<float4*>(mine + c * E + 2 * q) =
-            make_float4(acc[k][q].x, acc[k][q].y, acc[k][q + 1].x, acc[k][q + 1].y);
-    }
-  }
-  cl.sync();
-  const int slice = (((D + CS - 1) / CS) + 3) & ~3;
-  const int lo = crank * slice;
-  const int hi = lo + slice < D ? lo + slice : D;
-  float* cpart = a.part + (size_t)cid * D;
-  for (int j = lo + tid * 4; j < hi; j += kFfnBlock * 4) {
-    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = 0; r < CS; ++r) {
-      const float4 v = *reinterpret_cast<const float4*>(cl.map_shared_rank(mine, r) + j);
-      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-    }
-    *reinterpret_cast<float4*>(cpart + j) = sum;
-  }
-  cl.sync();  // no CTA leaves while its shared memory is being read
-  __threadfence();
-  __syncthreads();
-  __shared__ int s_last;
-  if (tid == 0) s_last = atomicAdd(&a.slice_cnt[crank], 1) == ncl - 1;
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    for (int j = lo + tid * 4; j < hi; j += kFfnBlock * 4) {
-      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-      int c = 0;
-      for (; c + 3 < ncl; c += 4) {  // four loads in flight, summed in cluster order
-        const float4 v0 = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)c * D + j));
-        const float4 v1 = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)(c + 1) * D + j));
-        const float4 v2 = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)(c + 2) * D + j));
-        const float4 v3 = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)(c + 3) * D + j));
-        y.x += v0.x; y.y += v0.y; y.z += v0.z; y.w += v0.w;
-        y.x += v1.x; y.y += v1.y; y.z += v1.z; y.w += v1.w;
-        y.x += v2.x; y.y += v2.y; y.z += v2.z; y.w += v2.w;
-        y.x += v3.x; y.y += v3.y; y.z += v3.z; y.w += v3.w;
-      }
-      for (; c < ncl; ++c) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)c * D + j));
-        y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
-      }
-      if (a.y_out) *reinterpret_cast<float4*>(a.y_out + j) = y;
-      if (a.h_out) {
-        const float4 h = *reinterpret_cast<const float4*>(a.h_in + j);
-        *reinterpret_cast<float4*>(a.h_out + j) = make_float4(h.x + y.x, h.y + y.y, h.z + y.z, h.w + y.w);
+        for (int q = 0; q < P; q += 2)
+          atomicAdd(reinterpret_cast<float4*>(a.y_acc + c * E + 2 * q),
+                    make_float4(acc[k][q].x, acc[k][q].y, acc[k][q + 1].x, acc[k][q + 1].y));
       }
     }
-    if (tid == 0) a.slice_cnt[crank] = 0;
   }
 }
 
@@ -413,51 +382,39 @@ static void* pick_kernel(int dtype, bool gated, int D, int dtype_bytes) {
 }
 
 size_t ffn_smem_bytes(int D, int dtype_bytes, int nproj, int n_stages) {
-  size_t ring = (size_t)n_stages * nproj * D * dtype_bytes;
-  if (ring < (size_t)D * 4) ring = (size_t)D * 4;  // the ring also parks the partial y
-  return 512 + ring + 64 * 4;
+  return 512 + (size_t)n_stages * nproj * D * dtype_bytes + 64 * 4;
 }
 
 int ffn_max_chunks() { return kFfnThreads * 4; }
-size_t ffn_counter_bytes() { return 16 * sizeof(int); }
 
-cudaError_t ffn_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_optin, int n_sms, int* n_stages,
-                     int* cluster, int* grid) {
+cudaError_t ffn_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_per_sm, int n_sms, int* n_stages,
+                     int* grid) {
   const int nproj = gated ? 3 : 2;
-  int ns = 16;  // one CTA per SM with as many ring slots (4..16) as fit
-  while (ns > 4 && ffn_smem_bytes(D, dtype_bytes, nproj, ns) > smem_optin) --ns;
-  if (ffn_smem_bytes(D, dtype_bytes, nproj, ns) > smem_optin) return cudaErrorInvalidValue;
+  // shared memory for two CTAs per SM (so the next layer's CTAs can prefetch
+  // beside the current ones), each with as many ring slots (2..16) as fit
+  const size_t per_cta = smem_per_sm / 2 > 1024 ? smem_per_sm / 2 - 1024 : 0;
+  int ns = 16;
+  while (ns > 2 && ffn_smem_bytes(D, dtype_bytes, nproj, ns) > per_cta) --ns;
+  if (ffn_smem_bytes(D, dtype_bytes, nproj, ns) > per_cta) return cudaErrorInvalidValue;
   void* k = pick_kernel(dtype, gated != 0, D, dtype_bytes);
   const size_t smem = ffn_smem_bytes(D, dtype_bytes, nproj, ns);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // the largest cluster that still keeps (nearly) every SM busy
-  int best_cs = 1, best_ctas = 0;
-  for (int cs : {8, 4, 2}) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cs * ((n_sms + cs - 1) / cs), 1, 1);
-    cfg.blockDim = dim3(kFfnBlock, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = cs;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n * cs > best_ctas + n_sms / 16) {  // prefer larger clusters unless they idle >6% of SMs
-      best_ctas = n * cs;
-      best_cs = cs;
-    }
-  }
-  if (best_ctas == 0) return cudaErrorInvalidConfiguration;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kFfnBlock, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // one CTA per SM per launch: the second slot of every SM is left to the
+  // next launch in the stream, which then streams beside this one
   *n_stages = ns;
-  *cluster = best_cs;
-  *grid = best_ctas;
+  *grid = n_sms;
   return cudaSuccess;
+}
+
+cudaError_t ffn_set_smem(int dtype, int gated, int D, int dtype_bytes, int n_stages) {
+  void* k = pick_kernel(dtype, gated != 0, D, dtype_bytes);
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)ffn_smem_bytes(D, dtype_bytes, gated ? 3 : 2, n_stages));
 }
 
 cudaError_t launch_ffn_rows(const FfnLaunch& a, cudaStream_t st) {
@@ -468,10 +425,8 @@ cudaError_t launch_ffn_rows(const FfnLaunch& a, cudaStream_t st) {
   cfg.dynamicSmemBytes = ffn_smem_bytes(a.D, a.dtype_bytes, a.gated ? 3 : 2, a.n_stages);
   cfg.stream = st;
   cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = a.cluster;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   FfnLaunch arg = a;

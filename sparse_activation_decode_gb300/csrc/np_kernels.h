@@ -17,7 +17,11 @@ constexpr int kMaxChunksPerThread = 4; // 16-byte chunks per row <= kThreads * 4
 
 // ---- FFN over a row list (np_ffn.cu) -------------------------------------
 struct FfnLaunch {
-  const float* h_in;      // [D] residual stream entering the layer
+  const float* h_in;      // [D] residual base entering the layer
+  const float* yprev;     // [D] previous layer's y (h = h_in + yprev), or null
+  float* hb_out;          // CTA 0 stores h here, or null
+  float* y_acc;           // [D] y is added here (cleared beforehand)
+  float* y_zero;          // [D] CTA 0 clears it (the accumulator after next), or null
   const void* w_gate;     // [rows][D] or null when !gated
   const void* w_up;       // [rows][D]
   const void* w_down;     // [rows][D] (down^T rows)
@@ -26,11 +30,6 @@ struct FfnLaunch {
   int n_rows_host;
   int list_cap;           // capacity of row_list (upper bound of the count)
   int row_limit;          // rows present in the weight buffers
-  float* part;            // [grid / cluster][D] cluster partial sums
-  int* slice_cnt;         // [cluster] arrival counters, zero between launches
-  int cluster;            // CTAs per thread-block cluster (grid % cluster == 0)
-  float* h_out;           // h_in + y (may alias h_in), or null
-  float* y_out;           // y, or null
   int D;
   int dtype;              // 0 f32, 1 f16, 2 bf16
   int dtype_bytes;
@@ -40,11 +39,12 @@ struct FfnLaunch {
   int* err;
 };
 size_t ffn_smem_bytes(int D, int dtype_bytes, int nproj, int n_stages);
-// Ring depth, cluster size and grid (one CTA per SM) of the FFN launch.
-cudaError_t ffn_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_optin, int n_sms, int* n_stages,
-                     int* cluster, int* grid);
+// Ring depth and grid (two CTAs per SM) of the FFN launch.
+cudaError_t ffn_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_per_sm, int n_sms, int* n_stages,
+                     int* grid);
 int ffn_max_chunks();        // 16-byte chunks per row the FFN supports
-size_t ffn_counter_bytes();  // bytes of slice-counter state
+// Allow the dynamic shared memory of an n_stages ring (after changing it).
+cudaError_t ffn_set_smem(int dtype, int gated, int D, int dtype_bytes, int n_stages);
 cudaError_t launch_ffn_rows(const FfnLaunch& a, cudaStream_t st);
 
 // ---- row dot products: predictor layers (np_pred.cu) ----------------------
@@ -55,7 +55,8 @@ struct RowdotLaunch {
   int n_rows;
   int len;
   const float* vec;       // [len] fp32 input vector
-  int vec_rmsnorm;        // 1: use rmsnorm(vec) instead of vec
+  const float* vec2;      // added to vec before the rmsnorm, or null
+  int vec_rmsnorm;        // 1: use rmsnorm(vec + vec2) instead of vec
   int mode;
   const void* bias;       // mode 2: [n_rows] of dtype
   float* out_f;           // modes 0, 2

@@ -5,16 +5,16 @@
 // latency-critical path where a device allocation would implicitly
 // synchronize the device.  For them this entry point runs the same FFN
 // kernel as np_sparse_mlp / np_dense_mlp on caller-provided weights, row
-// list, input and output, with its split-K scratch (cluster partial sums,
-// per-slice arrival counters, error word) in one file-scope __device__
-// array of fixed size instead of model-owned device allocations.
+// list, input and output.  The kernel's only state besides the caller's
+// buffers is its error word, which lives in one file-scope __device__ array
+// of fixed size instead of a model-owned device allocation.
 //
 // The array is a host-side stand-in in host code: its device address is
 // looked up once per device with cudaGetSymbolAddress while that device is
 // current (the first call on a device does this, so that first call should
 // come before any stream capture), and only that address is passed to the
 // kernel.  Every call on a device shares the array and it keeps the last
-// call's contents; the counters and the error word are cleared on the
+// call's contents; the error word and the output are cleared on the
 // caller's stream before each launch.  Calls whose kernels overlap on the
 // GPU race on the array: serialize them (one stream, or events).
 #include <mutex>
@@ -25,12 +25,10 @@
 namespace np {
 
 constexpr int kNoallocMaxDevices = 64;
-constexpr size_t kNoallocPartialFloats = 256 * 1024;  // 1 MiB of cluster partials
-constexpr size_t kNoallocCounters = 64;               // slice counters + error word
+constexpr size_t kNoallocWords = 64;  // error word (and room to grow)
 
 struct NoallocScratch {
-  float partial[kNoallocPartialFloats];
-  int counters[kNoallocCounters];
+  int words[kNoallocWords];
 };
 
 static __device__ __align__(256) NoallocScratch g_noalloc_scratch;
@@ -75,22 +73,20 @@ extern "C" np_status np_ffn_rows_noalloc(const float* h_dev, const void* w_gate,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   NoallocScratch* scratch = nullptr;
   if (noalloc_scratch_for_current_device(&scratch) != cudaSuccess) return NP_ERR_CUDA;
-  int dev = 0, sms = 0, optin = 0;
+  int dev = 0, sms = 0, smem_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return NP_ERR_CUDA;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  int n_stages = 0, cluster = 1, grid = 0;
-  if (ffn_plan(dtype, has_gate, d_model, esz, (size_t)optin - 1024, sms, &n_stages, &cluster, &grid) != cudaSuccess)
+  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  int n_stages = 0, grid = 0;
+  if (ffn_plan(dtype, has_gate, d_model, esz, (size_t)smem_sm, sms, &n_stages, &grid) != cudaSuccess)
     return NP_ERR_CUDA;
-  // the cluster partials must fit the fixed scratch: shrink the grid if needed
-  const int max_clusters = (int)(kNoallocPartialFloats / (size_t)d_model);
-  if (grid / cluster > max_clusters) grid = max_clusters * cluster;
-  if (grid < cluster || cluster + 1 > (int)kNoallocCounters) return NP_ERR_ARG;
-  int* err_word = scratch->counters + kNoallocCounters - 1;
-  if (cudaMemsetAsync(scratch->counters, 0, sizeof(scratch->counters), st) != cudaSuccess) return NP_ERR_CUDA;
+  int* err_word = scratch->words;
+  if (cudaMemsetAsync(scratch->words, 0, sizeof(scratch->words), st) != cudaSuccess) return NP_ERR_CUDA;
+  if (cudaMemsetAsync(y_dev, 0, sizeof(float) * (size_t)d_model, st) != cudaSuccess) return NP_ERR_CUDA;
 
   FfnLaunch a{};
   a.h_in = h_dev;
+  a.y_acc = y_dev;
   a.w_gate = has_gate ? w_gate : nullptr;
   a.w_up = w_up;
   a.w_down = w_down;
@@ -99,11 +95,6 @@ extern "C" np_status np_ffn_rows_noalloc(const float* h_dev, const void* w_gate,
   a.n_rows_host = n_rows;
   a.list_cap = rows_dev ? n_rows : row_limit;
   a.row_limit = row_limit;
-  a.part = scratch->partial;
-  a.slice_cnt = scratch->counters;
-  a.h_out = nullptr;
-  a.y_out = y_dev;
-  a.cluster = cluster;
   a.D = d_model;
   a.dtype = dtype;
   a.dtype_bytes = esz;

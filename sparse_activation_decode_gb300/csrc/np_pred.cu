@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 2) rowdot_kernel(RowdotLaunch a) {
   }
 
   if (a.vec_rmsnorm) {
-    rmsnorm_to_smem(a.vec, xs, len, red1);
+    rmsnorm_to_smem(a.vec, a.vec2, xs, len, red1);
   } else {
     for (int j = tid; j < len; j += kThreads) xs[j] = a.vec[j];
     __syncthreads();

@@ -194,6 +194,14 @@ class SparseDecoder:
         self._back()
         return y
 
+    def ffn_layers(self, first: int, count: int, h: torch.Tensor) -> torch.Tensor:
+        """FFNs of layers first..first+count-1 on the resident rows, h updated
+        in place ([batch][D] float32 on the device)."""
+        self._on_main(h)
+        L.check(self.lib.np_ffn_layers(self.model, first, count, h.data_ptr()), "np_ffn_layers")
+        self._back()
+        return h
+
     def reset_sequence(self) -> None:
         L.check(self.lib.np_reset_sequence(self.model), "np_reset_sequence")
 
