@@ -101,6 +101,9 @@ struct np_model {
   std::vector<void*> allocs;
   // launch shapes
   int ffn_grid = 0, ffn_stages = 0;
+  int chain_grid = 0, chain_stages = 0;  // persistent FFN chain (batch 1)
+  unsigned* arrive = nullptr;            // [2L] arrival counters of the chain
+  float* chain_part = nullptr;           // [chain_grid][D] partial y of the chain
   int gather_grid = 0, scatter_grid = 0, pred_grid = 0;
   int rps1 = 1, rps2 = 1, ns1 = 2, ns2 = 2;
   // state
@@ -761,6 +764,11 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     }
     const int ctas = env_int("NP_TUNE_FFN_CTAS", 0);
     if (ctas > 0) m->ffn_grid = ctas;
+    if (m->B == 1) {
+      e = ffn_chain_plan(m->d.dtype, m->d.has_gate, m->D, m->esz, m->smem_optin - 1024, m->sms, &m->chain_stages,
+                         &m->chain_grid);
+      if (e != cudaSuccess) return fail(cuda_fail(e, "ffn_chain_plan"));
+    }
   }
   // Host-link gathers need only a few MB in flight to fill the link; keeping
   // their grids small leaves the SMs to the FFN running beside them.
@@ -807,6 +815,8 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if ((st = dev_alloc(m, &m->ids, (size_t)m->B * (m->NH > 0 ? m->NH : 1))) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->fire, (size_t)m->W)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->logits, F)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->arrive, 2 * (size_t)m->L)) != NP_OK) return fail(st);
+  if (m->B == 1 && (st = dev_alloc(m, &m->chain_part, (size_t)m->chain_grid * m->D)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->hbase, 2 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->yacc, 3 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
 
@@ -1038,6 +1048,33 @@ np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev)
   // the same chaining as np_decode_token, relative to `first`
   cudaStream_t st = m->main;
   CUDA_TRY(cudaMemsetAsync(chain_y(m, 0), 0, sizeof(float) * m->B * m->D, st));
+  if (!m->tc) {
+    // batch 1: one persistent kernel streams the whole range
+    CUDA_TRY(cudaMemsetAsync(m->arrive, 0, sizeof(unsigned) * 2 * (size_t)count, st));
+    FfnChainLaunch a{};
+    a.dense_w = m->d.dense_w;
+    a.bufs = m->bufs;
+    a.active_slot = m->active_slot;
+    a.counts = m->counts;
+    a.n_dense = m->dn;
+    a.F = m->F;
+    a.K = m->K;
+    a.first = first;
+    a.count = count;
+    a.h = h_dev;
+    a.hbase = m->hbase;
+    a.yacc = m->yacc;
+    a.part = m->chain_part;
+    a.arrive = m->arrive;
+    a.D = m->D;
+    a.dtype = m->d.dtype;
+    a.dtype_bytes = m->esz;
+    a.gated = m->d.has_gate;
+    a.n_stages = m->chain_stages;
+    a.grid = m->chain_grid;
+    a.err = m->err;
+    return launch(m, NP_KIND_FFN, st, 0, [&] { return launch_ffn_chain(a, st); });
+  }
   for (int i = 0; i < count; ++i) {
     const float* hb = i <= 1 ? h_dev : chain_base(m, i - 1);
     NP_TRY(enqueue_layer_ffn(m, st, first + i, hb, i == 0 ? nullptr : chain_y(m, i - 1),

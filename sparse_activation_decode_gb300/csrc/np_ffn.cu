@@ -38,9 +38,12 @@
 
 namespace np {
 
-constexpr int kFfnThreads = 256;                 // consumer threads
+constexpr int kFfnThreads = 256;                 // consumer threads of the per-layer kernel
 constexpr int kFfnWarps = kFfnThreads / 32;      // consumer warps
 constexpr int kFfnBlock = kFfnThreads + 32;      // plus one producer warp
+constexpr int kChainThreads = 512;               // consumer threads of the persistent chain
+constexpr int kChainBlock = kChainThreads + 32;
+constexpr int kChainGroup = 4;                   // rows per block barrier in the chain
 constexpr int kRowCache = 64;                    // row indices cached per CTA
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -82,13 +85,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ void consumer_sync() {  // warps 0-7 only
-  asm volatile("bar.sync 1, %0;" ::"n"(kFfnThreads) : "memory");
+// Named barrier 1 over the NT consumer threads (the producer warp never joins).
+template <int NT> __device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
-// Named barrier over the consumer warps that also ORs a predicate: every
-// consumer thread gets the same answer.
-__device__ __forceinline__ bool consumer_sync_or(bool pred) {
+// The same barrier, also ORing a predicate: every consumer gets the answer.
+template <int NT> __device__ __forceinline__ bool consumer_sync_or(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
@@ -96,7 +99,7 @@ __device__ __forceinline__ bool consumer_sync_or(bool pred) {
       "bar.red.or.pred q, 1, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)pred), "n"(kFfnThreads)
+      : "r"((uint32_t)pred), "n"(NT)
       : "memory");
   return r != 0;
 }
@@ -106,12 +109,296 @@ __device__ __forceinline__ void grid_dependents_launch() {
 }
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------------------------
+// Pieces shared by the per-layer kernel and the persistent chain kernel.
+// ---------------------------------------------------------------------------
+// x = rmsnorm(h_in + yprev) into registers: consumer thread t holds the
+// chunks t, t+NT, ... it multiplies.  A writer CTA also stores h (hb_out)
+// and clears y_zero.
+template <typename T, int MAXC, int NT>
+__device__ __forceinline__ void load_x(const float* __restrict__ h_in, const float* __restrict__ yprev,
+                                       float* hb_out, float* y_zero, bool writer, int D,
+                                       float2 (&xr)[MAXC][Pairs<T>::N], float* red) {
+  constexpr int P = Pairs<T>::N, E = 2 * P;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int NC = D / E;
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < MAXC; ++k) {
+    const int c = tid + k * NT;
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      float2 v = make_float2(0.f, 0.f);
+      if (c < NC) {
+        v = *reinterpret_cast<const float2*>(h_in + c * E + 2 * q);
+        if (yprev) {
+          const float2 w = *reinterpret_cast<const float2*>(yprev + c * E + 2 * q);
+          v.x += w.x;
+          v.y += w.y;
+        }
+        if (writer) {
+          if (hb_out) *reinterpret_cast<float2*>(hb_out + c * E + 2 * q) = v;
+          if (y_zero) *reinterpret_cast<float2*>(y_zero + c * E + 2 * q) = make_float2(0.f, 0.f);
+        }
+      }
+      xr[k][q] = v;
+      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, ss));
+    }
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) red[warp] = ss;
+  consumer_sync<NT>();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / (float)D + 1e-6f);
+#pragma unroll
+  for (int k = 0; k < MAXC; ++k)
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      xr[k][q].x *= inv;
+      xr[k][q].y *= inv;
+    }
+  consumer_sync<NT>();  // red is reused by the rows
+}
+
+// A group of up to GR records (rr[0..nrow) in shared memory): GR gate and up
+// dot products per thread, reduce-scattered over each warp, one named
+// barrier (that also ORs !ok) to publish the warps' partials, then every warp
+// adds the partials itself, forms the GR activations and applies the down
+// projection to its chunks.  Returns false, for every consumer alike, if
+// any thread's record never arrived.  `grp` alternates the halves of `red`.
+template <typename T, bool GATED, int MAXC, int NT, int GR>
+__device__ __forceinline__ bool consume_group(const uint4* __restrict__ sm4, const int (&off)[GR], int nrow, bool ok,
+                                              int grp, int NC, const float2 (&xr)[MAXC][Pairs<T>::N],
+                                              float2 (&acc)[MAXC][Pairs<T>::N], float* red) {
+  constexpr int P = Pairs<T>::N;
+  constexpr int NPROJ = GATED ? 3 : 2;
+  constexpr int NV = (GATED ? 2 : 1) * GR;  // dot products per group
+  constexpr int NW = NT / 32;
+  static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "values per group must be a power of two");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float2 d2[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) d2[v] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < MAXC; ++k) {
+    const int c = tid + k * NT;
+    if (c < NC) {
+      float2 f[P];
+#pragma unroll
+      for (int r = 0; r < GR; ++r) {
+        if (r < nrow) {
+          if (GATED) {
+            Pairs<T>::load(sm4[off[r] + c], f);
+#pragma unroll
+            for (int q = 0; q < P; ++q) d2[2 * r] = ffma2(f[q], xr[k][q], d2[2 * r]);
+            Pairs<T>::load(sm4[off[r] + NC + c], f);
+#pragma unroll
+            for (int q = 0; q < P; ++q) d2[2 * r + 1] = ffma2(f[q], xr[k][q], d2[2 * r + 1]);
+          } else {
+            Pairs<T>::load(sm4[off[r] + c], f);
+#pragma unroll
+            for (int q = 0; q < P; ++q) d2[r] = ffma2(f[q], xr[k][q], d2[r]);
+          }
+        }
+      }
+    }
+  }
+  // warp reduce-scatter: the lanes with (lane & (32/NV - 1)) == 0 end with
+  // the warp sum of value vi(lane)
+  float pv[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) pv[v] = d2[v].x + d2[v].y;
+  int cnt = NV, vi = 0;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (cnt > 1) {
+      const bool up = (lane & off) != 0;
+      const int half = cnt >> 1;
+#pragma unroll
+      for (int q = 0; q < NV / 2; ++q) {
+        if (q < half) {
+          const float send = up ? pv[q] : pv[q + half];
+          const float keep = up ? pv[q + half] : pv[q];
+          pv[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+      vi = vi * 2 + (up ? 1 : 0);
+      cnt = half;
+    } else {
+      pv[0] += __shfl_xor_sync(0xffffffffu, pv[0], off);
+    }
+  }
+  float* rb = red + (grp & 1) * NW * NV;
+  if ((lane & (32 / NV - 1)) == 0) rb[warp * NV + vi] = pv[0];
+  if (consumer_sync_or<NT>(!ok)) return false;  // a copy never arrived: all consumers stop
+  // lane v < NV adds value v over the warps (fixed order), then the
+  // activations go to every lane
+  float tot = 0.f;
+  if (lane < NV) {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) tot += rb[w * NV + lane];
+  }
+  float hv[GR];
+#pragma unroll
+  for (int r = 0; r < GR; ++r) {
+    if (GATED) {
+      const float g = __shfl_sync(0xffffffffu, tot, 2 * r);
+      const float u = __shfl_sync(0xffffffffu, tot, 2 * r + 1);
+      hv[r] = (g > 0.f ? g : 0.f) * u;
+    } else {
+      const float u = __shfl_sync(0xffffffffu, tot, r);
+      hv[r] = u > 0.f ? u : 0.f;
+    }
+  }
+  const int dn = (NPROJ - 1) * NC;
+#pragma unroll
+  for (int k = 0; k < MAXC; ++k) {
+    const int c = tid + k * NT;
+    if (c < NC) {
+      float2 f[P];
+#pragma unroll
+      for (int r = 0; r < GR; ++r) {
+        if (r < nrow) {
+          const float2 h2 = make_float2(hv[r], hv[r]);
+          Pairs<T>::load(sm4[off[r] + dn + c], f);
+#pragma unroll
+          for (int q = 0; q < P; ++q) acc[k][q] = ffma2(h2, f[q], acc[k][q]);
+        }
+      }
+    }
+  }
+  return true;
+}
+
+// The same group computation, but every chunk of the group's records (gate,
+// up and down^T) is read into registers first and the slots are released
+// right away (one arrive per warp on each slot's `empty` barrier), so the
+// producer refills them while this group's reduction and down projection
+// run.
+template <typename T, bool GATED, int MAXC, int NT, int GR>
+__device__ __forceinline__ bool consume_group_early(const uint4* __restrict__ sm4, const int (&off)[GR],
+                                                    const int (&slot)[GR], uint64_t* empty, int nrow, bool ok,
+                                                    int grp, int NC, const float2 (&xr)[MAXC][Pairs<T>::N],
+                                                    float2 (&acc)[MAXC][Pairs<T>::N], float* red) {
+  constexpr int P = Pairs<T>::N;
+  constexpr int NPROJ = GATED ? 3 : 2;
+  constexpr int NV = (GATED ? 2 : 1) * GR;
+  constexpr int NW = NT / 32;
+  static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "values per group must be a power of two");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint4 w[GR][NPROJ][MAXC];
+#pragma unroll
+  for (int r = 0; r < GR; ++r)
+#pragma unroll
+    for (int p = 0; p < NPROJ; ++p)
+#pragma unroll
+      for (int k = 0; k < MAXC; ++k) {
+        const int c = tid + k * NT;
+        w[r][p][k] = (r < nrow && c < NC) ? sm4[off[r] + p * NC + c] : make_uint4(0u, 0u, 0u, 0u);
+      }
+  __syncwarp();
+  if (lane == 0)
+    for (int r = 0; r < nrow; ++r) mbar_arrive(&empty[slot[r]]);
+  float2 d2[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) d2[v] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < MAXC; ++k) {
+    float2 f[P];
+#pragma unroll
+    for (int r = 0; r < GR; ++r) {
+      if (GATED) {
+        Pairs<T>::load(w[r][0][k], f);
+#pragma unroll
+        for (int q = 0; q < P; ++q) d2[2 * r] = ffma2(f[q], xr[k][q], d2[2 * r]);
+        Pairs<T>::load(w[r][1][k], f);
+#pragma unroll
+        for (int q = 0; q < P; ++q) d2[2 * r + 1] = ffma2(f[q], xr[k][q], d2[2 * r + 1]);
+      } else {
+        Pairs<T>::load(w[r][0][k], f);
+#pragma unroll
+        for (int q = 0; q < P; ++q) d2[r] = ffma2(f[q], xr[k][q], d2[r]);
+      }
+    }
+  }
+  float pv[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) pv[v] = d2[v].x + d2[v].y;
+  int cnt = NV, vi = 0;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (cnt > 1) {
+      const bool up = (lane & o) != 0;
+      const int half = cnt >> 1;
+#pragma unroll
+      for (int q = 0; q < NV / 2; ++q) {
+        if (q < half) {
+          const float send = up ? pv[q] : pv[q + half];
+          const float keep = up ? pv[q + half] : pv[q];
+          pv[q] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      vi = vi * 2 + (up ? 1 : 0);
+      cnt = half;
+    } else {
+      pv[0] += __shfl_xor_sync(0xffffffffu, pv[0], o);
+    }
+  }
+  float* rb = red + (grp & 1) * NW * NV;
+  if ((lane & (32 / NV - 1)) == 0) rb[warp * NV + vi] = pv[0];
+  if (consumer_sync_or<NT>(!ok)) return false;
+  float tot = 0.f;
+  if (lane < NV) {
+#pragma unroll
+    for (int ww = 0; ww < NW; ++ww) tot += rb[ww * NV + lane];
+  }
+#pragma unroll
+  for (int r = 0; r < GR; ++r) {
+    float hv;
+    if (GATED) {
+      const float g = __shfl_sync(0xffffffffu, tot, 2 * r);
+      const float u = __shfl_sync(0xffffffffu, tot, 2 * r + 1);
+      hv = (g > 0.f ? g : 0.f) * u;
+    } else {
+      const float u = __shfl_sync(0xffffffffu, tot, r);
+      hv = u > 0.f ? u : 0.f;
+    }
+    const float2 h2 = make_float2(hv, hv);
+#pragma unroll
+    for (int k = 0; k < MAXC; ++k) {
+      float2 f[P];
+      Pairs<T>::load(w[r][NPROJ - 1][k], f);  // zero chunks add nothing
+#pragma unroll
+      for (int q = 0; q < P; ++q) acc[k][q] = ffma2(h2, f[q], acc[k][q]);
+    }
+  }
+  return true;
+}
+
+// This CTA's partial y into the layer's accumulator (vector atomics).
+template <typename T, int MAXC, int NT>
+__device__ __forceinline__ void add_partial_y(const float2 (&acc)[MAXC][Pairs<T>::N], float* y_acc, int NC) {
+  constexpr int P = Pairs<T>::N, E = 2 * P;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int k = 0; k < MAXC; ++k) {
+    const int c = tid + k * NT;
+    if (c < NC) {
+#pragma unroll
+      for (int q = 0; q < P; q += 2)
+        atomicAdd(reinterpret_cast<float4*>(y_acc + c * E + 2 * q),
+                  make_float4(acc[k][q].x, acc[k][q].y, acc[k][q + 1].x, acc[k][q + 1].y));
+    }
+  }
+}
+
 template <typename T, bool GATED, int MAXC>
 __global__ void __launch_bounds__(kFfnBlock, 2) ffn_rows_kernel(FfnLaunch a) {
   constexpr int P = Pairs<T>::N;      // float pairs per 16-byte chunk
   constexpr int E = 2 * P;            // elements per chunk
   constexpr int NPROJ = GATED ? 3 : 2;
-  constexpr int NV = GATED ? 4 : 2;   // dot products per pair of rows
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // [16]
   uint64_t* empty = full + 16;                           // [16]
@@ -158,9 +445,10 @@ __global__ void __launch_bounds__(kFfnBlock, 2) ffn_rows_kernel(FfnLaunch a) {
       const T* w_gate = static_cast<const T*>(a.w_gate);
       const T* w_up = static_cast<const T*>(a.w_up);
       const T* w_down = static_cast<const T*>(a.w_down);
+      int s = 0;
+      uint32_t wrap = 0;  // ring position without divisions: slot s, pass `wrap`
       for (int j = 0; j < my_n; ++j) {
-        const int s = j % n_slots;
-        if (j >= n_slots && !mbar_wait(&empty[s], (uint32_t)(j / n_slots - 1) & 1u, a.err)) {
+        if (wrap > 0 && !mbar_wait(&empty[s], (wrap - 1) & 1u, a.err)) {
           s_abort = 1;
           break;
         }
@@ -176,155 +464,41 @@ __global__ void __launch_bounds__(kFfnBlock, 2) ffn_rows_kernel(FfnLaunch a) {
         bulk_load(dst + (p++) * row_bytes, w_up + (size_t)r * D, row_bytes, &full[s], pol);
         bulk_load(dst + p * row_bytes, w_down + (size_t)r * D, row_bytes, &full[s], pol);
         s_issued = j + 1;
+        if (++s == n_slots) {
+          s = 0;
+          ++wrap;
+        }
       }
     }
   } else {
     // ------------------------------------------------------------ consumers
-    // x = rmsnorm(h_in + yprev): each thread reads its own chunks of h, once
-    // the previous kernel's writes are visible.  CTA 0 stores h for the next
-    // layer and clears the accumulator after next.
+    // x = rmsnorm(h_in + yprev), once the previous kernel's writes are
+    // visible; CTA 0 stores h for the next layer and clears the accumulator
+    // after next.
     grid_dependency_wait();
     float2 xr[MAXC][P];
-    float ss = 0.f;
-#pragma unroll
-    for (int k = 0; k < MAXC; ++k) {
-      const int c = tid + k * kFfnThreads;
-#pragma unroll
-      for (int q = 0; q < P; ++q) {
-        float2 v = make_float2(0.f, 0.f);
-        if (c < NC) {
-          v = *reinterpret_cast<const float2*>(a.h_in + c * E + 2 * q);
-          if (a.yprev) {
-            const float2 w = *reinterpret_cast<const float2*>(a.yprev + c * E + 2 * q);
-            v.x += w.x;
-            v.y += w.y;
-          }
-          if (blockIdx.x == 0) {
-            if (a.hb_out) *reinterpret_cast<float2*>(a.hb_out + c * E + 2 * q) = v;
-            if (a.y_zero) *reinterpret_cast<float2*>(a.y_zero + c * E + 2 * q) = make_float2(0.f, 0.f);
-          }
-        }
-        xr[k][q] = v;
-        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, ss));
-      }
-    }
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    consumer_sync();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kFfnWarps; ++w) tot += red[w];
-    const float inv = rsqrtf(tot / (float)D + 1e-6f);
-#pragma unroll
-    for (int k = 0; k < MAXC; ++k)
-#pragma unroll
-      for (int q = 0; q < P; ++q) {
-        xr[k][q].x *= inv;
-        xr[k][q].y *= inv;
-      }
-    consumer_sync();  // red is reused below
-
+    load_x<T, MAXC, kFfnThreads>(a.h_in, a.yprev, a.hb_out, a.y_zero, blockIdx.x == 0, D, xr, red);
+    int cs = 0;
+    uint32_t cwrap = 0;  // ring position of row j: slot cs, pass cwrap
     for (int j = 0; j < my_n; j += 2) {
       const bool two = j + 1 < my_n;
-      const int s0 = j % n_slots, s1 = (j + 1) % n_slots;
-      bool ok = mbar_wait(&full[s0], (uint32_t)(j / n_slots) & 1u, a.err);
-      if (two) ok = mbar_wait(&full[s1], (uint32_t)((j + 1) / n_slots) & 1u, a.err) && ok;
-      const uint4* r0 = reinterpret_cast<const uint4*>(ring + (size_t)s0 * slot_bytes);
-      const uint4* r1 = reinterpret_cast<const uint4*>(ring + (size_t)s1 * slot_bytes);
-      float2 d2[NV];
-#pragma unroll
-      for (int v = 0; v < NV; ++v) d2[v] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < MAXC; ++k) {
-        const int c = tid + k * kFfnThreads;
-        if (c < NC) {
-          float2 f[P];
-#pragma unroll
-          for (int row = 0; row < 2; ++row) {
-            if (row == 1 && !two) break;
-            const uint4* rr = row ? r1 : r0;
-            if (GATED) {
-              Pairs<T>::load(rr[c], f);
-#pragma unroll
-              for (int q = 0; q < P; ++q) d2[row * 2] = ffma2(f[q], xr[k][q], d2[row * 2]);
-              Pairs<T>::load(rr[NC + c], f);
-#pragma unroll
-              for (int q = 0; q < P; ++q) d2[row * 2 + 1] = ffma2(f[q], xr[k][q], d2[row * 2 + 1]);
-            } else {
-              Pairs<T>::load(rr[c], f);
-#pragma unroll
-              for (int q = 0; q < P; ++q) d2[row] = ffma2(f[q], xr[k][q], d2[row]);
-            }
-          }
-        }
+      const int s0 = cs;
+      const bool w1 = cs + 1 == n_slots;
+      const int s1 = w1 ? 0 : cs + 1;
+      bool ok = mbar_wait(&full[s0], cwrap & 1u, a.err);
+      if (two) ok = mbar_wait(&full[s1], (cwrap + (w1 ? 1u : 0u)) & 1u, a.err) && ok;
+      if (two) {
+        cs = w1 ? 1 : (cs + 2 == n_slots ? 0 : cs + 2);
+        cwrap += (w1 || cs == 0) ? 1u : 0u;
+      } else {
+        cs = w1 ? 0 : cs + 1;
+        cwrap += w1 ? 1u : 0u;
       }
-      // warp reduce-scatter: lane l ends with the warp sum of value vi(l)
-      float pv[NV];
-#pragma unroll
-      for (int v = 0; v < NV; ++v) pv[v] = d2[v].x + d2[v].y;
-      int cnt = NV, vi = 0;
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        if (cnt > 1) {
-          const bool up = (lane & off) != 0;
-          const int half = cnt >> 1;
-#pragma unroll
-          for (int q = 0; q < NV / 2; ++q) {
-            if (q < half) {
-              const float send = up ? pv[q] : pv[q + half];
-              const float keep = up ? pv[q + half] : pv[q];
-              pv[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-            }
-          }
-          vi = vi * 2 + (up ? 1 : 0);
-          cnt = half;
-        } else {
-          pv[0] += __shfl_xor_sync(0xffffffffu, pv[0], off);
-        }
-      }
-      float* rb = red + ((j >> 1) & 1) * kFfnWarps * NV;
-      if ((lane & (32 / NV - 1)) == 0) rb[warp * NV + vi] = pv[0];
-      if (consumer_sync_or(!ok)) {  // a copy never arrived: all consumers stop
+      const int off[2] = {(int)((512 + (size_t)s0 * slot_bytes) >> 4), (int)((512 + (size_t)s1 * slot_bytes) >> 4)};
+      if (!consume_group<T, GATED, MAXC, kFfnThreads, 2>(reinterpret_cast<const uint4*>(smem), off, two ? 2 : 1, ok,
+                                                          j >> 1, NC, xr, acc, red)) {
         if (tid == 0) s_abort = 1;
         break;
-      }
-      float t[NV];
-#pragma unroll
-      for (int v = 0; v < NV; ++v) t[v] = 0.f;
-#pragma unroll
-      for (int w = 0; w < kFfnWarps; ++w) {
-        if (NV == 4) {
-          const float4 x4 = reinterpret_cast<const float4*>(rb)[w];
-          t[0] += x4.x; t[1] += x4.y; t[2 % NV] += x4.z; t[3 % NV] += x4.w;
-        } else {
-          const float2 x2 = reinterpret_cast<const float2*>(rb)[w];
-          t[0] += x2.x; t[1] += x2.y;
-        }
-      }
-      float hv0, hv1;
-      if (GATED) {
-        hv0 = (t[0] > 0.f ? t[0] : 0.f) * t[1];
-        hv1 = (t[2 % NV] > 0.f ? t[2 % NV] : 0.f) * t[3 % NV];
-      } else {
-        hv0 = t[0] > 0.f ? t[0] : 0.f;
-        hv1 = t[1] > 0.f ? t[1] : 0.f;
-      }
-      const float2 h0 = make_float2(hv0, hv0), h1 = make_float2(hv1, hv1);
-      const int dn = (NPROJ - 1) * NC;
-#pragma unroll
-      for (int k = 0; k < MAXC; ++k) {
-        const int c = tid + k * kFfnThreads;
-        if (c < NC) {
-          float2 f[P];
-          Pairs<T>::load(r0[dn + c], f);
-#pragma unroll
-          for (int q = 0; q < P; ++q) acc[k][q] = ffma2(h0, f[q], acc[k][q]);
-          if (two) {
-            Pairs<T>::load(r1[dn + c], f);
-#pragma unroll
-            for (int q = 0; q < P; ++q) acc[k][q] = ffma2(h1, f[q], acc[k][q]);
-          }
-        }
       }
       // this warp is done with both slots
       __syncwarp();
@@ -342,19 +516,287 @@ __global__ void __launch_bounds__(kFfnBlock, 2) ffn_rows_kernel(FfnLaunch a) {
     const int first = issued > n_slots ? issued - n_slots : 0;
     for (int j = first; j < issued; ++j) mbar_wait(&full[j % n_slots], (uint32_t)(j / n_slots) & 1u, nullptr);
   }
-
   // ---- split-K: this CTA's partial y into the layer's accumulator
-  if (tid < kFfnThreads && !s_abort) {
-#pragma unroll
-    for (int k = 0; k < MAXC; ++k) {
-      const int c = tid + k * kFfnThreads;
-      if (c < NC) {
-#pragma unroll
-        for (int q = 0; q < P; q += 2)
-          atomicAdd(reinterpret_cast<float4*>(a.y_acc + c * E + 2 * q),
-                    make_float4(acc[k][q].x, acc[k][q].y, acc[k][q + 1].x, acc[k][q + 1].y));
+  if (tid < kFfnThreads && !s_abort) add_partial_y<T, MAXC, kFfnThreads>(acc, a.y_acc, NC);
+}
+
+// ---------------------------------------------------------------------------
+// Persistent chain over consecutive layers (np_ffn_layers, batch 1).  One
+// cooperative launch, one CTA per SM.  The producer streams every layer's
+// records without a break (the weights do not depend on h); the consumers
+// of layer i wait until every CTA has added its part of layer i-1 (an
+// arrival counter per layer, bounded spin) and then read h.  The ring keeps
+// the copies going while the consumers wait, so the per-layer barrier costs
+// little bandwidth.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until *cnt reaches `target` (bounded: about one second).
+__device__ __forceinline__ bool wait_count(const unsigned* cnt, unsigned target, int* err) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire_u32(cnt) >= target) return true;
+    if ((it & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) {
+      atomicExch(err, kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
+template <typename T, bool GATED, int MAXC>
+__global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunch a) {
+  constexpr int P = Pairs<T>::N;
+  constexpr int E = 2 * P;
+  constexpr int NPROJ = GATED ? 3 : 2;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // [16]
+  uint64_t* empty = full + 16;                           // [16]
+  const int D = a.D, n_slots = a.n_stages;
+  const uint32_t row_bytes = (uint32_t)D * sizeof(T);
+  const uint32_t slot_bytes = NPROJ * row_bytes;
+  unsigned char* ring = smem + 512;
+  float* red = reinterpret_cast<float*>(ring + (size_t)n_slots * slot_bytes);
+  __shared__ int s_abort, s_issued;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int NC = D / E;
+  const int G = (int)gridDim.x;
+  const size_t BD = (size_t)D;
+  const int n_slices = (D + 31) / 32;            // 32-column slices of y
+  const int n_red = n_slices < G ? n_slices : G;  // CTAs that sum slices
+
+  // layer i of the chain: weights, rows and this CTA's share of them
+  auto layer_rows = [&](int i, const T** wg, const T** wu, const T** wd, const int** list, int* limit) -> int {
+    const int l = a.first + i;
+    const unsigned char* base;
+    size_t proj;
+    int n;
+    if (l < a.n_dense) {
+      proj = (size_t)a.F * row_bytes;
+      base = static_cast<const unsigned char*>(a.dense_w) + (size_t)l * NPROJ * proj;
+      *list = nullptr;
+      n = a.F;
+      *limit = a.F;
+    } else {
+      const int s = l - a.n_dense;
+      proj = (size_t)a.K * row_bytes;
+      base = static_cast<const unsigned char*>(a.bufs) + (size_t)s * NPROJ * proj;
+      *list = a.active_slot + (size_t)s * a.K;
+      n = a.counts[(size_t)s * 4];
+      n = n < 0 ? 0 : (n > a.K ? a.K : n);
+      *limit = a.K;
+    }
+    int p = 0;
+    *wg = GATED ? reinterpret_cast<const T*>(base + (p++) * proj) : nullptr;
+    *wu = reinterpret_cast<const T*>(base + (p++) * proj);
+    *wd = reinterpret_cast<const T*>(base + p * proj);
+    return n > (int)blockIdx.x ? (n - 1 - (int)blockIdx.x) / G + 1 : 0;
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < n_slots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kChainThreads / 32);
+    }
+    fence_barrier_init();
+    s_abort = 0;
+    s_issued = 0;
+  }
+  __syncthreads();
+
+  if (warp == kChainThreads / 32) {
+    // ------------------------------------------------------------ producer
+    // The whole warp walks the rows: each lane fetches one of the next 32
+    // row indices, lane 0 takes them by shuffle and issues the copies, so no
+    // index load sits on the issue path.
+    const uint64_t pol = policy_evict_first();
+    int j = 0;
+    int ps = 0;          // slot of row j
+    uint32_t pwrap = 0;  // passes over the ring so far
+    bool stop = false;
+    for (int i = 0; i < a.count && !stop; ++i) {
+      const T *wg, *wu, *wd;
+      const int* list;
+      int limit;
+      const int my_n = layer_rows(i, &wg, &wu, &wd, &list, &limit);
+      for (int b0 = 0; b0 < my_n && !stop; b0 += 32) {
+        int mine = 0;
+        if (b0 + lane < my_n) {
+          mine = list ? list[blockIdx.x + (b0 + lane) * G] : (int)blockIdx.x + (b0 + lane) * G;
+          if ((unsigned)mine >= (unsigned)limit) {
+            atomicExch(a.err, kDevErrBounds);
+            mine = 0;
+          }
+        }
+        const int cnt = my_n - b0 < 32 ? my_n - b0 : 32;
+        for (int q = 0; q < cnt; ++q, ++j) {
+          const int r = __shfl_sync(0xffffffffu, mine, q);
+          int fail = 0;
+          if (lane == 0) {
+            const int s = ps;
+            if (pwrap > 0 && !mbar_wait(&empty[s], (pwrap - 1) & 1u, a.err)) {
+              fail = 1;
+            } else {
+              unsigned char* dst = ring + (size_t)s * slot_bytes;
+              mbar_arrive_expect_tx(&full[s], slot_bytes);
+              int p = 0;
+              if (GATED) bulk_load(dst + (p++) * row_bytes, wg + (size_t)r * D, row_bytes, &full[s], pol);
+              bulk_load(dst + (p++) * row_bytes, wu + (size_t)r * D, row_bytes, &full[s], pol);
+              bulk_load(dst + p * row_bytes, wd + (size_t)r * D, row_bytes, &full[s], pol);
+              s_issued = j + 1;
+            }
+          }
+          if (++ps == n_slots) {
+            ps = 0;
+            ++pwrap;
+          }
+          if (__shfl_sync(0xffffffffu, fail, 0)) {
+            if (lane == 0) s_abort = 1;
+            stop = true;
+            break;
+          }
+        }
       }
     }
+  } else {
+    // ------------------------------------------------------------ consumers
+    int cs = 0;          // slot of the next row
+    uint32_t cwrap = 0;  // passes over the ring so far
+    for (int i = 0; i < a.count; ++i) {
+      if (i > 0) {  // every slice of y(i-1) has been summed
+        bool ok = true;
+        if (tid == 0) ok = wait_count(a.arrive + 2 * (i - 1) + 1, (unsigned)n_red, a.err);
+        if (consumer_sync_or<kChainThreads>(!ok)) {
+          if (tid == 0) s_abort = 1;
+          break;
+        }
+      }
+      const float* hb = i <= 1 ? a.h : a.hbase + (size_t)((i - 1) & 1) * BD;
+      const float* yp = i == 0 ? nullptr : a.yacc + (size_t)((i - 1) % 3) * BD;
+      float* hb_out = i >= 1 ? a.hbase + (size_t)(i & 1) * BD : nullptr;
+      float* yi = a.yacc + (size_t)(i % 3) * BD;
+      float2 xr[MAXC][P];
+      load_x<T, MAXC, kChainThreads>(hb, yp, hb_out, nullptr, blockIdx.x == 0, D, xr, red);
+      float2 acc[MAXC][P];
+#pragma unroll
+      for (int k = 0; k < MAXC; ++k)
+#pragma unroll
+        for (int q = 0; q < P; ++q) acc[k][q] = make_float2(0.f, 0.f);
+      const T *wg, *wu, *wd;
+      const int* list;
+      int limit;
+      const int my_n = layer_rows(i, &wg, &wu, &wd, &list, &limit);
+      bool aborted = false;
+      for (int jj = 0; jj < my_n; jj += kChainGroup) {
+        const int nrow = my_n - jj < kChainGroup ? my_n - jj : kChainGroup;
+        bool ok = true;
+        int off[kChainGroup], slot[kChainGroup];
+#pragma unroll
+        for (int r = 0; r < kChainGroup; ++r) {
+          slot[r] = cs;
+          off[r] = (int)((512 + (size_t)cs * slot_bytes) >> 4);
+          if (r < nrow) {
+            ok = mbar_wait(&full[cs], cwrap & 1u, a.err) && ok;
+            if (++cs == n_slots) {
+              cs = 0;
+              ++cwrap;
+            }
+          }
+        }
+        if (!consume_group_early<T, GATED, MAXC, kChainThreads, kChainGroup>(
+                reinterpret_cast<const uint4*>(smem), off, slot, empty, nrow, ok, jj / kChainGroup, NC, xr, acc,
+                red)) {
+          aborted = true;
+          break;
+        }
+      }
+      if (aborted) {
+        if (tid == 0) s_abort = 1;
+        break;
+      }
+      // split-K in two fixed-order steps: every CTA stores its partial y;
+      // once all have, CTA r sums column slice r over the CTAs in order
+      {
+        float* mine = a.part + (size_t)blockIdx.x * BD;
+#pragma unroll
+        for (int k = 0; k < MAXC; ++k) {
+          const int c = tid + k * kChainThreads;
+          if (c < NC)
+#pragma unroll
+            for (int q = 0; q < P; q += 2)
+              *reinterpret_cast<float4*>(mine + c * E + 2 * q) =
+                  make_float4(acc[k][q].x, acc[k][q].y, acc[k][q + 1].x, acc[k][q + 1].y);
+        }
+      }
+      __threadfence();
+      consumer_sync<kChainThreads>();
+      if (tid == 0) atomicAdd(a.arrive + 2 * i, 1u);
+      if ((int)blockIdx.x < n_red) {
+        bool ok = true;
+        if (tid == 0) ok = wait_count(a.arrive + 2 * i, (unsigned)G, a.err);
+        if (consumer_sync_or<kChainThreads>(!ok)) {
+          if (tid == 0) s_abort = 1;
+          break;
+        }
+        float4* tmp = reinterpret_cast<float4*>(red + 64);  // [64][8]
+        const int f = tid & 7, g = tid >> 3;
+        for (int sl = (int)blockIdx.x; sl < n_slices; sl += G) {
+          // threads (g, f): float4 f of the slice, partials g, g + 64, ...
+          const int col = sl * 32 + 4 * f;
+          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (col < D)
+            for (int cta = g; cta < G; cta += kChainThreads / 8) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)cta * BD + col));
+              sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+            }
+          tmp[g * 8 + f] = sum;
+          consumer_sync<kChainThreads>();
+          if (tid < 8 && sl * 32 + 4 * tid < D) {
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int gg = 0; gg < kChainThreads / 8; ++gg) {
+              const float4 v = tmp[gg * 8 + tid];
+              t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+            }
+            *reinterpret_cast<float4*>(yi + sl * 32 + 4 * tid) = t;
+          }
+          consumer_sync<kChainThreads>();  // tmp is reused by the next slice
+        }
+        __threadfence();
+        consumer_sync<kChainThreads>();
+        if (tid == 0) atomicAdd(a.arrive + 2 * i + 1, 1u);
+      }
+    }
+    // the residual stream after the last layer: h = h_last + y_last
+    if (blockIdx.x == 0 && !s_abort) {
+      bool ok = true;
+      if (tid == 0) ok = wait_count(a.arrive + 2 * (a.count - 1) + 1, (unsigned)n_red, a.err);
+      if (!consumer_sync_or<kChainThreads>(!ok)) {
+        const int i = a.count - 1;
+        const float* hl = i == 0 ? a.h : a.hbase + (size_t)(i & 1) * BD;
+        const float* yl = a.yacc + (size_t)(i % 3) * BD;
+        for (int d = tid; d < D; d += kChainThreads) a.h[d] = hl[d] + yl[d];
+      }
+    }
+  }
+  __syncthreads();
+  if (s_abort && tid == kChainThreads) {
+    atomicExch(a.err, kDevErrTimeout);
+    const int issued = s_issued;
+    const int first = issued > n_slots ? issued - n_slots : 0;
+    for (int j = first; j < issued; ++j) mbar_wait(&full[j % n_slots], (uint32_t)(j / n_slots) & 1u, nullptr);
+  }
+}
+
+template <typename T, bool GATED>
+static void* chain_kernel_for(int maxc) {
+  switch (maxc) {
+    case 1: return reinterpret_cast<void*>(ffn_chain_kernel<T, GATED, 1>);
+    case 2: return reinterpret_cast<void*>(ffn_chain_kernel<T, GATED, 2>);
+    case 3: return reinterpret_cast<void*>(ffn_chain_kernel<T, GATED, 3>);
+    default: return reinterpret_cast<void*>(ffn_chain_kernel<T, GATED, 4>);
   }
 }
 
@@ -381,8 +823,22 @@ static void* pick_kernel(int dtype, bool gated, int D, int dtype_bytes) {
                                                                : kernel_for<__nv_bfloat16, false>(mc);
 }
 
+static void* pick_chain_kernel(int dtype, bool gated, int D, int dtype_bytes) {
+  const int mc = (D * dtype_bytes / 16 + kChainThreads - 1) / kChainThreads;
+  if (gated)
+    return dtype == 0 ? chain_kernel_for<float, true>(mc)
+                      : dtype == 1 ? chain_kernel_for<__half, true>(mc) : chain_kernel_for<__nv_bfloat16, true>(mc);
+  return dtype == 0 ? chain_kernel_for<float, false>(mc)
+                    : dtype == 1 ? chain_kernel_for<__half, false>(mc) : chain_kernel_for<__nv_bfloat16, false>(mc);
+}
+
 size_t ffn_smem_bytes(int D, int dtype_bytes, int nproj, int n_stages) {
-  return 512 + (size_t)n_stages * nproj * D * dtype_bytes + 64 * 4;
+  return 512 + (size_t)n_stages * nproj * D * dtype_bytes + 1024;  // barriers/rows, ring, partial sums
+}
+
+// the chain kernel also sums y slices in shared memory: 64 x 8 float4 more
+static size_t chain_smem_bytes(int D, int dtype_bytes, int nproj, int n_stages) {
+  return ffn_smem_bytes(D, dtype_bytes, nproj, n_stages) + 256 + 64 * 8 * 16;
 }
 
 int ffn_max_chunks() { return kFfnThreads * 4; }
@@ -430,6 +886,42 @@ cudaError_t launch_ffn_rows(const FfnLaunch& a, cudaStream_t st) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   FfnLaunch arg = a;
+  void* params[] = {&arg};
+  return cudaLaunchKernelExC(&cfg, k, params);
+}
+
+cudaError_t ffn_chain_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_optin, int n_sms,
+                           int* n_stages, int* grid) {
+  const int nproj = gated ? 3 : 2;
+  int ns = 16;  // one CTA per SM with as many ring slots as fit
+  while (ns > 2 && chain_smem_bytes(D, dtype_bytes, nproj, ns) > smem_optin) --ns;
+  const size_t smem = chain_smem_bytes(D, dtype_bytes, nproj, ns);
+  if (smem > smem_optin) return cudaErrorInvalidValue;
+  void* k = pick_chain_kernel(dtype, gated != 0, D, dtype_bytes);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kChainBlock, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  *n_stages = ns;
+  *grid = n_sms;  // every CTA co-resident (cooperative launch)
+  return cudaSuccess;
+}
+
+cudaError_t launch_ffn_chain(const FfnChainLaunch& a, cudaStream_t st) {
+  void* k = pick_chain_kernel(a.dtype, a.gated != 0, a.D, a.dtype_bytes);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid, 1, 1);
+  cfg.blockDim = dim3(kChainBlock, 1, 1);
+  cfg.dynamicSmemBytes = chain_smem_bytes(a.D, a.dtype_bytes, a.gated ? 3 : 2, a.n_stages);
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeCooperative;
+  attr.val.cooperative = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  FfnChainLaunch arg = a;
   void* params[] = {&arg};
   return cudaLaunchKernelExC(&cfg, k, params);
 }

@@ -43,6 +43,27 @@ size_t ffn_smem_bytes(int D, int dtype_bytes, int nproj, int n_stages);
 cudaError_t ffn_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_per_sm, int n_sms, int* n_stages,
                      int* grid);
 int ffn_max_chunks();        // 16-byte chunks per row the FFN supports
+// Persistent FFN over consecutive layers first..first+count-1 (batch 1),
+// launched cooperatively: one CTA per SM, two arrival counters per layer
+// (partials stored; y slices summed).  The split-K order is fixed.
+struct FfnChainLaunch {
+  const void* dense_w;       // [n_dense][n_proj][F][D]
+  const void* bufs;          // [S][n_proj][K][D] resident rows
+  const int* active_slot;    // [S][K]
+  const int* counts;         // [S][4] (|A| first)
+  int n_dense, F, K;
+  int first, count;
+  float* h;                  // [D] residual stream, in and out
+  float* hbase;              // [2][D] residual bases
+  float* yacc;               // [3][D] layer outputs y
+  float* part;               // [grid][D] per-CTA partial y
+  unsigned* arrive;          // [2 count] arrival counters, zero beforehand
+  int D, dtype, dtype_bytes, gated, n_stages, grid;
+  int* err;
+};
+cudaError_t ffn_chain_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_optin, int n_sms,
+                           int* n_stages, int* grid);
+cudaError_t launch_ffn_chain(const FfnChainLaunch& a, cudaStream_t st);
 // Allow the dynamic shared memory of an n_stages ring (after changing it).
 cudaError_t ffn_set_smem(int dtype, int gated, int D, int dtype_bytes, int n_stages);
 cudaError_t launch_ffn_rows(const FfnLaunch& a, cudaStream_t st);
