@@ -36,8 +36,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # source file still has the recorded hash.
 NCU_TRAFFIC = {
     ("gather", "llama2-7b-relu"): {"src": "np_scatter.cu", "src_hash": "785fcdae10bbda3b", "bytes_per_launch": 7552},
-    ("ffn", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "dec4aff414fd38f9", "bytes_per_launch": 50400896},
-    ("dense", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "dec4aff414fd38f9", "bytes_per_launch": 273935360},
+    ("ffn", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "650a8e3351bf67ce", "bytes_per_launch": 50405632},
+    ("dense", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "650a8e3351bf67ce", "bytes_per_launch": 273324544},
+    # one persistent launch over the 31 sparse layers, per layer
+    ("ffn_chain", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "650a8e3351bf67ce",
+                                      "bytes_per_launch": 50470896},
+    ("ffn", "llama2-7b-batch8"): {"src": "np_mma.cu", "src_hash": "a6395d2f54e8c479", "bytes_per_launch": 85350656},
+    ("dense", "llama2-7b-batch8"): {"src": "np_mma.cu", "src_hash": "a6395d2f54e8c479", "bytes_per_launch": 281533696},
 }
 SRC_DIR = os.path.join(ROOT, "sparse_activation_decode_gb300", "csrc")
 
@@ -237,7 +242,8 @@ def isolated_kernels(dec, torch, cfg, reps=5):
 def profile_case(args):
     """Small capture case for ncu: 8-step workload of --config (optionally
     cut to --layers layers), 3 decoded steps, then standalone calls of every
-    kernel kind: two sparse FFNs, dense layer 0, predictor, delta, scatter."""
+    kernel kind: two sparse FFNs, dense layer 0, the chained sparse FFNs,
+    predictor, delta, scatter."""
     import torch
     from sparse_activation_decode_gb300 import decoder_for
     from sparse_activation_decode_gb300.build import build
@@ -257,6 +263,7 @@ def profile_case(args):
     dec.sparse_mlp(l1, h)
     dec.sparse_mlp(l2, h)
     dec.dense_mlp(0, h)
+    dec.ffn_layers(cfg.n_dense, cfg.n_sparse, h.clone())  # chained sparse FFNs
     ids = dec.predict(h)
     dec.delta(ids, -1)
     dec.scatter(-1)
@@ -407,7 +414,8 @@ def run_cuda(args):
         g = iso["ffn_chain"]["gbs"]
         hbm_kernels["ffn_chain"] = {"gbs": g, "us_per_layer": iso["ffn_chain"]["us_per_layer"],
                                     "frac_of_measured_hbm": round(g / peaks["hbm_gbs"], 4),
-                                    "frac_of_nominal_8tbs": round(g / 8000.0, 4)}
+                                    "frac_of_nominal_8tbs": round(g / 8000.0, 4),
+                                    "traffic_per_layer": traffic_for("ffn_chain", cfg.name)}
     if "predictor" in iso:
         g = iso["predictor"]["gbs"]
         hbm_kernels["predictor"] = {"isolated_gbs": g, "frac_of_measured_hbm": round(g / peaks["hbm_gbs"], 4),
