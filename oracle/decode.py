@@ -30,7 +30,8 @@ design notes):
 * freed slots are handed out in ascending slot order to incoming neurons in
   ascending ID order;
 * activation h_n = relu(g_n . x) * (u_n . x) (ReLU-fied Llama), or
-  relu(u_n . x) without a gate (OPT);
+  relu(u_n . x) without a gate (OPT); optionally silu(g_n . x) * (u_n . x)
+  (SwiGLU) over the same predicted rows;
 * the rest of the transformer block is replaced by a residual stream
   h <- h + y with a weightless RMSNorm (eps 1e-6) in front of every FFN and of
   the predictor;
@@ -72,8 +73,15 @@ def rmsnorm(h: np.ndarray) -> np.ndarray:
     return h / np.sqrt(np.mean(h * h) + RMS_EPS)
 
 
+def silu(a: np.ndarray) -> np.ndarray:
+    """silu(a) = a * sigmoid(a) = a / (1 + exp(-a)) (the SwiGLU gate)."""
+    a = np.asarray(a, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return a / (1.0 + np.exp(-a))
+
+
 def ffn_rows(gate: np.ndarray | None, up: np.ndarray, down_t: np.ndarray,
-             xhat: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+             xhat: np.ndarray, activation: str = "relu") -> tuple[np.ndarray, np.ndarray]:
     """FFN over an explicit list of neurons.
 
     gate, up, down_t: [n, D] rows (row n of the gate, up and down^T
@@ -81,6 +89,10 @@ def ffn_rows(gate: np.ndarray | None, up: np.ndarray, down_t: np.ndarray,
     each active neuron i, the runtime uses row i of the gate, up, and down^T
     projections").  Returns (y[D], h[n]) with
         h_n = relu(gate_n . x) * (up_n . x)   (ReLU-fied Llama)
+        h_n = silu(gate_n . x) * (up_n . x)   (activation "swiglu": the
+                                               SwiGLU MLP of the pages'
+                                               models, NeuroPrefetcher
+                                               "Predictive Delta Prefetching")
         h_n = relu(up_n . x)                   (no gate: OPT)
         y   = sum_n h_n * down_t_n.
     """
@@ -89,7 +101,8 @@ def ffn_rows(gate: np.ndarray | None, up: np.ndarray, down_t: np.ndarray,
         hn = np.maximum(b, 0.0)
     else:
         a = gate @ xhat
-        hn = np.where(a > 0.0, a, 0.0) * b
+        g = silu(a) if activation == "swiglu" else np.where(a > 0.0, a, 0.0)
+        hn = g * b
     y = down_t.T @ hn
     return y, hn
 
@@ -296,7 +309,7 @@ class OracleDecoder:
             rec.h_in_dense.append(h.copy())
             yd = np.zeros((B, cfg.d_model))
             for b in range(B):
-                yd[b], _ = ffn_rows(g, u, dt, rmsnorm(h[b]))
+                yd[b], _ = ffn_rows(g, u, dt, rmsnorm(h[b]), cfg.activation)
                 h[b] += yd[b]
             rec.y_dense.append(yd)
             if layer == 0:
@@ -345,7 +358,7 @@ class OracleDecoder:
             rec.h_in.append(h.copy())
             ys = np.zeros((B, cfg.d_model))
             for b in range(B):
-                ys[b], _ = ffn_rows(g, u, dt, rmsnorm(h[b]))
+                ys[b], _ = ffn_rows(g, u, dt, rmsnorm(h[b]), cfg.activation)
                 h[b] += ys[b]
             rec.y.append(ys)
         rec.h = h

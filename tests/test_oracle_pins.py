@@ -457,3 +457,26 @@ def test_batched_ffn_equals_dense_masked_ffn_per_sequence():
     assert rec2.active == rec.active
     for s in range(cfg.n_sparse):
         assert np.array_equal(rec2.y[s], rec.y[s][perm])
+
+
+def test_swiglu_hand_worked_and_against_scipy():
+    # silu(a) = a * sigmoid(a): hand-worked values and scipy's logistic
+    # function (an independent implementation of sigmoid)
+    from scipy.special import expit
+    a = np.array([-30.0, -2.0, -0.5, 0.0, 0.5, 2.0, 30.0])
+    assert np.allclose(oracle.silu(a), a * expit(a), rtol=1e-14, atol=0)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+    assert abs(oracle.silu(np.array([1.0]))[0] - 1.0 / (1.0 + np.exp(-1.0))) < 1e-15
+    # one neuron, D = 2: g.x = 1, u.x = 3 -> h = silu(1) * 3, y = h * d
+    g = np.array([[1.0, 0.0]])
+    u = np.array([[1.0, 2.0]])
+    d = np.array([[2.0, -1.0]])
+    x = np.array([1.0, 1.0])
+    y, h = oracle.ffn_rows(g, u, d, x, "swiglu")
+    want = (1.0 / (1.0 + np.exp(-1.0))) * 3.0
+    assert abs(h[0] - want) < 1e-15
+    assert np.allclose(y, want * d[0], rtol=1e-15)
+    # a negative gate does not zero the neuron under SwiGLU (it does under ReLU)
+    y2, h2 = oracle.ffn_rows(-g, u, d, x, "swiglu")
+    _, h3 = oracle.ffn_rows(-g, u, d, x, "relu")
+    assert h2[0] < 0.0 and h3[0] == 0.0

@@ -60,6 +60,7 @@ class Config:
     pred_hidden: int = 512   # predictor hidden width
     pred_kind: str = "shared_argmax"  # or 'perlayer_sigmoid'
     has_gate: bool = True    # False: OPT-style records (up | down^T)
+    activation: str = "relu"  # gated FFN: 'relu' (ReLU-fied) or 'swiglu' (silu gate)
     combine: str = "union"   # 'union' | 'intersect' of the gate and up masks
     residency: str = "slotmap"  # 'slotmap' | 'window'
     window: int = 5          # W tokens (window residency)
