@@ -81,6 +81,12 @@ typedef int32_t np_status;
 #define NP_H2D_STAGED 0
 #define NP_H2D_FUSED 1
 
+/* activation of a gated FFN: relu(g.x) * (u.x) (ReLU-fied), or
+ * silu(g.x) * (u.x) (SwiGLU, NeuroPrefetcher "Predictive Delta Prefetching")
+ * over the same predicted rows.  Models without a gate use relu(u.x). */
+#define NP_ACT_RELU 0
+#define NP_ACT_SWIGLU 1
+
 /* Optional storage read hook, called on the host once per sparse layer before
  * that layer's records are read, with the layer index (absolute) and the
  * token counter.  A non-zero return makes the read fail with NP_ERR_IO. */
@@ -107,6 +113,7 @@ typedef struct {
   int32_t pred_hidden;  /* H: predictor hidden width */
   int32_t pred_kind;    /* NP_PRED_* */
   int32_t h2d_mode;     /* NP_H2D_* */
+  int32_t activation;   /* NP_ACT_* (NP_ACT_SWIGLU needs has_gate = 1) */
   /* Host weight store (caller-owned, CPU memory the device can read; e.g.
    * registered with np_host_register).  Layout: record-major per sparse
    * layer, [L-d][F][n_proj][D] elements of `dtype`, n_proj = 3 (gate, up,

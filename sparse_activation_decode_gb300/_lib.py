@@ -26,7 +26,7 @@ class ModelDesc(ctypes.Structure):
         ("dtype", ctypes.c_int32), ("has_gate", ctypes.c_int32), ("combine", ctypes.c_int32),
         ("residency", ctypes.c_int32), ("window", ctypes.c_int32), ("batch", ctypes.c_int32),
         ("staging_rows", ctypes.c_int32), ("pred_hidden", ctypes.c_int32), ("pred_kind", ctypes.c_int32),
-        ("h2d_mode", ctypes.c_int32),
+        ("h2d_mode", ctypes.c_int32), ("activation", ctypes.c_int32),
         ("host_store", ctypes.c_void_p), ("dense_w", ctypes.c_void_p), ("pred_w1", ctypes.c_void_p),
         ("pred_w2", ctypes.c_void_p), ("pred_b2", ctypes.c_void_p), ("centroids", ctypes.c_void_p),
         ("main_stream", ctypes.c_void_p), ("side_stream", ctypes.c_void_p),

@@ -233,6 +233,7 @@ np_status enqueue_ffn(np_model* m, cudaStream_t st, int kind, const unsigned cha
   a.dtype = m->d.dtype;
   a.dtype_bytes = m->esz;
   a.gated = m->d.has_gate;
+  a.swiglu = m->d.activation == NP_ACT_SWIGLU;
   a.n_stages = m->ffn_stages;
   a.grid = m->ffn_grid;
   a.err = m->err;
@@ -271,6 +272,7 @@ float* chain_y(np_model* m, int i) { return m->yacc + (size_t)(i % 3) * m->B * m
 np_status enqueue_mma(np_model* m, cudaStream_t st, int kind, int mode, const RowMaps& map, const MmaPlan& p,
                       MmaArgs& a, int64_t fixed_bytes) {
   a.B = m->B;
+  a.swiglu = m->d.activation == NP_ACT_SWIGLU;
   a.err = m->err;
   const int bf16 = m->d.dtype == NP_BF16;
   return launch(m, kind, st, fixed_bytes, [&] { return launch_mma_rows(mode, bf16, map, a, p, st); });
@@ -671,6 +673,8 @@ static np_status validate(const np_model_desc* d) {
   }
   if (d->staging_rows < 0 || d->staging_rows > d->k_max) return arg_fail("staging_rows must be in [0, k_max]");
   if (d->h2d_mode != NP_H2D_STAGED && d->h2d_mode != NP_H2D_FUSED) return arg_fail("bad h2d_mode");
+  if (d->activation != NP_ACT_RELU && d->activation != NP_ACT_SWIGLU) return arg_fail("bad activation");
+  if (d->activation == NP_ACT_SWIGLU && !d->has_gate) return arg_fail("SwiGLU needs a gate projection");
   if (d->pred_hidden < 1 || (d->pred_hidden * esz) % 16 != 0 ||
       d->pred_hidden / (16 / esz) > kThreads * kMaxChunksPerThread)
     return arg_fail("pred_hidden must be positive, rows a multiple of 16 bytes, <= 8192");
@@ -1070,6 +1074,7 @@ np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev)
     a.dtype = m->d.dtype;
     a.dtype_bytes = m->esz;
     a.gated = m->d.has_gate;
+    a.swiglu = m->d.activation == NP_ACT_SWIGLU;
     a.n_stages = m->chain_stages;
     a.grid = m->chain_grid;
     a.err = m->err;

@@ -2,7 +2,8 @@
 //
 // For each listed row r (a slot of a sparse layer's resident buffers, or a
 // neuron of a dense layer):
-//     h_r = relu(g_r . x) * (u_r . x)      (or relu(u_r . x) without a gate)
+//     h_r = relu(g_r . x) * (u_r . x)      (or relu(u_r . x) without a gate,
+//                                          or silu(g_r . x) * (u_r . x): SwiGLU)
 //     y  += h_r * d_r
 // with x = rmsnorm(h), h = h_base + y_prev (NeuroPrefetcher full text, delta
 // runtime: row i of the gate, up and down^T projections serves active neuron
@@ -104,6 +105,9 @@ template <int NT> __device__ __forceinline__ bool consumer_sync_or(bool pred) {
   return r != 0;
 }
 
+// silu(v) = v * sigmoid(v), the SwiGLU gate
+__device__ __forceinline__ float silu(float v) { return v / (1.f + expf(-v)); }
+
 __device__ __forceinline__ void grid_dependents_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -171,7 +175,7 @@ __device__ __forceinline__ void load_x(const float* __restrict__ h_in, const flo
 template <typename T, bool GATED, int MAXC, int NT, int GR>
 __device__ __forceinline__ bool consume_group(const uint4* __restrict__ sm4, const int (&off)[GR], int nrow, bool ok,
                                               int grp, int NC, const float2 (&xr)[MAXC][Pairs<T>::N],
-                                              float2 (&acc)[MAXC][Pairs<T>::N], float* red) {
+                                              float2 (&acc)[MAXC][Pairs<T>::N], float* red, bool swiglu) {
   constexpr int P = Pairs<T>::N;
   constexpr int NPROJ = GATED ? 3 : 2;
   constexpr int NV = (GATED ? 2 : 1) * GR;  // dot products per group
@@ -246,7 +250,7 @@ __device__ __forceinline__ bool consume_group(const uint4* __restrict__ sm4, con
     if (GATED) {
       const float g = __shfl_sync(0xffffffffu, tot, 2 * r);
       const float u = __shfl_sync(0xffffffffu, tot, 2 * r + 1);
-      hv[r] = (g > 0.f ? g : 0.f) * u;
+      hv[r] = (swiglu ? silu(g) : (g > 0.f ? g : 0.f)) * u;
     } else {
       const float u = __shfl_sync(0xffffffffu, tot, r);
       hv[r] = u > 0.f ? u : 0.f;
@@ -281,7 +285,7 @@ template <typename T, bool GATED, int MAXC, int NT, int GR>
 __device__ __forceinline__ bool consume_group_early(const uint4* __restrict__ sm4, const int (&off)[GR],
                                                     const int (&slot)[GR], uint64_t* empty, int nrow, bool ok,
                                                     int grp, int NC, const float2 (&xr)[MAXC][Pairs<T>::N],
-                                                    float2 (&acc)[MAXC][Pairs<T>::N], float* red) {
+                                                    float2 (&acc)[MAXC][Pairs<T>::N], float* red, bool swiglu) {
   constexpr int P = Pairs<T>::N;
   constexpr int NPROJ = GATED ? 3 : 2;
   constexpr int NV = (GATED ? 2 : 1) * GR;
@@ -360,7 +364,7 @@ __device__ __forceinline__ bool consume_group_early(const uint4* __restrict__ sm
     if (GATED) {
       const float g = __shfl_sync(0xffffffffu, tot, 2 * r);
       const float u = __shfl_sync(0xffffffffu, tot, 2 * r + 1);
-      hv = (g > 0.f ? g : 0.f) * u;
+      hv = (swiglu ? silu(g) : (g > 0.f ? g : 0.f)) * u;
     } else {
       const float u = __shfl_sync(0xffffffffu, tot, r);
       hv = u > 0.f ? u : 0.f;
@@ -496,7 +500,7 @@ __global__ void __launch_bounds__(kFfnBlock, 2) ffn_rows_kernel(FfnLaunch a) {
       }
       const int off[2] = {(int)((512 + (size_t)s0 * slot_bytes) >> 4), (int)((512 + (size_t)s1 * slot_bytes) >> 4)};
       if (!consume_group<T, GATED, MAXC, kFfnThreads, 2>(reinterpret_cast<const uint4*>(smem), off, two ? 2 : 1, ok,
-                                                          j >> 1, NC, xr, acc, red)) {
+                                                          j >> 1, NC, xr, acc, red, a.swiglu != 0)) {
         if (tid == 0) s_abort = 1;
         break;
       }
@@ -708,7 +712,7 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
         }
         if (!consume_group_early<T, GATED, MAXC, kChainThreads, kChainGroup>(
                 reinterpret_cast<const uint4*>(smem), off, slot, empty, nrow, ok, jj / kChainGroup, NC, xr, acc,
-                red)) {
+                red, a.swiglu != 0)) {
           aborted = true;
           break;
         }

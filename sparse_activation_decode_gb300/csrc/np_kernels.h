@@ -34,6 +34,7 @@ struct FfnLaunch {
   int dtype;              // 0 f32, 1 f16, 2 bf16
   int dtype_bytes;
   int gated;
+  int swiglu;             // gated: silu(g.x) instead of relu(g.x)
   int n_stages;
   int grid;
   int* err;
@@ -58,7 +59,7 @@ struct FfnChainLaunch {
   float* yacc;               // [3][D] layer outputs y
   float* part;               // [grid][D] per-CTA partial y
   unsigned* arrive;          // [2 count] arrival counters, zero beforehand
-  int D, dtype, dtype_bytes, gated, n_stages, grid;
+  int D, dtype, dtype_bytes, gated, swiglu, n_stages, grid;
   int* err;
 };
 cudaError_t ffn_chain_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_optin, int n_sms,
@@ -190,6 +191,7 @@ struct MmaArgs {
   int n_heads, C;
   unsigned long long* keys_zero;  // hidden: cleared before the heads run
   int n_keys_zero;
+  int swiglu;               // gated FFN: silu(g.x) instead of relu(g.x)
   int n_stages;
   uint32_t stage_bytes;
   int* err;

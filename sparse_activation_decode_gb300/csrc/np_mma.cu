@@ -185,6 +185,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
     // ---------------- producer: tensor-map gathers into the ring ----------------
     const uint64_t pol = policy_evict_first();
     uint32_t it = 0;
+    int ps = 0;          // ring slot of copy `it`
+    uint32_t pph = 0;    // its pass parity
     bool ok = true;
     for (int tile = 0; tile < n_tiles && ok; ++tile) {
       const int t0 = r_begin + tile * kTileRows;
@@ -195,10 +197,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
       const int nb_gu = n32 + ((((nr + 7) & ~7) - 32 * n32) >> 3);
       const int rows_gu = 32 * n32 + 8 * (nb_gu - n32);
       for (int kb = 0; kb < n_kb && ok; ++kb) {
-        const int s = (int)(it % (uint32_t)NS);
+        const int s = ps;
         int w = 1;
         if (lane == 0) {
-          w = wait_phase(bar(kBarEmpty + s), ((it / NS) & 1u) ^ 1u, abort, a.err);
+          w = wait_phase(bar(kBarEmpty + s), pph ^ 1u, abort, a.err);
           if (w) mbar_arrive_expect_tx_a(bar(kBarFull + s), (uint32_t)(kProj * rows_gu * 128));
         }
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
@@ -213,15 +215,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
                       bar(kBarFull + s), pol);
         }
         ++it;
+        if (++ps == NS) {
+          ps = 0;
+          pph ^= 1u;
+        }
       }
       if (kFfn) {
         const int nb_dt = n32 + ((((nr + 15) & ~15) - 32 * n32) >> 3);
         const int rows_dt = 32 * n32 + 8 * (nb_dt - n32);
         for (int mt = 0; mt < n_mt && ok; ++mt) {
-          const int s = (int)(it % (uint32_t)NS);
+          const int s = ps;
           int w = 1;
           if (lane == 0) {
-            w = wait_phase(bar(kBarEmpty + s), ((it / NS) & 1u) ^ 1u, abort, a.err);
+            w = wait_phase(bar(kBarEmpty + s), pph ^ 1u, abort, a.err);
             if (w) mbar_arrive_expect_tx_a(bar(kBarFull + s), (uint32_t)(2 * rows_dt * 128));
           }
           ok = __shfl_sync(0xffffffffu, w, 0) != 0;
@@ -234,6 +240,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
                         slice0 + mt * 128 + grp * 64, a.row_base2 + t0 + r, bar(kBarFull + s), pol);
           }
           ++it;
+          if (++ps == NS) {
+            ps = 0;
+            pph ^= 1u;
+          }
         }
       }
     }
@@ -249,6 +259,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
       fence_proxy_async_cta();
       tc_fence_after();
       uint32_t it = 0;
+      int ms = 0;          // ring slot of copy `it`
+      uint32_t mph = 0;    // its pass parity
       for (int tile = 0; tile < n_tiles && ok; ++tile) {
         const int nr = min(kTileRows, r_end - (r_begin + tile * kTileRows));
         if (tile > 0) {
@@ -256,8 +268,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
           tc_fence_after();
         }
         for (int kb = 0; kb < n_kb && ok; ++kb) {
-          const int s = (int)(it % (uint32_t)NS);
-          ok = wait_phase(bar(kBarFull + s), (it / NS) & 1u, abort, a.err);
+          const int s = ms;
+          ok = wait_phase(bar(kBarFull + s), mph, abort, a.err);
           if (!ok) break;
           tc_fence_after();
           const uint32_t st_a = ring_a + (uint32_t)s * stage_bytes;
@@ -272,6 +284,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
           }
           tc_commit(bar(kBarEmpty + s));
           ++it;
+          if (++ms == NS) {
+            ms = 0;
+            mph ^= 1u;
+          }
         }
         if (!ok) break;
         tc_commit(bar(kBarAccFull));
@@ -282,8 +298,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
           tc_fence_after();
           const int nks = (nr + 15) >> 4;
           for (int mt = 0; mt < n_mt && ok; ++mt) {
-            const int s = (int)(it % (uint32_t)NS);
-            ok = wait_phase(bar(kBarFull + s), (it / NS) & 1u, abort, a.err);
+            const int s = ms;
+            ok = wait_phase(bar(kBarFull + s), mph, abort, a.err);
             if (!ok) break;
             tc_fence_after();
             const uint32_t st_a = ring_a + (uint32_t)s * stage_bytes;
@@ -295,6 +311,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
             }
             tc_commit(bar(kBarEmpty + s));
             ++it;
+            if (++ms == NS) {
+              ms = 0;
+              mph ^= 1u;
+            }
           }
         }
       }
@@ -484,7 +504,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           float hv = 0.f;
-          if (valid && j < B) hv = kGated ? fmaxf(av[j], 0.f) * bv[j] : fmaxf(av[j], 0.f);
+          if (valid && j < B)
+            hv = kGated ? (a.swiglu ? av[j] / (1.f + expf(-av[j])) : fmaxf(av[j], 0.f)) * bv[j] : fmaxf(av[j], 0.f);
           split16<BF16>(hv, v16[j], v16[8 + j]);
         }
         // write this row's 16 operand values into the local buffer, then copy

@@ -44,7 +44,7 @@ class SparseDecoder:
                  dense_w: torch.Tensor | None = None, centroids: torch.Tensor | None = None,
                  pred_hidden: int, pred_kind: str = "shared_argmax", has_gate: bool = True,
                  combine: str = "union", residency: str = "slotmap", window: int = 1, batch: int = 1,
-                 staging_rows: int = 0, h2d_mode: str = "fused",
+                 staging_rows: int = 0, h2d_mode: str = "fused", activation: str = "relu",
                  main_stream: torch.cuda.Stream | None = None, side_stream: torch.cuda.Stream | None = None,
                  read_hook=None):
         self.lib = L.load()
@@ -71,6 +71,7 @@ class SparseDecoder:
         d.combine = {"intersect": L.NP_COMBINE_INTERSECT, "union": L.NP_COMBINE_UNION}[combine]
         d.residency = {"slotmap": L.NP_RES_SLOTMAP, "window": L.NP_RES_WINDOW}[residency]
         d.window, d.batch, d.staging_rows, d.pred_hidden = window, batch, staging_rows, pred_hidden
+        d.activation = {"relu": 0, "swiglu": 1}[activation]
         d.pred_kind = {"shared_argmax": L.NP_PRED_SHARED_ARGMAX,
                        "perlayer_sigmoid": L.NP_PRED_PERLAYER_SIGMOID}[pred_kind]
         d.h2d_mode = {"staged": L.NP_H2D_STAGED, "fused": L.NP_H2D_FUSED}[h2d_mode]
@@ -271,6 +272,7 @@ def decoder_for(wl, *, h2d_mode: str = "fused", staging_rows: int | None = None,
         pred_kind=cfg.pred_kind, has_gate=cfg.has_gate, combine=cfg.combine, residency=cfg.residency,
         window=cfg.window if cfg.residency == "window" else 1, batch=cfg.batch,
         staging_rows=cfg.staging_rows if staging_rows is None else staging_rows, h2d_mode=h2d_mode,
+        activation=cfg.activation,
         read_hook=read_hook, **kw)
 
 

@@ -36,6 +36,9 @@ SMALL_CASES = {
     "small-batched-fused": (SMALL_BATCHED, {"h2d_mode": "fused"}),
     "small-batched-b3-f16": (SMALL_BATCHED.replace(batch=3, dtype="f16", k_max=700), {}),
     "small-batched-nogate": (SMALL_BATCHED.replace(has_gate=False), {}),
+    # SwiGLU activation (silu gate) on the CUDA-core and tensor-core FFNs
+    "small-f16-swiglu": (SMALL_F16.replace(activation="swiglu"), {}),
+    "small-batched-swiglu": (SMALL_BATCHED.replace(activation="swiglu"), {}),
 }
 
 
@@ -156,7 +159,8 @@ def test_state_machine_errors():
     dec.close()
 
 
-@pytest.mark.parametrize("bad", [{"k_max": 5000}, {"d_model": 12}, {"n_dense": 0}])
+@pytest.mark.parametrize("bad", [{"k_max": 5000}, {"d_model": 12}, {"n_dense": 0},
+                                 {"activation": "swiglu", "has_gate": False}])
 def test_invalid_config_rejected(bad):
     from sparse_activation_decode_gb300 import NpError
     cfg = SMALL_F16
@@ -220,7 +224,8 @@ def test_full_size_sampled(cfg, tokens):
     assert summ["max_h_rel"] < FFN_TOL
 
 
-@pytest.mark.parametrize("cfg", [SMALL_F16, SMALL_BATCHED], ids=["small-f16", "small-batched"])
+@pytest.mark.parametrize("cfg", [SMALL_F16, SMALL_BATCHED, SMALL_F16.replace(activation="swiglu")],
+                         ids=["small-f16", "small-batched", "small-f16-swiglu"])
 def test_ffn_layers_equals_layer_by_layer(cfg):
     # the chained FFN entry point equals h += FFN_l(h) applied layer by layer
     # through the standalone entry points, over dense and sparse layers
