@@ -195,6 +195,50 @@ def assign_slots(slotmap: np.ndarray, inv: np.ndarray, d_in: list[int],
     return pairs
 
 
+def assign_slots_compact(slotmap: np.ndarray, inv: np.ndarray, d_in: list[int],
+                         d_out: list[int], n_rows: int) -> tuple[list[tuple[int, int]], list[tuple[int, int]], int]:
+    """Compact placement, in place (LLM in a flash, 3.3 "Optimized Data
+    Management in DRAM": a removed neuron's row is replaced with a row from
+    the end of the occupied region; incoming rows are appended; the occupied
+    rows stay [0, num_rows)).
+
+    Reading: with n_new = num_rows - |D_out|, every removed neuron whose slot
+    lies below n_new is replaced by a surviving row from the end region
+    [n_new, num_rows), the i-th such slot in ascending order by the i-th
+    surviving end row in ascending order (one copy per slot to refill, the
+    fewest possible); removed rows in the end region just fall away.  The
+    incoming neurons, in ascending ID order, then take n_new, n_new + 1, ...
+    Returns (the (neuron, slot) pairs of D_in, the (from_slot, to_slot) row
+    moves, the new num_rows)."""
+    out_slots = set()
+    for n in d_out:
+        sl = int(slotmap[n])
+        assert 0 <= sl < n_rows
+        out_slots.add(sl)
+    n_new = n_rows - len(d_out)
+    holes = sorted(sl for sl in out_slots if sl < n_new)
+    movers = sorted(sl for sl in range(n_new, n_rows) if sl not in out_slots)
+    assert len(holes) == len(movers)
+    for n in d_out:
+        sl = int(slotmap[n])
+        slotmap[n] = -1
+        inv[sl] = -1
+    moves = list(zip(movers, holes))
+    for src, dst in moves:
+        n = int(inv[src])
+        slotmap[n] = dst
+        inv[dst] = n
+        inv[src] = -1
+    pairs = []
+    for i, n in enumerate(d_in):
+        sl = n_new + i
+        assert sl < len(inv), "resident set larger than K_max"
+        slotmap[n] = sl
+        inv[sl] = n
+        pairs.append((n, sl))
+    return pairs, moves, n_new + len(d_in)
+
+
 def window_resident(resident_prev: list[int], active: list[int], last_seen: dict,
                     t: int, window: int, k_max: int) -> list[int]:
     """Resident set after token t under windowing: the neurons active in the
@@ -227,6 +271,7 @@ class TokenRecord:
     overflow: list = field(default_factory=list)    # per layer: dropped by the cap
     d_in: list = field(default_factory=list)        # per layer: [(neuron, slot)]
     d_out: list = field(default_factory=list)       # per layer: sorted IDs
+    moves: list = field(default_factory=list)       # per layer: [(from_slot, to_slot)] (compact)
     y: list = field(default_factory=list)           # per layer: [B][D] fp64
     h_in: list = field(default_factory=list)        # per layer: [B][D] input
     y_dense: list = field(default_factory=list)     # per dense layer: [B][D]
@@ -245,6 +290,7 @@ class OracleDecoder:
         S, F, K, D = cfg.n_sparse, cfg.d_ff, cfg.k_max, cfg.d_model
         self.slotmap = np.full((S, F), -1, dtype=np.int64)
         self.inv = np.full((S, K), -1, dtype=np.int64)
+        self.n_rows = [0] * S          # occupied rows under compact placement
         self.resident = [[] for _ in range(S)]
         self.last_seen = [dict() for _ in range(S)]
         self.t = 0
@@ -342,14 +388,23 @@ class OracleDecoder:
             else:
                 nxt = active
             d_in, d_out = set_delta(active, prev, nxt)
-            pairs = assign_slots(self.slotmap[s], self.inv[s], d_in, d_out, cfg.k_max)
+            moves = []
+            if cfg.slots == "compact":
+                pairs, moves, self.n_rows[s] = assign_slots_compact(
+                    self.slotmap[s], self.inv[s], d_in, d_out, self.n_rows[s])
+            else:
+                pairs = assign_slots(self.slotmap[s], self.inv[s], d_in, d_out, cfg.k_max)
             self.resident[s] = nxt
             rec.d_in.append(pairs)
             rec.d_out.append(d_out)
-            # Scatter: each staged record's rows go to the slot the delta
-            # runtime assigned (NeuroPrefetcher "I/O Path",
-            # launch_deinterleave_scatter).
+            rec.moves.append(moves)
+            # Compact placement first moves the kept rows into the freed
+            # slots, then the incoming rows are written.  Scatter: each staged
+            # record's rows go to the slot the delta runtime assigned
+            # (NeuroPrefetcher "I/O Path", launch_deinterleave_scatter).
             if self.materialize:
+                for src, dst in moves:
+                    self.bufs[s, :, dst] = self.bufs[s, :, src]
                 for n, slot in pairs:
                     for p in range(cfg.n_proj):
                         self.bufs[s, p, slot] = wl.store[s, n, p]

@@ -480,3 +480,78 @@ def test_swiglu_hand_worked_and_against_scipy():
     y2, h2 = oracle.ffn_rows(-g, u, d, x, "swiglu")
     _, h3 = oracle.ffn_rows(-g, u, d, x, "relu")
     assert h2[0] < 0.0 and h3[0] == 0.0
+
+
+def test_compact_placement_brute_force():
+    # random resident sets, checked against a model of the buffer: the
+    # occupied slots stay exactly [0, |R|), every resident neuron's row sits at
+    # its slot, maps stay consistent, moves only fill freed slots below the
+    # new count from the end region (one copy each: as few as possible, and
+    # never more than the number removed), and appends follow in ID order
+    rng = random.Random(11)
+    F = 60
+    for trial in range(300):
+        K = rng.randint(1, 40)
+        slotmap = np.full(F, -1, dtype=np.int64)
+        inv = np.full(K, -1, dtype=np.int64)
+        content = {}
+        resident = []
+        n_rows = 0
+        for step in range(6):
+            nxt = sorted(rng.sample(range(F), rng.randint(0, K)))
+            d_in, d_out = oracle.set_delta(nxt, resident, nxt)
+            old_slot = {n: int(slotmap[n]) for n in resident}
+            n_new = n_rows - len(d_out)
+            must_fill = sorted(old_slot[n] for n in d_out if old_slot[n] < n_new)
+            pairs, moves, n2 = oracle.assign_slots_compact(slotmap, inv, d_in, d_out, n_rows)
+            assert len(moves) == len(must_fill) <= len(d_out)
+            assert sorted(dst for _, dst in moves) == must_fill
+            assert all(src >= n_new for src, _ in moves)
+            for src, dst in moves:
+                assert content[src] not in d_out
+                content[dst] = content[src]
+            for n, sl in pairs:
+                content[sl] = n
+            assert [n for n, _ in pairs] == d_in and [sl for _, sl in pairs] == list(range(n_new, n2))
+            assert n2 == len(nxt)
+            assert sorted(int(x) for x in inv[:n2]) == nxt and all(inv[n2:] == -1)
+            for n in nxt:
+                assert inv[slotmap[n]] == n and content[int(slotmap[n])] == n
+            resident, n_rows = nxt, n2
+
+
+def test_compact_decode_keeps_rows_contiguous_and_ffn_unchanged():
+    # the compact placement moves rows but not results: y equals the slot-reuse
+    # decode; buffers hold each resident neuron's record at its slot
+    base = SMALL_F16
+    wl_a = make_workload(base)
+    wl_b = make_workload(base.replace(slots="compact"))
+    da, db = OracleDecoder(wl_a), OracleDecoder(wl_b)
+    for t in range(5):
+        ra = da.step(wl_a.x[t].numpy())
+        rb = db.step(wl_b.x[t].numpy())
+        assert ra.active == rb.active
+        for s in range(base.n_sparse):
+            assert np.allclose(ra.y[s], rb.y[s], rtol=1e-12, atol=1e-15)
+            n = len(rb.active[s])
+            assert sorted(int(v) for v in db.inv[s][:n]) == rb.active[s]
+            assert all(db.inv[s][n:] == -1)
+            for nn in rb.active[s]:
+                sl = int(db.slotmap[s][nn])
+                assert torch.equal(db.bufs[s, :, sl], wl_b.store[s, nn])
+
+
+def test_compact_hand_worked():
+    # five resident rows a..e at slots 0..4 (neurons 10..14); 10 and 12 leave,
+    # 20 arrives: the two kept end rows (13 at 3, 14 at 4) fill slots 0 and 2,
+    # 20 is appended at 3, and the region is [0, 4)
+    slotmap = np.full(32, -1, dtype=np.int64)
+    inv = np.full(8, -1, dtype=np.int64)
+    for i, n in enumerate([10, 11, 12, 13, 14]):
+        slotmap[n], inv[i] = i, n
+    pairs, moves, n2 = oracle.assign_slots_compact(slotmap, inv, [20], [10, 12], 5)
+    assert moves == [(3, 0), (4, 2)] and pairs == [(20, 3)] and n2 == 4
+    assert list(inv[:5]) == [13, 11, 14, 20, -1]
+    # a removed row already in the end region needs no copy
+    pairs, moves, n2 = oracle.assign_slots_compact(slotmap, inv, [], [20, 11], 4)
+    assert moves == [(2, 1)] and n2 == 2 and list(inv[:3]) == [13, 14, -1]

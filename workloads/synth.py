@@ -64,6 +64,7 @@ class Config:
     combine: str = "union"   # 'union' | 'intersect' of the gate and up masks
     residency: str = "slotmap"  # 'slotmap' | 'window'
     window: int = 5          # W tokens (window residency)
+    slots: str = "reuse"     # 'reuse' free slots, or 'compact' (swap-with-last + append)
     batch: int = 1           # sequences decoded together
     weight_std: float = 0.02
     pred_std: float = 0.02
