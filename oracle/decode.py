@@ -408,8 +408,11 @@ class OracleDecoder:
                 for n, slot in pairs:
                     for p in range(cfg.n_proj):
                         self.bufs[s, p, slot] = wl.store[s, n, p]
-            # Sparse FFN over the resident active rows.
-            g, u, dt = self._sparse_rows(s, active)
+            # Sparse FFN over the resident active rows; the compact placement
+            # computes over its whole occupied region (LLM in a flash 3.3: the
+            # inference views are the first num_rows rows), which is the
+            # active set unless windowing keeps recently used rows as well.
+            g, u, dt = self._sparse_rows(s, nxt if cfg.slots == "compact" else active)
             rec.h_in.append(h.copy())
             ys = np.zeros((B, cfg.d_model))
             for b in range(B):

@@ -555,3 +555,30 @@ def test_compact_hand_worked():
     # a removed row already in the end region needs no copy
     pairs, moves, n2 = oracle.assign_slots_compact(slotmap, inv, [], [20, 11], 4)
     assert moves == [(2, 1)] and n2 == 2 and list(inv[:3]) == [13, 14, -1]
+
+
+def test_compact_window_ffn_covers_occupied_rows():
+    # with windowing the occupied region holds R >= A; the compact FFN is the
+    # reuse FFN (over A) plus the separate contribution of each row in R \ A
+    # (the FFN is a sum over rows), and the region is R in some order
+    cfg = SMALL_OPT.replace(slots="compact")
+    wl_a, wl_b = make_workload(SMALL_OPT), make_workload(cfg)
+    da, db = OracleDecoder(wl_a, materialize_buffers=False), OracleDecoder(wl_b, materialize_buffers=False)
+    seen_extra = 0
+    for t in range(6):
+        x = wl_a.x[t].numpy()
+        ra = da.step(x)
+        fire = [np.isin(np.arange(cfg.d_ff), ra.active[s]) for s in range(cfg.n_sparse)]
+        rb = db.step(x, fire_override=fire)
+        for s in range(cfg.n_sparse):
+            R = sorted(int(v) for v in db.inv[s][:db.n_rows[s]])
+            assert R == db.resident[s] and set(rb.active[s]) <= set(R)
+            extra = sorted(set(R) - set(rb.active[s]))
+            seen_extra += len(extra)
+            xs = oracle.rmsnorm(oracle.f64(rb.h_in[s][0]))
+            rows = oracle.f64(wl_b.store[s][extra]).transpose(1, 0, 2) if extra else None
+            y_extra = oracle.ffn_rows(None, rows[0], rows[1], xs)[0] if extra else 0.0
+            y_a = oracle.ffn_rows(None, *[oracle.f64(wl_b.store[s][rb.active[s]]).transpose(1, 0, 2)[p]
+                                          for p in range(2)], xs)[0]
+            assert np.allclose(rb.y[s][0], y_a + y_extra, rtol=1e-10, atol=1e-13)
+    assert seen_extra > 0
