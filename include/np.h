@@ -87,6 +87,19 @@ typedef int32_t np_status;
 #define NP_ACT_RELU 0
 #define NP_ACT_SWIGLU 1
 
+/* placement of resident rows in a layer's buffers: freed slots are reused
+ * in place (NeuroPrefetcher full text, delta runtime), or the rows are kept
+ * contiguous in [0, |R|) (LLM in a flash, section 3.3 "Optimized Data
+ * Management in DRAM"): with n = |R_prev| - |D_out|, each slot below n freed
+ * by D_out receives a kept row from [n, |R_prev|) (the i-th freed slot in
+ * ascending order the i-th such row in ascending order, one device-side row
+ * copy each) and D_in is appended at n, n + 1, ... in ascending ID order.
+ * Under the compact placement the sparse FFN covers the whole occupied
+ * region (that section's [:num_rows] views): the active set, plus the rows
+ * that windowing keeps. */
+#define NP_SLOTS_REUSE 0
+#define NP_SLOTS_COMPACT 1
+
 /* Optional storage read hook, called on the host once per sparse layer before
  * that layer's records are read, with the layer index (absolute) and the
  * token counter.  A non-zero return makes the read fail with NP_ERR_IO. */
@@ -114,6 +127,8 @@ typedef struct {
   int32_t pred_kind;    /* NP_PRED_* */
   int32_t h2d_mode;     /* NP_H2D_* */
   int32_t activation;   /* NP_ACT_* (NP_ACT_SWIGLU needs has_gate = 1) */
+  int32_t slots;        /* NP_SLOTS_* (batch > 1 with NP_RES_WINDOW needs
+                           NP_SLOTS_COMPACT) */
   /* Host weight store (caller-owned, CPU memory the device can read; e.g.
    * registered with np_host_register).  Layout: record-major per sparse
    * layer, [L-d][F][n_proj][D] elements of `dtype`, n_proj = 3 (gate, up,
@@ -152,6 +167,9 @@ typedef struct {
   const int32_t* dout_neuron; /* [S][K]: outgoing neuron IDs, ascending */
   const int32_t* ids;         /* shared predictor: [batch][2(L-1)] centroid IDs of the
                                  last prediction; NULL for the per-layer predictor */
+  const int32_t* move_count;  /* [S]: row moves of the compact placement (0 otherwise) */
+  const int32_t* move_src;    /* [S][K]: slot each moved row came from; NULL unless compact */
+  const int32_t* move_dst;    /* [S][K]: slot it went to (a slot freed by D_out) */
 } np_delta_view;
 
 typedef struct {
@@ -161,6 +179,7 @@ typedef struct {
   int64_t dout_rows;     /* sum of |D_out| */
   int64_t dropped_rows;  /* rows removed by the K_max cap */
   int64_t h2d_bytes;     /* din_rows * record bytes */
+  int64_t moved_rows;    /* records copied inside device memory by the compact placement */
 } np_stats;
 
 /* Create a model from `desc`; allocates device state (resident buffers
@@ -205,7 +224,8 @@ np_status np_last_delta(np_model* m, np_delta_view* out);
 /* Read the pending delta's incoming records from the host store and scatter
  * their rows into the resident buffers at the assigned slots, chunked by the
  * staging capacity (NeuroPrefetcher section 3.5, launch_deinterleave_scatter;
- * "independent submit-and-scatter chunks").  layer = -1: all pending layers;
+ * "independent submit-and-scatter chunks"); under the compact placement the
+ * delta's row moves inside the buffers run first.  layer = -1: all pending layers;
  * layer = l: that layer only.  On success the pending state is committed.
  * If the read hook fails, rows already written are restored from the store,
  * every pending delta is rolled back, and NP_ERR_IO is returned with the
@@ -213,7 +233,8 @@ np_status np_last_delta(np_model* m, np_delta_view* out);
 np_status np_scatter(np_model* m, int32_t layer);
 
 /* Sparse FFN of sparse layer `layer` over its resident active rows, read
- * through the slot map: x = rmsnorm(h) (no weight, eps 1e-6),
+ * through the slot map (the occupied rows [0, |R|) under the compact
+ * placement): x = rmsnorm(h) (no weight, eps 1e-6),
  * h_n = relu(g_n . x)(u_n . x) (or relu(u_n . x) without a gate),
  * y = sum_n h_n d_n.  h_dev, y_dev: float32 [batch][D]; y_dev may not alias
  * h_dev.  Uses the committed state. */

@@ -13,6 +13,7 @@ NP_COMBINE_INTERSECT, NP_COMBINE_UNION = 0, 1
 NP_RES_SLOTMAP, NP_RES_WINDOW = 0, 1
 NP_PRED_SHARED_ARGMAX, NP_PRED_PERLAYER_SIGMOID = 0, 1
 NP_H2D_STAGED, NP_H2D_FUSED = 0, 1
+NP_SLOTS_REUSE, NP_SLOTS_COMPACT = 0, 1
 KIND_NAMES = ["dense", "predictor", "set", "gather", "scatter", "ffn", "finish"]
 NP_N_KINDS = len(KIND_NAMES)
 
@@ -26,7 +27,7 @@ class ModelDesc(ctypes.Structure):
         ("dtype", ctypes.c_int32), ("has_gate", ctypes.c_int32), ("combine", ctypes.c_int32),
         ("residency", ctypes.c_int32), ("window", ctypes.c_int32), ("batch", ctypes.c_int32),
         ("staging_rows", ctypes.c_int32), ("pred_hidden", ctypes.c_int32), ("pred_kind", ctypes.c_int32),
-        ("h2d_mode", ctypes.c_int32), ("activation", ctypes.c_int32),
+        ("h2d_mode", ctypes.c_int32), ("activation", ctypes.c_int32), ("slots", ctypes.c_int32),
         ("host_store", ctypes.c_void_p), ("dense_w", ctypes.c_void_p), ("pred_w1", ctypes.c_void_p),
         ("pred_w2", ctypes.c_void_p), ("pred_b2", ctypes.c_void_p), ("centroids", ctypes.c_void_p),
         ("main_stream", ctypes.c_void_p), ("side_stream", ctypes.c_void_p),
@@ -40,12 +41,14 @@ class DeltaView(ctypes.Structure):
         ("counts", ctypes.c_void_p), ("active", ctypes.c_void_p), ("active_slot", ctypes.c_void_p),
         ("din_neuron", ctypes.c_void_p), ("din_slot", ctypes.c_void_p), ("dout_neuron", ctypes.c_void_p),
         ("ids", ctypes.c_void_p),
+        ("move_count", ctypes.c_void_p), ("move_src", ctypes.c_void_p), ("move_dst", ctypes.c_void_p),
     ]
 
 
 class Stats(ctypes.Structure):
     _fields_ = [("token", ctypes.c_int64), ("active_rows", ctypes.c_int64), ("din_rows", ctypes.c_int64),
-                ("dout_rows", ctypes.c_int64), ("dropped_rows", ctypes.c_int64), ("h2d_bytes", ctypes.c_int64)]
+                ("dout_rows", ctypes.c_int64), ("dropped_rows", ctypes.c_int64), ("h2d_bytes", ctypes.c_int64),
+                ("moved_rows", ctypes.c_int64)]
 
 
 # symbol -> (restype, argtypes)

@@ -92,7 +92,10 @@ struct np_model {
   // predictor hidden layer as hi/lo 16-bit operands [16][H]
   bool tc = false;
   RowMaps map_bufs{}, map_dense{}, map_w1{}, map_w2{};
-  int* slot_hw = nullptr;  // [S] one past the highest occupied slot
+  int* slot_hw = nullptr;  // [S] one past the highest occupied slot (|R| when compact)
+  // compact placement (rows in [0, |R|)): row moves of the last delta
+  bool compact = false;
+  int *mv_src = nullptr, *mv_dst = nullptr, *mv_oldct = nullptr, *mv_count = nullptr;
   MmaPlan plan_ffn{}, plan_hid{}, plan_heads{};
   uint16_t* zhl = nullptr;
   // residual chaining (every batch size): bases [2][B][D], accumulators [3][B][D]
@@ -257,6 +260,9 @@ np_status enqueue_layer_ffn(np_model* m, cudaStream_t st, int l, const float* hb
   }
   const int s = l - m->dn;
   const size_t proj_stride = (size_t)m->K * m->row_bytes;
+  if (m->compact)  // the occupied region [0, |R|)
+    return enqueue_ffn(m, st, NP_KIND_FFN, layer_bufs(m, s), proj_stride, nullptr, m->slot_hw + s, 0, m->K, m->K,
+                       hb, yprev, hb_out, y_acc, y_zero, 0);
   return enqueue_ffn(m, st, NP_KIND_FFN, layer_bufs(m, s), proj_stride, m->active_slot + (size_t)s * m->K,
                      m->counts + (size_t)s * 4, 0, m->K, m->K, hb, yprev, hb_out, y_acc, y_zero, 0);
 }
@@ -444,6 +450,12 @@ MoveLaunch move_args(const np_model* m, int s) {
   a.count = m->counts + (size_t)s * 4 + 1;
   a.staging = static_cast<unsigned char*>(m->staging) + (size_t)(s & 1) * m->staging_rows * m->rec_bytes;
   a.bufs_layer = const_cast<unsigned char*>(layer_bufs(m, s));
+  if (m->compact) {
+    a.mv_src = m->mv_src + (size_t)s * m->K;
+    a.mv_dst = m->mv_dst + (size_t)s * m->K;
+    a.mv_oldct = m->mv_oldct + (size_t)s * m->K;
+    a.mv_count = m->mv_count + s;
+  }
   a.err = m->err;
   return a;
 }
@@ -465,6 +477,12 @@ np_status join_side(np_model* m, cudaStream_t st) {
 np_status enqueue_move(np_model* m, int s) {
   cudaStream_t g = gather_stream(m, s), x = m->xs;
   MoveLaunch a = move_args(m, s);
+  if (m->compact) {
+    // kept rows fill the freed slots before incoming rows may overwrite the
+    // end of the region (device to device, HBM-bound)
+    a.grid = m->scatter_grid;
+    NP_TRY(launch(m, NP_KIND_SCATTER, g, 0, [&] { return launch_move_rows(a, g); }));
+  }
   if (m->d.h2d_mode == NP_H2D_FUSED) {
     a.chunk_begin = 0;
     a.chunk_cap = m->K;
@@ -534,6 +552,11 @@ SetLaunch set_args(np_model* m, int first_sparse, int n_layers) {
   a.ls_old = m->ls_old;
   a.totals = m->totals;
   a.slot_hw = m->slot_hw;
+  a.compact = m->compact;
+  a.mv_src = m->mv_src;
+  a.mv_dst = m->mv_dst;
+  a.mv_oldct = m->mv_oldct;
+  a.mv_count = m->mv_count;
   a.err = m->err;
   return a;
 }
@@ -675,6 +698,9 @@ static np_status validate(const np_model_desc* d) {
   if (d->h2d_mode != NP_H2D_STAGED && d->h2d_mode != NP_H2D_FUSED) return arg_fail("bad h2d_mode");
   if (d->activation != NP_ACT_RELU && d->activation != NP_ACT_SWIGLU) return arg_fail("bad activation");
   if (d->activation == NP_ACT_SWIGLU && !d->has_gate) return arg_fail("SwiGLU needs a gate projection");
+  if (d->slots != NP_SLOTS_REUSE && d->slots != NP_SLOTS_COMPACT) return arg_fail("bad slots");
+  if (d->batch > 1 && d->residency == NP_RES_WINDOW && d->slots != NP_SLOTS_COMPACT)
+    return arg_fail("batched decoding with windowing needs the compact placement (its FFN covers the occupied rows)");
   if (d->pred_hidden < 1 || (d->pred_hidden * esz) % 16 != 0 ||
       d->pred_hidden / (16 / esz) > kThreads * kMaxChunksPerThread)
     return arg_fail("pred_hidden must be positive, rows a multiple of 16 bytes, <= 8192");
@@ -718,6 +744,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   m->esz = desc->dtype == NP_F32 ? 4 : 2;
   m->staging_rows = desc->staging_rows > 0 ? desc->staging_rows : m->K;
   m->window = desc->residency == NP_RES_WINDOW ? desc->window : 1;
+  m->compact = desc->slots == NP_SLOTS_COMPACT;
   m->row_bytes = (size_t)m->D * m->esz;
   m->rec_bytes = m->nproj * m->row_bytes;
   m->main = static_cast<cudaStream_t>(desc->main_stream);
@@ -812,6 +839,11 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if ((st = dev_alloc(m, &m->dout_n, Sa * K)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->dout_s, Sa * K)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->ls_old, Sa * K)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->slot_hw, Sa)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->mv_count, Sa)) != NP_OK) return fail(st);
+  if (m->compact && ((st = dev_alloc(m, &m->mv_src, Sa * K)) != NP_OK || (st = dev_alloc(m, &m->mv_dst, Sa * K)) != NP_OK ||
+                     (st = dev_alloc(m, &m->mv_oldct, Sa * K)) != NP_OK))
+    return fail(st);
   if ((st = dev_alloc(m, &m->totals, 8)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->err, 4)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->z, (size_t)m->B * m->H)) != NP_OK) return fail(st);
@@ -843,7 +875,6 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     if ((e = make_row_maps(&m->map_w1, m->d.pred_w1, dt, (uint64_t)m->H, m->D)) != cudaSuccess ||
         (e = make_row_maps(&m->map_w2, m->d.pred_w2, dt, (uint64_t)m->NH * m->C, m->H)) != cudaSuccess)
       return fail(cuda_fail(e, "tensor map of the predictor"));
-    if ((st = dev_alloc(m, &m->slot_hw, Sa)) != NP_OK) return fail(st);
     if ((st = dev_alloc(m, &m->zhl, 16 * (size_t)m->H)) != NP_OK) return fail(st);
     if (env_int("NP_TUNE_VERBOSE", 0) == 1)
       std::fprintf(stderr, "np: tensor-core ffn %d clusters x %d, %d stages; hidden %d x %d; heads %d x %d\n",
@@ -930,7 +961,7 @@ np_status np_reset_sequence(np_model* m) {
   cudaStream_t st = m->main;
   NP_TRY(join_side(m, st));
   return launch(m, NP_KIND_SET, st, 0, [&] {
-    return launch_reset_state(m->slotmap, m->inv, m->resbits, m->S, m->F, m->K, m->W, st);
+    return launch_reset_state(m->slotmap, m->inv, m->resbits, m->slot_hw, m->S, m->F, m->K, m->W, st);
   });
 }
 
@@ -959,6 +990,9 @@ static void fill_view(const np_model* m, np_delta_view* v) {
   v->din_slot = m->din_s;
   v->dout_neuron = m->dout_n;
   v->ids = m->d.pred_kind == NP_PRED_SHARED_ARGMAX ? m->ids : nullptr;
+  v->move_count = m->mv_count;
+  v->move_src = m->mv_src;
+  v->move_dst = m->mv_dst;
 }
 
 np_status np_last_delta(np_model* m, np_delta_view* out) {
@@ -1060,6 +1094,8 @@ np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev)
     a.bufs = m->bufs;
     a.active_slot = m->active_slot;
     a.counts = m->counts;
+    a.n_rows = m->slot_hw;
+    a.compact = m->compact;
     a.n_dense = m->dn;
     a.F = m->F;
     a.K = m->K;
@@ -1197,8 +1233,10 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
     NP_TRY(sync_model(m));
     NP_TRY(read_device_error(m));
     if (m->S > 0) {
-      std::vector<int> c((size_t)m->S * 4);
+      std::vector<int> c((size_t)m->S * 4), mv((size_t)m->S);
       CUDA_TRY(cudaMemcpy(c.data(), m->counts, c.size() * sizeof(int), cudaMemcpyDeviceToHost));
+      CUDA_TRY(cudaMemcpy(mv.data(), m->mv_count, mv.size() * sizeof(int), cudaMemcpyDeviceToHost));
+      for (int s = 0; s < m->S; ++s) stats_host->moved_rows += mv[s];
       for (int s = 0; s < m->S; ++s) {
         stats_host->active_rows += c[s * 4 + 0];
         stats_host->din_rows += c[s * 4 + 1];

@@ -588,8 +588,9 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
       const int s = l - a.n_dense;
       proj = (size_t)a.K * row_bytes;
       base = static_cast<const unsigned char*>(a.bufs) + (size_t)s * NPROJ * proj;
-      *list = a.active_slot + (size_t)s * a.K;
-      n = a.counts[(size_t)s * 4];
+      // compact placement: the occupied region [0, n_rows); else the active rows
+      *list = a.compact ? nullptr : a.active_slot + (size_t)s * a.K;
+      n = a.compact ? a.n_rows[s] : a.counts[(size_t)s * 4];
       n = n < 0 ? 0 : (n > a.K ? a.K : n);
       *limit = a.K;
     }

@@ -52,6 +52,8 @@ struct FfnChainLaunch {
   const void* bufs;          // [S][n_proj][K][D] resident rows
   const int* active_slot;    // [S][K]
   const int* counts;         // [S][4] (|A| first)
+  const int* n_rows;         // [S] occupied rows; with `compact` the FFN covers rows [0, n_rows)
+  int compact;
   int n_dense, F, K;
   int first, count;
   float* h;                  // [D] residual stream, in and out
@@ -132,13 +134,21 @@ struct SetLaunch {
   int* dout_s;            // [S][K] slot each outgoing neuron held
   int* ls_old;            // [S][K] previous last use of each active neuron
   unsigned long long* totals;  // running sums: |A|, |D_in|, |D_out|, dropped
-  int* slot_hw;           // [S] one past the highest occupied slot (an upper bound), or null
+  int* slot_hw;           // [S] one past the highest occupied slot (an upper bound), or null;
+                          // exactly |R| under the compact placement
+  // compact placement: rows stay in [0, |R|); freed slots below the new count
+  // are refilled from the end of the region, incoming rows are appended
+  int compact;
+  int* mv_src;            // [S][K] row moves, slot read
+  int* mv_dst;            // [S][K] slot written (a slot freed by D_out)
+  int* mv_oldct;          // [S][K] previous content of each written slot
+  int* mv_count;          // [S] number of moves
   int* err;
 };
 cudaError_t launch_set(const SetLaunch& a, cudaStream_t st);
 cudaError_t launch_rollback(const SetLaunch& a, cudaStream_t st);  // undo launch_set from its lists
-cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int S, int F, int K, int words,
-                               cudaStream_t st);
+cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int* slot_hw, int S, int F, int K,
+                               int words, cudaStream_t st);
 
 // ---- host-link gather and deinterleave-scatter (np_scatter.cu) -----------
 struct MoveLaunch {
@@ -156,6 +166,10 @@ struct MoveLaunch {
   void* staging;            // [chunk_cap][rec_vec] device
   void* bufs_layer;         // [n_proj][K][row_vec] device
   const int* din_oldct;     // restore: neuron whose bytes each incoming slot held (-1: zero)
+  const int* mv_src;        // compact placement: row moves inside the buffers
+  const int* mv_dst;
+  const int* mv_oldct;      // restore: neuron whose bytes each move target held
+  const int* mv_count;      // device number of moves, or null (no moves)
   int grid;
   int* err;
 };
@@ -163,6 +177,7 @@ cudaError_t launch_gather(const MoveLaunch& a, cudaStream_t st);    // host stor
 cudaError_t launch_scatter(const MoveLaunch& a, cudaStream_t st);   // staging -> buffers
 cudaError_t launch_fused(const MoveLaunch& a, cudaStream_t st);     // host store -> buffers
 cudaError_t launch_restore(const MoveLaunch& a, cudaStream_t st);   // previous slot contents back
+cudaError_t launch_move_rows(const MoveLaunch& a, cudaStream_t st); // bufs[dst] = bufs[src] per move
 
 
 // ---- batched row products on the tensor cores (np_mma.cu) ----------------

@@ -1,5 +1,5 @@
 // Incoming-row movement (sm_103a): host weight store -> device staging ->
-// projection buffers.
+// projection buffers, and the row moves of the compact placement.
 //
 // NeuroPrefetcher section 3.5 ("I/O Path") and its full text: incoming
 // neuron IDs are sorted and read as neuron-centric records (gate | up |
@@ -96,23 +96,55 @@ __global__ void __launch_bounds__(kMoveThreads) fused_kernel(MoveLaunch a) {
   }
 }
 
-// Put back what the assigned slots held before this delta: the record of
-// din_oldct[i], or zeros for a slot that never held a row.
-__global__ void __launch_bounds__(kMoveThreads) restore_kernel(MoveLaunch a) {
-  const int end = chunk_end(a);
+// Compact placement: bufs[p][mv_dst[i]] = bufs[p][mv_src[i]], one CTA per
+// (move, projection row).  Sources lie at or above the region's new end and
+// targets below it, so no copy reads a row another one writes.
+__global__ void __launch_bounds__(kMoveThreads) move_rows_kernel(MoveLaunch a) {
+  int cnt = *a.mv_count;
+  if (cnt > a.K) cnt = a.K;
+  const int units = cnt * a.n_proj;
+  uint4* bufs = static_cast<uint4*>(a.bufs_layer);
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int i = u / a.n_proj, p = u - i * a.n_proj;
+    const int src = a.mv_src[i], dst = a.mv_dst[i];
+    if ((unsigned)src >= (unsigned)a.K || (unsigned)dst >= (unsigned)a.K) {
+      if (threadIdx.x == 0) atomicExch(a.err, kDevErrBounds);
+      continue;
+    }
+    copy_vecs(bufs + ((size_t)p * a.K + src) * a.row_vec, bufs + ((size_t)p * a.K + dst) * a.row_vec, a.row_vec);
+  }
+}
+
+// One slot's rows back to the record of neuron n, or zeros (n < 0: the slot
+// never held a row).
+__device__ __forceinline__ void restore_slot(const MoveLaunch& a, int slot, int n) {
   const uint4* store = static_cast<const uint4*>(a.store_layer);
   uint4* bufs = static_cast<uint4*>(a.bufs_layer);
+  for (int p = 0; p < a.n_proj; ++p) {
+    uint4* dst = bufs + ((size_t)p * a.K + slot) * a.row_vec;
+    if ((unsigned)n < (unsigned)a.F) {
+      copy_vecs(store + (size_t)n * a.rec_vec + (size_t)p * a.row_vec, dst, a.row_vec);
+    } else {
+      for (int j = threadIdx.x; j < a.row_vec; j += kMoveThreads) dst[j] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+// Put back what the slots written by this delta held before it: the slots
+// assigned to D_in (din_oldct) and, under the compact placement, the move
+// targets (mv_oldct).  The two sets of slots are disjoint.
+__global__ void __launch_bounds__(kMoveThreads) restore_kernel(MoveLaunch a) {
+  const int end = chunk_end(a);
   for (int i = a.chunk_begin + blockIdx.x; i < end; i += gridDim.x) {
     const int slot = a.din_s[i];
-    if ((unsigned)slot >= (unsigned)a.K) continue;
-    const int n = a.din_oldct[i];
-    for (int p = 0; p < a.n_proj; ++p) {
-      uint4* dst = bufs + ((size_t)p * a.K + slot) * a.row_vec;
-      if ((unsigned)n < (unsigned)a.F) {
-        copy_vecs(store + (size_t)n * a.rec_vec + (size_t)p * a.row_vec, dst, a.row_vec);
-      } else {
-        for (int j = threadIdx.x; j < a.row_vec; j += kMoveThreads) dst[j] = make_uint4(0u, 0u, 0u, 0u);
-      }
+    if ((unsigned)slot < (unsigned)a.K) restore_slot(a, slot, a.din_oldct[i]);
+  }
+  if (a.mv_count) {
+    int cnt = *a.mv_count;
+    if (cnt > a.K) cnt = a.K;
+    for (int i = blockIdx.x; i < cnt; i += gridDim.x) {
+      const int slot = a.mv_dst[i];
+      if ((unsigned)slot < (unsigned)a.K) restore_slot(a, slot, a.mv_oldct[i]);
     }
   }
 }
@@ -127,6 +159,10 @@ cudaError_t launch_scatter(const MoveLaunch& a, cudaStream_t st) {
 }
 cudaError_t launch_fused(const MoveLaunch& a, cudaStream_t st) {
   fused_kernel<<<a.grid, kMoveThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+cudaError_t launch_move_rows(const MoveLaunch& a, cudaStream_t st) {
+  move_rows_kernel<<<a.grid, kMoveThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 cudaError_t launch_restore(const MoveLaunch& a, cudaStream_t st) {

@@ -12,9 +12,12 @@
 //     runtime), or with windowing (LLM in a flash 3.1) the neurons of R_prev
 //     still used within the last W tokens plus A, evicting the oldest last
 //     use first (ties: lowest ID first) while more than K_max remain.
-//  4. D_in = A \ R_prev, D_out = R_prev \ R_next.  Slots of R_prev ∩ R_next
-//     stay; the free slots in ascending order go to D_in in ascending ID
-//     order.
+//  4. D_in = A \ R_prev, D_out = R_prev \ R_next.  Slot reuse: slots of
+//     R_prev ∩ R_next stay; the free slots in ascending order go to D_in in
+//     ascending ID order.  Compact placement (LLM in a flash 3.3): the rows
+//     occupy exactly [0, |R|); with n = |R_prev| - |D_out|, each slot below n
+//     freed by D_out takes a kept row from [n, |R_prev|) (both in ascending
+//     slot order, one row move each), and D_in is appended at n, n + 1, ...
 //
 // The state (slot map S, inverse map inv, slot contents, resident bitmask,
 // last use) is updated in place and only where it changes; every value
@@ -74,11 +77,80 @@ __device__ __forceinline__ int bit_rank(const uint32_t* words, const int* excl, 
   return excl[w] + __popc(words[w] & ((1u << (n & 31)) - 1u));
 }
 
+// Slot reuse: the free slots (not held by a kept neuron) in ascending order
+// into free_list; *n_free and the high-water mark are published by thread 0.
+__device__ __forceinline__ void reuse_assign(const SetLaunch& a, int s, int tid, int KW, int n_in,
+                                             const uint32_t* occ, int* wsum, int* s_hw, int* free_list,
+                                             int* nfree_out) {
+  const int K = a.K;
+  uint32_t fw = 0;
+  if (tid < KW) {
+    fw = ~occ[tid];
+    if (tid == KW - 1 && (K & 31)) fw &= (1u << (K & 31)) - 1u;
+  }
+  int n_free;
+  const int efree = block_scan(__popc(fw), wsum, &n_free);
+  {
+    int p = efree;
+    for (uint32_t w = fw; w; w &= w - 1) free_list[p++] = tid * 32 + __ffs(w) - 1;
+  }
+  if (tid < KW && occ[tid]) atomicMax(s_hw, tid * 32 + 32 - __clz(occ[tid]));
+  __syncthreads();
+  if (tid == 0) {
+    if (n_in > n_free) atomicExch(a.err, kDevErrBounds);
+    *nfree_out = n_free;
+    // one past the highest occupied slot after this delta (kept slots, and
+    // the free slots handed out in ascending order)
+    if (a.slot_hw) {
+      const int na = n_in < n_free ? n_in : n_free;
+      int hw = *s_hw;
+      if (na > 0 && free_list[na - 1] + 1 > hw) hw = free_list[na - 1] + 1;
+      a.slot_hw[s] = hw;
+    }
+    if (a.mv_count) a.mv_count[s] = 0;
+  }
+}
+
+// Compact placement: the i-th freed slot below n_keep (ascending) takes the
+// row of the i-th kept slot at or above n_keep (ascending); the moves are
+// written to the layer's move lists.  Incoming rows go to n_keep, n_keep+1...
+__device__ __forceinline__ void compact_assign(const SetLaunch& a, int s, int tid, int KW, int n_keep, int n_in,
+                                               const uint32_t* s_hole, const uint32_t* s_mov, int* wsum,
+                                               int* hole_list, int* nfree_out) {
+  const uint32_t hw = tid < KW ? s_hole[tid] : 0u;
+  const uint32_t mw = tid < KW ? s_mov[tid] : 0u;
+  int n_holes, n_mov;
+  const int eh = block_scan(__popc(hw), wsum, &n_holes);
+  const int em = block_scan(__popc(mw), wsum, &n_mov);
+  {
+    int p = eh;
+    for (uint32_t w = hw; w; w &= w - 1) hole_list[p++] = tid * 32 + __ffs(w) - 1;
+  }
+  __syncthreads();
+  const int n_mv = n_holes < n_mov ? n_holes : n_mov;
+  int* msrc = a.mv_src + (size_t)s * a.K;
+  int* mdst = a.mv_dst + (size_t)s * a.K;
+  {
+    int p = em;
+    for (uint32_t w = mw; w && p < n_mv; w &= w - 1, ++p) {
+      msrc[p] = tid * 32 + __ffs(w) - 1;
+      mdst[p] = hole_list[p];
+    }
+  }
+  if (tid == 0) {
+    if (n_holes != n_mov || n_keep < 0 || n_keep + n_in > a.K) atomicExch(a.err, kDevErrBounds);
+    *nfree_out = a.K - (n_keep < 0 ? 0 : n_keep);  // slots left for appends
+    a.mv_count[s] = n_mv;
+    if (a.slot_hw) a.slot_hw[s] = n_keep + n_in;
+  }
+}
+
 __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   __shared__ int wsum[32];
   __shared__ uint32_t occ[kMaxKmax / 32];
+  __shared__ uint32_t s_hole[kMaxKmax / 32], s_mov[kMaxKmax / 32];  // compact: slots to refill / to move
   __shared__ int hist[33];
-  __shared__ int cut_age, cut_need, s_hw;
+  __shared__ int cut_age, cut_need, s_hw, s_nfree;
   __shared__ uint32_t s_a[kMaxWords], s_out[kMaxWords], s_keep[kMaxWords];
   __shared__ int s_ea[kMaxWords], s_eout[kMaxWords];
   extern __shared__ int free_list[];  // [K]
@@ -100,6 +172,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   int* __restrict__ out_out = a.dout_n + (size_t)s * K;
   int* __restrict__ out_outs = a.dout_s + (size_t)s * K;
   int* __restrict__ out_lsold = a.ls_old + (size_t)s * K;
+  const bool compact = a.compact != 0;
 
   if (a.keys && a.ids_out && blockIdx.x == 0)
     for (int h = tid; h < a.batch * a.n_heads; h += kSetThreads)
@@ -201,7 +274,8 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   const uint32_t doutw = rw & ~nw;
 
   // 4. ranks within A, D_in, D_out; the lists in ascending ID order
-  int n_a, n_in, n_out;
+  int n_a, n_in, n_out, n_old = 0;
+  if (compact) (void)block_scan(__popc(rw), wsum, &n_old);
   const int ea = block_scan(__popc(aw), wsum, &n_a);
   const int ein = block_scan(__popc(dinw), wsum, &n_in);
   const int eout = block_scan(__popc(doutw), wsum, &n_out);
@@ -219,9 +293,14 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     for (uint32_t w = doutw; w; w &= w - 1) out_out[p++] = i * 32 + __ffs(w) - 1;
   }
   const int KW = (K + 31) / 32;
-  if (tid < KW) occ[tid] = 0u;
+  if (tid < KW) {
+    occ[tid] = 0u;
+    s_hole[tid] = 0u;
+    s_mov[tid] = 0u;
+  }
   if (tid == 0) s_hw = 0;
   __syncthreads();
+  const int n_keep = n_old - n_out;  // compact: rows that stay below this count
 
   // 5. one pass over the slots: occupied = holds a neuron that stays;
   //    kept active neurons get their slot, outgoing neurons record theirs
@@ -230,37 +309,24 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     if ((unsigned)n >= (unsigned)F) continue;
     const uint32_t bit = 1u << (n & 31);
     const int w = n >> 5;
+    const uint32_t kbit = 1u << (k & 31);
     if (s_out[w] & bit) {
       out_outs[bit_rank(s_out, s_eout, n)] = k;
+      if (compact && k < n_keep) atomicOr(&s_hole[k >> 5], kbit);
     } else if (s_keep[w] & bit) {
-      atomicOr(&occ[k >> 5], 1u << (k & 31));
+      atomicOr(&occ[k >> 5], kbit);
+      if (compact && k >= n_keep) atomicOr(&s_mov[k >> 5], kbit);
       if (s_a[w] & bit) out_as[bit_rank(s_a, s_ea, n)] = k;
     }
+    if (compact && k >= n_old) atomicExch(a.err, kDevErrBounds);  // region not contiguous
   }
   __syncthreads();
-  // free slots in ascending order
-  uint32_t fw = 0;
-  if (tid < KW) {
-    fw = ~occ[tid];
-    if (tid == KW - 1 && (K & 31)) fw &= (1u << (K & 31)) - 1u;
+  if (compact) {
+    compact_assign(a, s, tid, KW, n_keep, n_in, s_hole, s_mov, wsum, free_list, &s_nfree);
+  } else {
+    reuse_assign(a, s, tid, KW, n_in, occ, wsum, &s_hw, free_list, &s_nfree);
   }
-  int n_free;
-  const int efree = block_scan(__popc(fw), wsum, &n_free);
-  {
-    int p = efree;
-    for (uint32_t w = fw; w; w &= w - 1) free_list[p++] = tid * 32 + __ffs(w) - 1;
-  }
-  if (tid < KW && occ[tid]) atomicMax(&s_hw, tid * 32 + 32 - __clz(occ[tid]));
   __syncthreads();
-  if (n_in > n_free && tid == 0) atomicExch(a.err, kDevErrBounds);
-  // one past the highest occupied slot after this delta (kept slots, and the
-  // free slots handed out in ascending order)
-  if (tid == 0 && a.slot_hw) {
-    const int na = n_in < n_free ? n_in : n_free;
-    int hw = s_hw;
-    if (na > 0 && free_list[na - 1] + 1 > hw) hw = free_list[na - 1] + 1;
-    a.slot_hw[s] = hw;
-  }
 
   // 6. outgoing neurons leave (before incoming ones may take their slots)
   for (int r = tid; r < n_out; r += kSetThreads) {
@@ -270,10 +336,31 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     if ((unsigned)k < (unsigned)K) inv[k] = -1;
   }
   __syncthreads();
-  // 7. incoming neurons take the free slots; remember what the slots held
+  // 6b. compact: kept rows from the end of the region fill the freed slots
+  if (compact) {
+    const int n_mv = a.mv_count[s];
+    const int* msrc = a.mv_src + (size_t)s * K;
+    const int* mdst = a.mv_dst + (size_t)s * K;
+    int* mold = a.mv_oldct + (size_t)s * K;
+    for (int r = tid; r < n_mv; r += kSetThreads) {
+      const int src = msrc[r], dst = mdst[r];
+      const int n = inv[src];
+      if ((unsigned)n >= (unsigned)F) continue;
+      S[n] = dst;
+      inv[dst] = n;
+      inv[src] = -1;
+      mold[r] = ct[dst];
+      ct[dst] = n;
+      if (s_a[n >> 5] & (1u << (n & 31))) out_as[bit_rank(s_a, s_ea, n)] = dst;
+    }
+    __syncthreads();
+  }
+  // 7. incoming neurons take the free slots (slot reuse) or are appended
+  //    (compact); remember what the slots held
+  const int n_free = s_nfree;
   for (int r = tid; r < n_in; r += kSetThreads) {
     const int n = out_in[r];
-    const int k = r < n_free ? free_list[r] : 0;
+    const int k = r < n_free ? (compact ? n_keep + r : free_list[r]) : 0;
     out_ins[r] = k;
     out_inct[r] = ct[k];
     ct[k] = n;
@@ -319,7 +406,8 @@ __global__ void __launch_bounds__(kSetThreads) rollback_kernel(SetLaunch a) {
   const int* dinct = a.din_oldct + (size_t)s * K;
   const int* dout = a.dout_n + (size_t)s * K;
   const int* douts = a.dout_s + (size_t)s * K;
-  if (threadIdx.x == 0 && a.slot_hw) a.slot_hw[s] = K;  // an upper bound is always safe
+  // slot reuse: an upper bound of the high-water mark is always safe
+  if (threadIdx.x == 0 && a.slot_hw && !a.compact) a.slot_hw[s] = K;
   for (int r = threadIdx.x; r < n_in; r += kSetThreads) {
     const int n = din[r], k = dins[r];
     if ((unsigned)n >= (unsigned)F || (unsigned)k >= (unsigned)K) continue;
@@ -329,6 +417,23 @@ __global__ void __launch_bounds__(kSetThreads) rollback_kernel(SetLaunch a) {
     atomicAnd(&res[n >> 5], ~(1u << (n & 31)));
   }
   __syncthreads();
+  if (a.compact) {  // moved rows go back to the end of the region
+    const int n_mv = a.mv_count[s];
+    const int* msrc = a.mv_src + (size_t)s * K;
+    const int* mdst = a.mv_dst + (size_t)s * K;
+    const int* mold = a.mv_oldct + (size_t)s * K;
+    for (int r = threadIdx.x; r < n_mv; r += kSetThreads) {
+      const int src = msrc[r], dst = mdst[r];
+      if ((unsigned)src >= (unsigned)K || (unsigned)dst >= (unsigned)K) continue;
+      const int n = inv[dst];
+      if ((unsigned)n >= (unsigned)F) continue;
+      S[n] = src;
+      inv[src] = n;
+      inv[dst] = -1;
+      ct[dst] = mold[r];
+    }
+    __syncthreads();
+  }
   for (int r = threadIdx.x; r < n_out; r += kSetThreads) {
     const int n = dout[r], k = douts[r];
     if ((unsigned)n >= (unsigned)F || (unsigned)k >= (unsigned)K) continue;
@@ -344,11 +449,23 @@ __global__ void __launch_bounds__(kSetThreads) rollback_kernel(SetLaunch a) {
       if ((unsigned)n < (unsigned)F) ls[n] = old[r];
     }
   }
+  if (a.compact) {  // the region is [0, |R_prev|) again
+    __shared__ int wsum[32];
+    __syncthreads();
+    int n_res;
+    (void)block_scan(threadIdx.x < W ? __popc(res[threadIdx.x]) : 0, wsum, &n_res);
+    if (threadIdx.x == 0) {
+      if (a.slot_hw) a.slot_hw[s] = n_res;
+      a.mv_count[s] = 0;
+    }
+  }
 }
 
-__global__ void reset_state_kernel(int* slotmap, int* inv, uint32_t* resbits, size_t n_sm, size_t n_inv,
-                                   size_t n_res) {
+__global__ void reset_state_kernel(int* slotmap, int* inv, uint32_t* resbits, int* slot_hw, int n_layers,
+                                   size_t n_sm, size_t n_inv, size_t n_res) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
+  if (slot_hw && blockIdx.x == 0)
+    for (int s = threadIdx.x; s < n_layers; s += blockDim.x) slot_hw[s] = 0;
   for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n_sm; k += stride) slotmap[k] = -1;
   for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n_inv; k += stride) inv[k] = -1;
   for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n_res; k += stride) resbits[k] = 0u;
@@ -368,9 +485,10 @@ cudaError_t launch_rollback(const SetLaunch& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int S, int F, int K, int words,
-                               cudaStream_t st) {
-  reset_state_kernel<<<256, 256, 0, st>>>(slotmap, inv, resbits, (size_t)S * F, (size_t)S * K, (size_t)S * words);
+cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int* slot_hw, int S, int F, int K,
+                               int words, cudaStream_t st) {
+  reset_state_kernel<<<256, 256, 0, st>>>(slotmap, inv, resbits, slot_hw, S, (size_t)S * F, (size_t)S * K,
+                                          (size_t)S * words);
   return cudaGetLastError();
 }
 

@@ -45,6 +45,7 @@ class SparseDecoder:
                  pred_hidden: int, pred_kind: str = "shared_argmax", has_gate: bool = True,
                  combine: str = "union", residency: str = "slotmap", window: int = 1, batch: int = 1,
                  staging_rows: int = 0, h2d_mode: str = "fused", activation: str = "relu",
+                 slots: str = "reuse",
                  main_stream: torch.cuda.Stream | None = None, side_stream: torch.cuda.Stream | None = None,
                  read_hook=None):
         self.lib = L.load()
@@ -72,6 +73,8 @@ class SparseDecoder:
         d.residency = {"slotmap": L.NP_RES_SLOTMAP, "window": L.NP_RES_WINDOW}[residency]
         d.window, d.batch, d.staging_rows, d.pred_hidden = window, batch, staging_rows, pred_hidden
         d.activation = {"relu": 0, "swiglu": 1}[activation]
+        d.slots = {"reuse": L.NP_SLOTS_REUSE, "compact": L.NP_SLOTS_COMPACT}[slots]
+        self.compact = slots == "compact"
         d.pred_kind = {"shared_argmax": L.NP_PRED_SHARED_ARGMAX,
                        "perlayer_sigmoid": L.NP_PRED_PERLAYER_SIGMOID}[pred_kind]
         d.h2d_mode = {"staged": L.NP_H2D_STAGED, "fused": L.NP_H2D_FUSED}[h2d_mode]
@@ -175,7 +178,10 @@ class SparseDecoder:
                 "active_slot": _wrap(v.active_slot, (S, K), torch.int32),
                 "din_neuron": _wrap(v.din_neuron, (S, K), torch.int32),
                 "din_slot": _wrap(v.din_slot, (S, K), torch.int32),
-                "dout_neuron": _wrap(v.dout_neuron, (S, K), torch.int32)}
+                "dout_neuron": _wrap(v.dout_neuron, (S, K), torch.int32),
+                "move_count": _wrap(v.move_count, (S,), torch.int32),
+                "move_src": _wrap(v.move_src, (S, K), torch.int32) if v.move_src else None,
+                "move_dst": _wrap(v.move_dst, (S, K), torch.int32) if v.move_dst else None}
 
     def scatter(self, layer: int = -1) -> None:
         L.check(self.lib.np_scatter(self.model, layer), "np_scatter")
@@ -272,7 +278,7 @@ def decoder_for(wl, *, h2d_mode: str = "fused", staging_rows: int | None = None,
         pred_kind=cfg.pred_kind, has_gate=cfg.has_gate, combine=cfg.combine, residency=cfg.residency,
         window=cfg.window if cfg.residency == "window" else 1, batch=cfg.batch,
         staging_rows=cfg.staging_rows if staging_rows is None else staging_rows, h2d_mode=h2d_mode,
-        activation=cfg.activation,
+        activation=cfg.activation, slots=cfg.slots,
         read_hook=read_hook, **kw)
 
 

@@ -114,6 +114,17 @@ def run_and_compare(wl, n_tokens=None, *, h2d_mode="staged", staging_rows=None, 
                 sm, inv = dec.get_state(cfg.n_dense + s)
                 assert np.array_equal(np.asarray(sm), orc.slotmap[s]), f"slot map differs, layer {s}"
                 assert np.array_equal(np.asarray(inv), orc.inv[s]), f"inverse map differs, layer {s}"
+            # ---- row moves of the compact placement (none under slot reuse)
+            mvc = view["move_count"].cpu().numpy()
+            msrc = view["move_src"].cpu().numpy() if view["move_src"] is not None else None
+            mdst = view["move_dst"].cpu().numpy() if view["move_dst"] is not None else None
+            for s in range(cfg.n_sparse):
+                assert mvc[s] == len(rec.moves[s]), f"token {t} layer {s}: {mvc[s]} moves vs {len(rec.moves[s])}"
+                if mvc[s]:
+                    got = list(zip(msrc[s, :mvc[s]].tolist(), mdst[s, :mvc[s]].tolist()))
+                    assert got == [tuple(m) for m in rec.moves[s]], f"token {t} layer {s}: moves differ"
+            assert st["moved_rows"] == int(mvc.sum())
+            summary["moved_rows"] = summary.get("moved_rows", 0) + int(mvc.sum())
             summary["din_rows"] += int(counts[:, 1].sum())
             assert st["din_rows"] == int(counts[:, 1].sum())
             # ---- residual stream after all layers

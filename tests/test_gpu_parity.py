@@ -39,6 +39,14 @@ SMALL_CASES = {
     # SwiGLU activation (silu gate) on the CUDA-core and tensor-core FFNs
     "small-f16-swiglu": (SMALL_F16.replace(activation="swiglu"), {}),
     "small-batched-swiglu": (SMALL_BATCHED.replace(activation="swiglu"), {}),
+    # compact placement (swap-with-last + append): moves, appends and the FFN
+    # over the occupied region, with and without windowing
+    "small-f16-compact": (SMALL_F16.replace(slots="compact"), {}),
+    "small-f16-compact-fused": (SMALL_F16.replace(slots="compact"), {"h2d_mode": "fused"}),
+    "small-bf16-compact-staging7": (SMALL_BF16.replace(slots="compact"), {"staging_rows": 7}),
+    "small-opt-window-compact": (SMALL_OPT.replace(slots="compact"), {}),
+    "small-batched-compact": (SMALL_BATCHED.replace(slots="compact"), {}),
+    "small-batched-window-compact": (SMALL_BATCHED.replace(residency="window", window=3, slots="compact"), {}),
 }
 
 
@@ -93,8 +101,9 @@ def test_repeated_token_has_empty_delta():
     dec.close()
 
 
-def test_reset_sequence_is_cold_start():
-    cfg = SMALL_F16
+@pytest.mark.parametrize("slots", ["reuse", "compact"])
+def test_reset_sequence_is_cold_start(slots):
+    cfg = SMALL_F16.replace(slots=slots)
     wl = make_workload(cfg)
     dec = build_decoder(wl)
     orc = OracleDecoder(wl)
@@ -109,8 +118,9 @@ def test_reset_sequence_is_cold_start():
     dec.close()
 
 
-def test_piecewise_entry_points_match_decode():
-    cfg = SMALL_BF16
+@pytest.mark.parametrize("slots", ["reuse", "compact"])
+def test_piecewise_entry_points_match_decode(slots):
+    cfg = SMALL_BF16.replace(slots=slots)
     wl = make_workload(cfg)
     dec = build_decoder(wl)
     orc = OracleDecoder(wl)
@@ -160,7 +170,8 @@ def test_state_machine_errors():
 
 
 @pytest.mark.parametrize("bad", [{"k_max": 5000}, {"d_model": 12}, {"n_dense": 0},
-                                 {"activation": "swiglu", "has_gate": False}])
+                                 {"activation": "swiglu", "has_gate": False},
+                                 {"batch": 2, "pred_hidden": 128, "residency": "window", "window": 3}])
 def test_invalid_config_rejected(bad):
     from sparse_activation_decode_gb300 import NpError
     cfg = SMALL_F16
@@ -176,8 +187,9 @@ def test_invalid_config_rejected(bad):
     assert e.value.status == -1
 
 
-def test_read_failure_restores_committed_state():
-    cfg = SMALL_F16
+@pytest.mark.parametrize("slots", ["reuse", "compact"])
+def test_read_failure_restores_committed_state(slots):
+    cfg = SMALL_F16.replace(slots=slots)
     wl = make_workload(cfg)
     fail_layer = {"layer": -1}
 
@@ -215,8 +227,11 @@ def test_read_failure_restores_committed_state():
 # Full-size shapes: every integer output compared in full, buffer bytes on
 # sampled slots, FFN outputs per layer.
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("cfg,tokens", [(LLAMA7B, 3), (LLAMA13B, 2), (OPT67B, 2), (BATCHED7B, 2)],
-                         ids=["llama2-7b", "llama2-13b", "opt-6.7b", "llama2-7b-batch8"])
+@pytest.mark.parametrize("cfg,tokens", [(LLAMA7B, 3), (LLAMA13B, 2), (OPT67B, 2), (BATCHED7B, 2),
+                                        (LLAMA7B.replace(slots="compact"), 3),
+                                        (BATCHED7B.replace(slots="compact"), 2)],
+                         ids=["llama2-7b", "llama2-13b", "opt-6.7b", "llama2-7b-batch8", "llama2-7b-compact",
+                              "llama2-7b-batch8-compact"])
 def test_full_size_sampled(cfg, tokens):
     wl = make_workload(cfg.replace(n_warm=0, n_decode=tokens), device="cuda")
     summ = run_and_compare(wl, tokens, check_buffers=False, sample_slots=64, check_layer_y=True)
@@ -224,8 +239,10 @@ def test_full_size_sampled(cfg, tokens):
     assert summ["max_h_rel"] < FFN_TOL
 
 
-@pytest.mark.parametrize("cfg", [SMALL_F16, SMALL_BATCHED, SMALL_F16.replace(activation="swiglu")],
-                         ids=["small-f16", "small-batched", "small-f16-swiglu"])
+@pytest.mark.parametrize("cfg", [SMALL_F16, SMALL_BATCHED, SMALL_F16.replace(activation="swiglu"),
+                                 SMALL_F16.replace(slots="compact"), SMALL_OPT.replace(slots="compact")],
+                         ids=["small-f16", "small-batched", "small-f16-swiglu", "small-f16-compact",
+                              "small-opt-window-compact"])
 def test_ffn_layers_equals_layer_by_layer(cfg):
     # the chained FFN entry point equals h += FFN_l(h) applied layer by layer
     # through the standalone entry points, over dense and sparse layers
