@@ -57,6 +57,8 @@ def parse():
     p.add_argument("--persistence", type=float, default=None,
                    help="override the workload's token-to-token mask persistence (batched sweep)")
     p.add_argument("--h2d-mode", default="fused", choices=["staged", "fused"])
+    p.add_argument("--slots", default=None, choices=["reuse", "compact"],
+                   help="placement of resident rows (default: the workload's)")
     p.add_argument("--cpu-sample-tokens", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -296,6 +298,8 @@ def run_cuda(args):
     base = CONFIGS[args.config]
     if args.persistence is not None:
         base = base.replace(persistence=args.persistence)
+    if args.slots is not None:
+        base = base.replace(slots=args.slots)
     span = (base.batch - 1) * base.phase_step + 24
     T = min(W + 3 * K, base.n_centroids - span if base.n_centroids else 10 ** 9)
     cfg = base.replace(n_warm=0, n_decode=T, seed=base.seed + 7919 * rank)
@@ -357,6 +361,18 @@ def run_cuda(args):
     table = kernel_table(prof, peaks, h2d_peak or 0.0)
     link_ms = link_busy_ms(timeline)
     iso = isolated_kernels(dec, torch, cfg)
+    # rows read over the host link and rows moved inside HBM per token
+    # (synchronising stats calls, after every timed region of the decode)
+    n_st, din_rows, moved_rows = 16, 0, 0
+    for k in range(n_st):
+        st = dec.decode_token(tok(W + K + KP + k), stats=True)
+        din_rows += st["din_rows"]
+        moved_rows += st["moved_rows"]
+    rec_b = cfg.n_proj * cfg.d_model * cfg.elem_bytes
+    movement = {"tokens": n_st, "h2d_records_per_token": round(din_rows / n_st, 1),
+                "h2d_bytes_per_token": int(din_rows * rec_b / n_st),
+                "hbm_moved_records_per_token": round(moved_rows / n_st, 1),
+                "hbm_move_bytes_per_token": int(2 * moved_rows * rec_b / n_st)}
 
     # end to end through host buffers (pinned), copies inside the timed region
     e2e = None
@@ -428,11 +444,11 @@ def run_cuda(args):
                    "d_model": cfg.d_model, "d_ff": cfg.d_ff, "k_max": cfg.k_max, "centroids": cfg.n_centroids,
                    "combine": cfg.combine, "persistence": cfg.persistence, "batch": cfg.batch,
                    "density": cfg.density, "ffn": "tcgen05 tensor cores" if cfg.batch > 1 else "CUDA cores",
-                   "h2d_mode": args.h2d_mode, "parallelism": f"replicas x{world}",
+                   "h2d_mode": args.h2d_mode, "slots": cfg.slots, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (per-token weights ~2 GB > 129 MB)"},
         "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": table,
         "h2d_peak_gbs": round(h2d_peak, 1), "h2d_peak_after_gbs": round(h2d_after, 1), "host_link_busy_ms_per_token": round(link_ms / KP, 4),
-        "profiled_tokens": KP,
+        "profiled_tokens": KP, "movement": movement,
         "gpu_launches": launches, "active_density_last_step": round(union_density, 4) if union_density else None,
         "clocks": clk.summary(), "e2e": e2e, "workload_gen_s": round(gen_s, 1),
     }
