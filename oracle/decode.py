@@ -258,6 +258,34 @@ def window_resident(resident_prev: list[int], active: list[int], last_seen: dict
     return sorted(cand)
 
 
+def frequency_resident(resident_prev: list[int], active: list[int], count, k_max: int) -> list[int]:
+    """Resident set after a token under frequency-weighted caching
+    (DynamicInfer, "hierarchical neuron cache": importance v = a + lambda f,
+    a = predicted active now, f = the neuron's activation frequency so far in
+    the sequence; the cache keeps the highest importance up to its budget).
+
+    Reading: every active neuron must be resident (there is no CPU-side FFN
+    here), so lambda f < 1 orders the rest: R = A plus the previously resident
+    neurons, and while more than k_max remain the least frequently active of
+    the non-active ones go first, ties by ascending ID.  `count[n]` = tokens of
+    this sequence in which n was active, this one included."""
+    cand = set(resident_prev) | set(active)
+    if len(cand) > k_max:
+        act = set(active)
+        order = sorted((n for n in cand if n not in act), key=lambda n: (count[n], n))
+        for n in order[:len(cand) - k_max]:
+            cand.discard(n)
+    return sorted(cand)
+
+
+def predictor_source_layer(layer: int, lookahead: int) -> int:
+    """Layer whose input feeds the per-layer predictor of `layer`: with a
+    lookahead of k layers (DynamicInfer, "cross-layer sparse prediction": the
+    predictor of layer i+k takes the hidden state of layer i) it is layer
+    layer - k, and the token's input to layer 0 for the first layers."""
+    return max(layer - lookahead, 0)
+
+
 # ---------------------------------------------------------------------------
 # Whole-token decode
 # ---------------------------------------------------------------------------
@@ -293,6 +321,7 @@ class OracleDecoder:
         self.n_rows = [0] * S          # occupied rows under compact placement
         self.resident = [[] for _ in range(S)]
         self.last_seen = [dict() for _ in range(S)]
+        self.count = [np.zeros(F, dtype=np.int64) for _ in range(S)]   # frequency residency
         self.t = 0
         self.materialize = materialize_buffers
         # Projection buffers start zeroed; storage dtype kept (exact copies).
@@ -348,11 +377,13 @@ class OracleDecoder:
         B = cfg.batch
         h = f64(x).reshape(B, cfg.d_model).copy()
         rec = TokenRecord()
+        layer_in = []   # the residual stream entering each layer
         # Dense prefix (NeuroPrefetcher "System Overview": the first d layers
         # keep their MLP fully resident).
         for layer in range(cfg.n_dense):
             g, u, dt = self._dense_rows(layer)
             rec.h_in_dense.append(h.copy())
+            layer_in.append(h.copy())
             yd = np.zeros((B, cfg.d_model))
             for b in range(B):
                 yd[b], _ = ffn_rows(g, u, dt, rmsnorm(h[b]), cfg.activation)
@@ -365,11 +396,12 @@ class OracleDecoder:
         # Sparse suffix.
         for s in range(cfg.n_sparse):
             layer = cfg.n_dense + s
+            layer_in.append(h.copy())
             if cfg.pred_kind == "shared_argmax":
                 active = self._active_from_ids(s, layer, rec.ids)
             else:
                 w1, w2, b2 = self._pred(layer)
-                xs = rmsnorm(h[0])
+                xs = rmsnorm(layer_in[predictor_source_layer(layer, cfg.lookahead)][0])
                 lg = predictor_logits(w1, w2, b2, xs)
                 rec.pred_xhat.append(xs)
                 rec.pred_logits_layer.append(lg)
@@ -385,6 +417,9 @@ class OracleDecoder:
                     self.last_seen[s][n] = self.t
                 nxt = window_resident(prev, active, self.last_seen[s], self.t,
                                       cfg.window, cfg.k_max)
+            elif cfg.residency == "frequency":
+                self.count[s][active] += 1
+                nxt = frequency_resident(prev, active, self.count[s], cfg.k_max)
             else:
                 nxt = active
             d_in, d_out = set_delta(active, prev, nxt)

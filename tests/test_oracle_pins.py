@@ -582,3 +582,59 @@ def test_compact_window_ffn_covers_occupied_rows():
                                           for p in range(2)], xs)[0]
             assert np.allclose(rb.y[s][0], y_a + y_extra, rtol=1e-10, atol=1e-13)
     assert seen_extra > 0
+
+
+def test_frequency_resident_hand_worked():
+    # K = 4; previous residents 1, 2, 3, 5; active now 7, 9; counts: 1 -> 5,
+    # 2 -> 1, 3 -> 1, 5 -> 2.  Six candidates, two go: the least frequent (2 and
+    # 3, count 1, tie by ascending ID: 2 first, then 3)
+    cnt = np.zeros(16, dtype=np.int64)
+    cnt[[1, 2, 3, 5, 7, 9]] = [5, 1, 1, 2, 1, 1]
+    assert oracle.frequency_resident([1, 2, 3, 5], [7, 9], cnt, 4) == [1, 5, 7, 9]
+    assert oracle.frequency_resident([1, 2, 3, 5], [7, 9], cnt, 5) == [1, 3, 5, 7, 9]
+    # active neurons stay even when rarer than every other resident
+    assert oracle.frequency_resident([1, 5], [2, 3], cnt, 2) == [2, 3]
+    assert oracle.frequency_resident([], [4], cnt, 2) == [4]
+
+
+def test_frequency_resident_characterised():
+    # the result is the unique set with A <= R <= A | R_prev, |R| = min(K, |A | R_prev|),
+    # and every kept non-active neuron ranks above every dropped one by (count, ID)
+    rng = random.Random(5)
+    for _ in range(400):
+        F = rng.randint(1, 40)
+        K = rng.randint(1, F)
+        act = sorted(rng.sample(range(F), rng.randint(0, K)))
+        prev = sorted(rng.sample(range(F), rng.randint(0, K)))
+        cnt = np.array([rng.randint(0, 3) for _ in range(F)])
+        R = oracle.frequency_resident(prev, act, cnt, K)
+        U = set(act) | set(prev)
+        assert set(act) <= set(R) <= U and len(R) == min(K, len(U)) and R == sorted(R)
+        kept = [n for n in R if n not in act]
+        dropped = [n for n in U if n not in R]
+        for x in kept:
+            for y in dropped:
+                assert (cnt[x], x) > (cnt[y], y)
+
+
+def test_lookahead_source_is_an_earlier_layer():
+    # the per-layer predictor of layer l reads the input of layer max(l - k, 0):
+    # changing the FFN weights of layers >= l - k leaves layer l's active set
+    # unchanged, changing an earlier layer's weights changes it
+    base = SMALL_OPT.replace(n_layers=5, window=1, residency="slotmap")
+    for k in (0, 1, 2, 9):
+        cfg = base.replace(lookahead=k)
+        wl = make_workload(cfg)
+        ref = OracleDecoder(wl, materialize_buffers=False).step(wl.x[0].numpy())
+        for m in range(cfg.n_layers):
+            wl2 = make_workload(cfg)
+            wl2.store[m].mul_(1.7)      # FFN rows of layer m only
+            rec = OracleDecoder(wl2, materialize_buffers=False).step(wl2.x[0].numpy())
+            for l in range(cfg.n_layers):
+                src = oracle.predictor_source_layer(l, k)
+                same = rec.active[l] == ref.active[l]
+                if m >= src:
+                    assert same, (k, m, l)
+                elif m == src - 1:
+                    assert not same, (k, m, l)
+    assert [oracle.predictor_source_layer(l, 2) for l in range(5)] == [0, 0, 0, 1, 2]

@@ -62,8 +62,9 @@ class Config:
     has_gate: bool = True    # False: OPT-style records (up | down^T)
     activation: str = "relu"  # gated FFN: 'relu' (ReLU-fied) or 'swiglu' (silu gate)
     combine: str = "union"   # 'union' | 'intersect' of the gate and up masks
-    residency: str = "slotmap"  # 'slotmap' | 'window'
+    residency: str = "slotmap"  # 'slotmap' | 'window' | 'frequency'
     window: int = 5          # W tokens (window residency)
+    lookahead: int = 0       # per-layer predictor of layer l reads the input of layer max(l - k, 0)
     slots: str = "reuse"     # 'reuse' free slots, or 'compact' (swap-with-last + append)
     batch: int = 1           # sequences decoded together
     weight_std: float = 0.02
