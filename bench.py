@@ -59,6 +59,10 @@ def parse():
     p.add_argument("--h2d-mode", default="fused", choices=["staged", "fused"])
     p.add_argument("--slots", default=None, choices=["reuse", "compact"],
                    help="placement of resident rows (default: the workload's)")
+    p.add_argument("--residency", default=None, choices=["slotmap", "window", "frequency"],
+                   help="residency policy (default: the workload's)")
+    p.add_argument("--lookahead", type=int, default=None,
+                   help="per-layer predictor: predict layer l from the input of layer l - k")
     p.add_argument("--cpu-sample-tokens", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -300,6 +304,10 @@ def run_cuda(args):
         base = base.replace(persistence=args.persistence)
     if args.slots is not None:
         base = base.replace(slots=args.slots)
+    if args.residency is not None:
+        base = base.replace(residency=args.residency)
+    if args.lookahead is not None:
+        base = base.replace(lookahead=args.lookahead)
     span = (base.batch - 1) * base.phase_step + 24
     T = min(W + 3 * K, base.n_centroids - span if base.n_centroids else 10 ** 9)
     cfg = base.replace(n_warm=0, n_decode=T, seed=base.seed + 7919 * rank)
@@ -444,7 +452,8 @@ def run_cuda(args):
                    "d_model": cfg.d_model, "d_ff": cfg.d_ff, "k_max": cfg.k_max, "centroids": cfg.n_centroids,
                    "combine": cfg.combine, "persistence": cfg.persistence, "batch": cfg.batch,
                    "density": cfg.density, "ffn": "tcgen05 tensor cores" if cfg.batch > 1 else "CUDA cores",
-                   "h2d_mode": args.h2d_mode, "slots": cfg.slots, "parallelism": f"replicas x{world}",
+                   "h2d_mode": args.h2d_mode, "slots": cfg.slots, "residency": cfg.residency,
+                   "lookahead": cfg.lookahead, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (per-token weights ~2 GB > 129 MB)"},
         "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": table,
         "h2d_peak_gbs": round(h2d_peak, 1), "h2d_peak_after_gbs": round(h2d_after, 1), "host_link_busy_ms_per_token": round(link_ms / KP, 4),

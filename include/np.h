@@ -64,9 +64,13 @@ typedef int32_t np_status;
 
 /* residency policy: slot map with resident set = active set (NeuroPrefetcher
  * full text, delta runtime), or the last `window` tokens' active sets (LLM in
- * a flash, section 3.1 Windowing) */
+ * a flash, section 3.1 Windowing), or frequency-weighted caching (DynamicInfer,
+ * hierarchical neuron cache, importance a + lambda f): the active set plus
+ * the previous residents, the non-active ones active in the fewest tokens of
+ * the sequence evicted first (ties: lowest ID) while more than k_max remain */
 #define NP_RES_SLOTMAP 0
 #define NP_RES_WINDOW 1
+#define NP_RES_FREQUENCY 2
 
 /* predictor: one shared predictor after layer 0 with a per-head argmax over
  * the centroid vocabulary (NeuroPrefetcher section 3.3), or one low-rank
@@ -127,8 +131,13 @@ typedef struct {
   int32_t pred_kind;    /* NP_PRED_* */
   int32_t h2d_mode;     /* NP_H2D_* */
   int32_t activation;   /* NP_ACT_* (NP_ACT_SWIGLU needs has_gate = 1) */
-  int32_t slots;        /* NP_SLOTS_* (batch > 1 with NP_RES_WINDOW needs
-                           NP_SLOTS_COMPACT) */
+  int32_t slots;        /* NP_SLOTS_* (batch > 1 with NP_RES_WINDOW or
+                           NP_RES_FREQUENCY needs NP_SLOTS_COMPACT) */
+  int32_t lookahead;    /* per-layer predictor only: the predictor of layer l
+                           reads the input of layer max(l - lookahead, 0)
+                           (DynamicInfer, cross-layer sparse prediction), so
+                           np_decode_token starts layer l's reads `lookahead`
+                           layers early; 0..n_layers, 0 = its own input */
   /* Host weight store (caller-owned, CPU memory the device can read; e.g.
    * registered with np_host_register).  Layout: record-major per sparse
    * layer, [L-d][F][n_proj][D] elements of `dtype`, n_proj = 3 (gate, up,

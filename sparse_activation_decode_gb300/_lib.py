@@ -10,7 +10,7 @@ LIB_PATH = os.path.join(HERE, "libnp.so")
 NP_OK, NP_ERR_ARG, NP_ERR_OOM, NP_ERR_CUDA, NP_ERR_IO, NP_ERR_TIMEOUT, NP_ERR_STATE = 0, -1, -2, -3, -4, -5, -6
 NP_F32, NP_F16, NP_BF16 = 0, 1, 2
 NP_COMBINE_INTERSECT, NP_COMBINE_UNION = 0, 1
-NP_RES_SLOTMAP, NP_RES_WINDOW = 0, 1
+NP_RES_SLOTMAP, NP_RES_WINDOW, NP_RES_FREQUENCY = 0, 1, 2
 NP_PRED_SHARED_ARGMAX, NP_PRED_PERLAYER_SIGMOID = 0, 1
 NP_H2D_STAGED, NP_H2D_FUSED = 0, 1
 NP_SLOTS_REUSE, NP_SLOTS_COMPACT = 0, 1
@@ -27,7 +27,7 @@ class ModelDesc(ctypes.Structure):
         ("dtype", ctypes.c_int32), ("has_gate", ctypes.c_int32), ("combine", ctypes.c_int32),
         ("residency", ctypes.c_int32), ("window", ctypes.c_int32), ("batch", ctypes.c_int32),
         ("staging_rows", ctypes.c_int32), ("pred_hidden", ctypes.c_int32), ("pred_kind", ctypes.c_int32),
-        ("h2d_mode", ctypes.c_int32), ("activation", ctypes.c_int32), ("slots", ctypes.c_int32),
+        ("h2d_mode", ctypes.c_int32), ("activation", ctypes.c_int32), ("slots", ctypes.c_int32), ("lookahead", ctypes.c_int32),
         ("host_store", ctypes.c_void_p), ("dense_w", ctypes.c_void_p), ("pred_w1", ctypes.c_void_p),
         ("pred_w2", ctypes.c_void_p), ("pred_b2", ctypes.c_void_p), ("centroids", ctypes.c_void_p),
         ("main_stream", ctypes.c_void_p), ("side_stream", ctypes.c_void_p),

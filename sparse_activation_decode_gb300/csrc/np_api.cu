@@ -66,6 +66,8 @@ struct np_model {
   np_model_desc d{};
   int L = 0, dn = 0, S = 0, D = 0, F = 0, K = 0, C = 0, W = 0, B = 1, H = 0, NH = 0;
   int nproj = 3, esz = 2, staging_rows = 0, window = 1;
+  int frequency = 0;  // frequency-weighted residency: last_seen holds activation counts
+  int lookahead = 0;  // per-layer predictor of layer l reads the input of layer max(l - k, 0)
   int sms = 0;
   size_t smem_optin = 0;
   size_t row_bytes = 0, rec_bytes = 0;
@@ -531,6 +533,7 @@ SetLaunch set_args(np_model* m, int first_sparse, int n_layers) {
   a.words = m->W;
   a.combine = m->d.combine;
   a.window = m->window;
+  a.frequency = m->frequency;
   a.batch = m->B;
   a.n_heads = m->NH;
   a.token = (int)m->token;
@@ -685,7 +688,11 @@ static np_status validate(const np_model_desc* d) {
   if (d->k_max < 1 || d->k_max > d->d_ff || d->k_max > 8192) return arg_fail("k_max must be in [1, min(d_ff, 8192)]");
   if (d->has_gate != 0 && d->has_gate != 1) return arg_fail("has_gate must be 0 or 1");
   if (d->combine != NP_COMBINE_INTERSECT && d->combine != NP_COMBINE_UNION) return arg_fail("bad combine");
-  if (d->residency != NP_RES_SLOTMAP && d->residency != NP_RES_WINDOW) return arg_fail("bad residency");
+  if (d->residency != NP_RES_SLOTMAP && d->residency != NP_RES_WINDOW && d->residency != NP_RES_FREQUENCY)
+    return arg_fail("bad residency");
+  if (d->lookahead < 0 || d->lookahead > d->n_layers) return arg_fail("lookahead must be in [0, n_layers]");
+  if (d->lookahead > 0 && d->pred_kind != NP_PRED_PERLAYER_SIGMOID)
+    return arg_fail("lookahead applies to the per-layer predictor");
   if (d->residency == NP_RES_WINDOW && (d->window < 1 || d->window > 32)) return arg_fail("window must be 1..32");
   if (d->batch < 1 || d->batch > 8) return arg_fail("batch must be in 1..8");
   if (d->batch > 1) {
@@ -699,8 +706,9 @@ static np_status validate(const np_model_desc* d) {
   if (d->activation != NP_ACT_RELU && d->activation != NP_ACT_SWIGLU) return arg_fail("bad activation");
   if (d->activation == NP_ACT_SWIGLU && !d->has_gate) return arg_fail("SwiGLU needs a gate projection");
   if (d->slots != NP_SLOTS_REUSE && d->slots != NP_SLOTS_COMPACT) return arg_fail("bad slots");
-  if (d->batch > 1 && d->residency == NP_RES_WINDOW && d->slots != NP_SLOTS_COMPACT)
-    return arg_fail("batched decoding with windowing needs the compact placement (its FFN covers the occupied rows)");
+  if (d->batch > 1 && d->residency != NP_RES_SLOTMAP && d->slots != NP_SLOTS_COMPACT)
+    return arg_fail("batched decoding with a window or frequency residency needs the compact placement (its FFN "
+                    "covers the occupied rows)");
   if (d->pred_hidden < 1 || (d->pred_hidden * esz) % 16 != 0 ||
       d->pred_hidden / (16 / esz) > kThreads * kMaxChunksPerThread)
     return arg_fail("pred_hidden must be positive, rows a multiple of 16 bytes, <= 8192");
@@ -745,6 +753,8 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   m->staging_rows = desc->staging_rows > 0 ? desc->staging_rows : m->K;
   m->window = desc->residency == NP_RES_WINDOW ? desc->window : 1;
   m->compact = desc->slots == NP_SLOTS_COMPACT;
+  m->frequency = desc->residency == NP_RES_FREQUENCY;
+  m->lookahead = desc->lookahead;
   m->row_bytes = (size_t)m->D * m->esz;
   m->rec_bytes = m->nproj * m->row_bytes;
   m->main = static_cast<cudaStream_t>(desc->main_stream);
@@ -829,7 +839,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if ((st = dev_alloc(m, &m->inv, Sa * K, 0xff)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->content, Sa * K, 0xff)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->resbits, Sa * m->W)) != NP_OK) return fail(st);
-  if (m->window > 1 && (st = dev_alloc(m, &m->last_seen, Sa * F)) != NP_OK) return fail(st);
+  if ((m->window > 1 || m->frequency) && (st = dev_alloc(m, &m->last_seen, Sa * F)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->counts, Sa * 4)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->active, Sa * K)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->active_slot, Sa * K)) != NP_OK) return fail(st);
@@ -961,7 +971,8 @@ np_status np_reset_sequence(np_model* m) {
   cudaStream_t st = m->main;
   NP_TRY(join_side(m, st));
   return launch(m, NP_KIND_SET, st, 0, [&] {
-    return launch_reset_state(m->slotmap, m->inv, m->resbits, m->slot_hw, m->S, m->F, m->K, m->W, st);
+    return launch_reset_state(m->slotmap, m->inv, m->resbits, m->slot_hw, m->frequency ? m->last_seen : nullptr, m->S,
+                              m->F, m->K, m->W, st);
   });
 }
 
@@ -1190,11 +1201,19 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
     }
     fin = m->fs;
   } else {
-    for (int l = 0; l < m->dn; ++l) NP_TRY(ffn_layer(m->main, l));
-    for (int s = 0; s < m->S; ++s) {
-      const int l = m->dn + s;
-      if (!shared) {
-        NP_TRY(enqueue_predict(m, l, base_of(l), true, l == 0 ? nullptr : chain_y(m, l - 1)));
+    // Per-layer predictor: the prediction, delta and reads of sparse layer j
+    // are enqueued once the input of layer max(j - k, 0) is final, i.e. just
+    // before that layer's FFN, so with a lookahead k > 0 the reads of layer
+    // j run on the gather streams during the FFNs of layers j - k .. j - 1.
+    // (A model with the shared predictor gets here only without sparse layers.)
+    const int k = m->lookahead;
+    int next = m->dn;  // next sparse layer to predict
+    for (int l = 0; l < m->L; ++l) {
+      const int upto = l == 0 ? k : l + k;  // layers whose predictor reads the input of layer l
+      for (; !shared && next < m->L && next <= upto; ++next) {
+        const int s = next - m->dn;
+        const int src = next - k > 0 ? next - k : 0;
+        NP_TRY(enqueue_predict(m, next, base_of(src), true, src == 0 ? nullptr : chain_y(m, src - 1)));
         NP_TRY(enqueue_set(m, s, 1, nullptr, m->fire));
         m->pending_bits |= 1ull << s;
         size_t n_moved = 0;
@@ -1208,7 +1227,7 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
           return rs;
         }
       }
-      CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_layer[s], 0));
+      if (l >= m->dn) CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_layer[l - m->dn], 0));
       NP_TRY(ffn_layer(m->main, l));
     }
   }

@@ -107,7 +107,8 @@ struct SetLaunch {
   int n_dense;            // absolute layer of sparse index 0
   int F, K, C, words;
   int combine;            // 0 intersect, 1 union
-  int window;             // 1 = slot-map policy (R = A)
+  int window;             // > 1: window residency over the last `window` tokens
+  int frequency;          // 1: frequency-weighted residency (last_seen holds activation counts)
   int batch;
   int n_heads;
   int token;
@@ -121,7 +122,7 @@ struct SetLaunch {
   int* inv;               // [S][K] neuron in each slot or -1
   int* content;           // [S][K] neuron whose rows the slot's bytes hold or -1
   uint32_t* resbits;      // [S][words] resident set
-  int* last_seen;         // [S][F] last active token (window > 1)
+  int* last_seen;         // [S][F] last active token (window > 1) or activation count (frequency)
   int S;
   // delta lists [S][...]
   int* counts;            // [S][4]
@@ -147,8 +148,10 @@ struct SetLaunch {
 };
 cudaError_t launch_set(const SetLaunch& a, cudaStream_t st);
 cudaError_t launch_rollback(const SetLaunch& a, cudaStream_t st);  // undo launch_set from its lists
-cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int* slot_hw, int S, int F, int K,
-                               int words, cudaStream_t st);
+// Cold state: empty maps and resident sets, zero high-water marks and (if
+// given) zero activation counts [S][F].
+cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int* slot_hw, int* counts, int S, int F,
+                               int K, int words, cudaStream_t st);
 
 // ---- host-link gather and deinterleave-scatter (np_scatter.cu) -----------
 struct MoveLaunch {

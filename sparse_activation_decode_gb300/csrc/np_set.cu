@@ -11,7 +11,11 @@
 //  3. Resident set: R_next = A (slot map, NeuroPrefetcher full text delta
 //     runtime), or with windowing (LLM in a flash 3.1) the neurons of R_prev
 //     still used within the last W tokens plus A, evicting the oldest last
-//     use first (ties: lowest ID first) while more than K_max remain.
+//     use first (ties: lowest ID first) while more than K_max remain, or
+//     with frequency-weighted caching (DynamicInfer, importance a + lambda f)
+//     R_prev plus A, evicting the non-active neurons active in the fewest
+//     tokens of the sequence first (ties: lowest ID first) while more than
+//     K_max remain.
 //  4. D_in = A \ R_prev, D_out = R_prev \ R_next.  Slot reuse: slots of
 //     R_prev ∩ R_next stay; the free slots in ascending order go to D_in in
 //     ascending ID order.  Compact placement (LLM in a flash 3.3): the rows
@@ -149,7 +153,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   __shared__ int wsum[32];
   __shared__ uint32_t occ[kMaxKmax / 32];
   __shared__ uint32_t s_hole[kMaxKmax / 32], s_mov[kMaxKmax / 32];  // compact: slots to refill / to move
-  __shared__ int hist[33];
+  __shared__ int hist[256];
   __shared__ int cut_age, cut_need, s_hw, s_nfree;
   __shared__ uint32_t s_a[kMaxWords], s_out[kMaxWords], s_keep[kMaxWords];
   __shared__ int s_ea[kMaxWords], s_eout[kMaxWords];
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   int* __restrict__ inv = a.inv + (size_t)s * K;
   int* __restrict__ ct = a.content + (size_t)s * K;
   uint32_t* __restrict__ res = a.resbits + (size_t)s * W;
-  int* __restrict__ ls = a.window > 1 ? a.last_seen + (size_t)s * F : nullptr;
+  int* __restrict__ ls = (a.window > 1 || a.frequency) ? a.last_seen + (size_t)s * F : nullptr;
   int* __restrict__ out_a = a.active + (size_t)s * K;
   int* __restrict__ out_as = a.active_slot + (size_t)s * K;
   int* __restrict__ out_in = a.din_n + (size_t)s * K;
@@ -269,6 +273,51 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
       cand &= ~(older | evict_b);
     }
     nw = cand;
+  } else if (a.frequency) {
+    uint32_t old = rw & ~aw;  // resident, not active now
+    int ctot;
+    (void)block_scan(__popc(aw | old), wsum, &ctot);
+    if (ctot > K) {
+      // the (ctot - K) smallest (count, ID) among `old`: radix selection of
+      // the count (saturated to 16 bits) in two 8-bit passes, then the
+      // lowest IDs of the boundary count
+      int need = ctot - K, prefix = 0;
+      for (int pass = 0; pass < 2; ++pass) {
+        if (tid < 256) hist[tid] = 0;
+        __syncthreads();
+        for (uint32_t w = old; w;) {
+          const int b = __ffs(w) - 1;
+          w &= w - 1;
+          const int key = min(ls[i * 32 + b], 65535);
+          if (pass == 0) atomicAdd(&hist[key >> 8], 1);
+          else if ((key >> 8) == prefix) atomicAdd(&hist[key & 255], 1);
+        }
+        __syncthreads();
+        if (tid == 0) {
+          int d = 0;
+          while (d < 255 && hist[d] < need) need -= hist[d++];
+          cut_age = d;
+          cut_need = need;
+        }
+        __syncthreads();
+        prefix = pass == 0 ? cut_age : (prefix << 8) | cut_age;
+        need = cut_need;
+      }
+      uint32_t bucket = 0, lower = 0;
+      for (uint32_t w = old; w;) {
+        const int b = __ffs(w) - 1;
+        w &= w - 1;
+        const int key = min(ls[i * 32 + b], 65535);
+        if (key < prefix) lower |= 1u << b;
+        else if (key == prefix) bucket |= 1u << b;
+      }
+      int btot;
+      const int bexcl = block_scan(__popc(bucket), wsum, &btot);
+      uint32_t evict_b = 0;
+      if (bexcl < need) evict_b = lowest_bits(bucket, need - bexcl);
+      old &= ~(lower | evict_b);
+    }
+    nw = aw | old;
   }
   const uint32_t dinw = aw & ~rw;
   const uint32_t doutw = rw & ~nw;
@@ -373,7 +422,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     for (int r = tid; r < n_a; r += kSetThreads) {
       const int n = out_a[r];
       out_lsold[r] = ls[n];
-      ls[n] = a.token;
+      ls[n] = a.frequency ? ls[n] + 1 : a.token;
     }
   if (tid == 0) {
     int* c = a.counts + (size_t)s * 4;
@@ -398,7 +447,7 @@ __global__ void __launch_bounds__(kSetThreads) rollback_kernel(SetLaunch a) {
   int* inv = a.inv + (size_t)s * K;
   int* ct = a.content + (size_t)s * K;
   uint32_t* res = a.resbits + (size_t)s * W;
-  int* ls = a.window > 1 ? a.last_seen + (size_t)s * F : nullptr;
+  int* ls = (a.window > 1 || a.frequency) ? a.last_seen + (size_t)s * F : nullptr;
   const int* c = a.counts + (size_t)s * 4;
   const int n_a = c[0], n_in = c[1], n_out = c[2];
   const int* din = a.din_n + (size_t)s * K;
@@ -461,9 +510,11 @@ __global__ void __launch_bounds__(kSetThreads) rollback_kernel(SetLaunch a) {
   }
 }
 
-__global__ void reset_state_kernel(int* slotmap, int* inv, uint32_t* resbits, int* slot_hw, int n_layers,
-                                   size_t n_sm, size_t n_inv, size_t n_res) {
+__global__ void reset_state_kernel(int* slotmap, int* inv, uint32_t* resbits, int* slot_hw, int* counts,
+                                   int n_layers, size_t n_sm, size_t n_inv, size_t n_res) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
+  if (counts)
+    for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n_sm; k += stride) counts[k] = 0;
   if (slot_hw && blockIdx.x == 0)
     for (int s = threadIdx.x; s < n_layers; s += blockDim.x) slot_hw[s] = 0;
   for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n_sm; k += stride) slotmap[k] = -1;
@@ -485,9 +536,9 @@ cudaError_t launch_rollback(const SetLaunch& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int* slot_hw, int S, int F, int K,
-                               int words, cudaStream_t st) {
-  reset_state_kernel<<<256, 256, 0, st>>>(slotmap, inv, resbits, slot_hw, S, (size_t)S * F, (size_t)S * K,
+cudaError_t launch_reset_state(int* slotmap, int* inv, uint32_t* resbits, int* slot_hw, int* counts, int S, int F,
+                               int K, int words, cudaStream_t st) {
+  reset_state_kernel<<<256, 256, 0, st>>>(slotmap, inv, resbits, slot_hw, counts, S, (size_t)S * F, (size_t)S * K,
                                           (size_t)S * words);
   return cudaGetLastError();
 }

@@ -45,7 +45,7 @@ class SparseDecoder:
                  pred_hidden: int, pred_kind: str = "shared_argmax", has_gate: bool = True,
                  combine: str = "union", residency: str = "slotmap", window: int = 1, batch: int = 1,
                  staging_rows: int = 0, h2d_mode: str = "fused", activation: str = "relu",
-                 slots: str = "reuse",
+                 slots: str = "reuse", lookahead: int = 0,
                  main_stream: torch.cuda.Stream | None = None, side_stream: torch.cuda.Stream | None = None,
                  read_hook=None):
         self.lib = L.load()
@@ -70,7 +70,9 @@ class SparseDecoder:
         d.k_max, d.n_centroids, d.dtype = k_max, n_centroids, _DTYPES[dtype]
         d.has_gate = int(has_gate)
         d.combine = {"intersect": L.NP_COMBINE_INTERSECT, "union": L.NP_COMBINE_UNION}[combine]
-        d.residency = {"slotmap": L.NP_RES_SLOTMAP, "window": L.NP_RES_WINDOW}[residency]
+        d.residency = {"slotmap": L.NP_RES_SLOTMAP, "window": L.NP_RES_WINDOW,
+                       "frequency": L.NP_RES_FREQUENCY}[residency]
+        d.lookahead = lookahead
         d.window, d.batch, d.staging_rows, d.pred_hidden = window, batch, staging_rows, pred_hidden
         d.activation = {"relu": 0, "swiglu": 1}[activation]
         d.slots = {"reuse": L.NP_SLOTS_REUSE, "compact": L.NP_SLOTS_COMPACT}[slots]
@@ -278,7 +280,7 @@ def decoder_for(wl, *, h2d_mode: str = "fused", staging_rows: int | None = None,
         pred_kind=cfg.pred_kind, has_gate=cfg.has_gate, combine=cfg.combine, residency=cfg.residency,
         window=cfg.window if cfg.residency == "window" else 1, batch=cfg.batch,
         staging_rows=cfg.staging_rows if staging_rows is None else staging_rows, h2d_mode=h2d_mode,
-        activation=cfg.activation, slots=cfg.slots,
+        activation=cfg.activation, slots=cfg.slots, lookahead=cfg.lookahead,
         read_hook=read_hook, **kw)
 
 
