@@ -131,22 +131,26 @@ __device__ __forceinline__ void load_x(const float* __restrict__ h_in, const flo
   for (int k = 0; k < MAXC; ++k) {
     const int c = tid + k * NT;
 #pragma unroll
-    for (int q = 0; q < P; ++q) {
-      float2 v = make_float2(0.f, 0.f);
+    for (int q = 0; q < P; q += 2) {  // 16-byte loads: two pairs at a time
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (c < NC) {
-        v = *reinterpret_cast<const float2*>(h_in + c * E + 2 * q);
+        v = *reinterpret_cast<const float4*>(h_in + c * E + 2 * q);
         if (yprev) {
-          const float2 w = *reinterpret_cast<const float2*>(yprev + c * E + 2 * q);
+          const float4 w = *reinterpret_cast<const float4*>(yprev + c * E + 2 * q);
           v.x += w.x;
           v.y += w.y;
+          v.z += w.z;
+          v.w += w.w;
         }
         if (writer) {
-          if (hb_out) *reinterpret_cast<float2*>(hb_out + c * E + 2 * q) = v;
-          if (y_zero) *reinterpret_cast<float2*>(y_zero + c * E + 2 * q) = make_float2(0.f, 0.f);
+          if (hb_out) *reinterpret_cast<float4*>(hb_out + c * E + 2 * q) = v;
+          if (y_zero) *reinterpret_cast<float4*>(y_zero + c * E + 2 * q) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      xr[k][q] = v;
+      xr[k][q] = make_float2(v.x, v.y);
+      xr[k][q + 1] = make_float2(v.z, v.w);
       ss = fmaf(v.x, v.x, fmaf(v.y, v.y, ss));
+      ss = fmaf(v.z, v.z, fmaf(v.w, v.w, ss));
     }
   }
   ss = warp_sum(ss);
@@ -281,10 +285,14 @@ __device__ __forceinline__ bool consume_group(const uint4* __restrict__ sm4, con
 // right away (one arrive per warp on each slot's `empty` barrier), so the
 // producer refills them while this group's reduction and down projection
 // run.
+//
+// Each row's slot is waited for, read and released on its own (per warp), so
+// a slot goes back to the producer as soon as its row is in registers.
 template <typename T, bool GATED, int MAXC, int NT, int GR>
 __device__ __forceinline__ bool consume_group_early(const uint4* __restrict__ sm4, const int (&off)[GR],
-                                                    const int (&slot)[GR], uint64_t* empty, int nrow, bool ok,
-                                                    int grp, int NC, const float2 (&xr)[MAXC][Pairs<T>::N],
+                                                    const int (&slot)[GR], const uint32_t (&par)[GR],
+                                                    uint64_t* full, uint64_t* empty, int nrow, int* err, int grp,
+                                                    int NC, const float2 (&xr)[MAXC][Pairs<T>::N],
                                                     float2 (&acc)[MAXC][Pairs<T>::N], float* red, bool swiglu) {
   constexpr int P = Pairs<T>::N;
   constexpr int NPROJ = GATED ? 3 : 2;
@@ -292,19 +300,24 @@ __device__ __forceinline__ bool consume_group_early(const uint4* __restrict__ sm
   constexpr int NW = NT / 32;
   static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "values per group must be a power of two");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  bool ok = true;
   uint4 w[GR][NPROJ][MAXC];
 #pragma unroll
-  for (int r = 0; r < GR; ++r)
+  for (int r = 0; r < GR; ++r) {
+    const bool have = r < nrow;
+    if (have) ok = mbar_wait(&full[slot[r]], par[r], err) && ok;
 #pragma unroll
     for (int p = 0; p < NPROJ; ++p)
 #pragma unroll
       for (int k = 0; k < MAXC; ++k) {
         const int c = tid + k * NT;
-        w[r][p][k] = (r < nrow && c < NC) ? sm4[off[r] + p * NC + c] : make_uint4(0u, 0u, 0u, 0u);
+        w[r][p][k] = (have && c < NC) ? sm4[off[r] + p * NC + c] : make_uint4(0u, 0u, 0u, 0u);
       }
-  __syncwarp();
-  if (lane == 0)
-    for (int r = 0; r < nrow; ++r) mbar_arrive(&empty[slot[r]]);
+    if (have) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot[r]]);
+    }
+  }
   float2 d2[NV];
 #pragma unroll
   for (int v = 0; v < NV; ++v) d2[v] = make_float2(0.f, 0.f);
@@ -697,14 +710,14 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
       bool aborted = false;
       for (int jj = 0; jj < my_n; jj += kChainGroup) {
         const int nrow = my_n - jj < kChainGroup ? my_n - jj : kChainGroup;
-        bool ok = true;
         int off[kChainGroup], slot[kChainGroup];
+        uint32_t par[kChainGroup];
 #pragma unroll
         for (int r = 0; r < kChainGroup; ++r) {
           slot[r] = cs;
+          par[r] = cwrap & 1u;
           off[r] = (int)((512 + (size_t)cs * slot_bytes) >> 4);
           if (r < nrow) {
-            ok = mbar_wait(&full[cs], cwrap & 1u, a.err) && ok;
             if (++cs == n_slots) {
               cs = 0;
               ++cwrap;
@@ -712,8 +725,8 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
           }
         }
         if (!consume_group_early<T, GATED, MAXC, kChainThreads, kChainGroup>(
-                reinterpret_cast<const uint4*>(smem), off, slot, empty, nrow, ok, jj / kChainGroup, NC, xr, acc,
-                red, a.swiglu != 0)) {
+                reinterpret_cast<const uint4*>(smem), off, slot, par, full, empty, nrow, a.err, jj / kChainGroup, NC,
+                xr, acc, red, a.swiglu != 0)) {
           aborted = true;
           break;
         }
@@ -736,9 +749,13 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
                   make_float4(acc[k][q].x, acc[k][q].y, acc[k][q + 1].x, acc[k][q + 1].y);
         }
       }
-      __threadfence();
+      // one release per CTA: the barrier orders every thread's stores before
+      // thread 0's fence, which makes them visible before its arrival
       consumer_sync<kChainThreads>();
-      if (tid == 0) atomicAdd(a.arrive + 2 * i, 1u);
+      if (tid == 0) {
+        __threadfence();
+        atomicAdd(a.arrive + 2 * i, 1u);
+      }
       if ((int)blockIdx.x < n_red) {
         bool ok = true;
         if (tid == 0) ok = wait_count(a.arrive + 2 * i, (unsigned)G, a.err);
@@ -752,26 +769,53 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
           // threads (g, f): float4 f of the slice, partials g, g + 64, ...
           const int col = sl * 32 + 4 * f;
           float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (col < D)
-            for (int cta = g; cta < G; cta += kChainThreads / 8) {
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)cta * BD + col));
-              sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+          if (col < D) {
+            // the first three partials of this thread in flight together
+            constexpr int GS = kChainThreads / 8;
+            float4 v[3];
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+              const int cta = g + u * GS;
+              v[u] = cta < G ? __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)cta * BD + col))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+              sum.x += v[u].x; sum.y += v[u].y; sum.z += v[u].z; sum.w += v[u].w;
+            }
+            for (int cta = g + 3 * GS; cta < G; cta += GS) {
+              const float4 w = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)cta * BD + col));
+              sum.x += w.x; sum.y += w.y; sum.z += w.z; sum.w += w.w;
+            }
+          }
           tmp[g * 8 + f] = sum;
           consumer_sync<kChainThreads>();
-          if (tid < 8 && sl * 32 + 4 * tid < D) {
+          if (warp == 0) {
+            // lane (part, f): every fourth group, then the four parts in a
+            // fixed tree (both lanes of a pair get the same, commutative sum)
+            const int f2 = lane & 7, part = lane >> 3;
             float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int gg = 0; gg < kChainThreads / 8; ++gg) {
-              const float4 v = tmp[gg * 8 + tid];
+#pragma unroll 4
+            for (int gg = part; gg < kChainThreads / 8; gg += 4) {
+              const float4 v = tmp[gg * 8 + f2];
               t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
             }
-            *reinterpret_cast<float4*>(yi + sl * 32 + 4 * tid) = t;
+#pragma unroll
+            for (int o = 8; o <= 16; o <<= 1) {
+              t.x += __shfl_xor_sync(0xffffffffu, t.x, o);
+              t.y += __shfl_xor_sync(0xffffffffu, t.y, o);
+              t.z += __shfl_xor_sync(0xffffffffu, t.z, o);
+              t.w += __shfl_xor_sync(0xffffffffu, t.w, o);
+            }
+            if (lane < 8 && sl * 32 + 4 * lane < D) *reinterpret_cast<float4*>(yi + sl * 32 + 4 * lane) = t;
           }
           consumer_sync<kChainThreads>();  // tmp is reused by the next slice
         }
-        __threadfence();
         consumer_sync<kChainThreads>();
-        if (tid == 0) atomicAdd(a.arrive + 2 * i + 1, 1u);
+        if (tid == 0) {
+          __threadfence();
+          atomicAdd(a.arrive + 2 * i + 1, 1u);
+        }
       }
     }
     // the residual stream after the last layer: h = h_last + y_last
