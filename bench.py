@@ -245,11 +245,54 @@ def isolated_kernels(dec, torch, cfg, reps=5):
     return out
 
 
+def scatter_isolated(wl, torch, xs, decoder_for):
+    """The deinterleave-scatter kernel of the staged host-link mode (staging
+    -> projection buffers, device memory only), timed by the library's
+    per-launch events with one layer per np_scatter call so that nothing runs
+    beside it: a cold start (every layer's full set) and a steady-state token.
+    Algorithmic bytes: 2 x records x record bytes (read staging, write the
+    buffers).  Shared-predictor workloads only (the per-layer predictor has
+    no all-layer delta)."""
+    cfg = wl.cfg
+    if cfg.pred_kind != "shared_argmax" or cfg.n_sparse == 0:
+        return None
+    dec = decoder_for(wl, h2d_mode="staged")
+    rec = cfg.n_proj * cfg.d_model * cfg.elem_bytes
+    out = {}
+
+    def one(t, label):
+        h = xs[t].reshape(-1).clone()
+        y = dec.dense_mlp(0, h)
+        ids = dec.predict(h + y)
+        dec.delta(ids, -1)
+        torch.cuda.synchronize()
+        rows = sum(c[1] for c in dec.counts())
+        dec.profile()
+        dec.set_profiling(True)
+        for l in range(cfg.n_dense, cfg.n_layers):
+            dec.scatter(l)
+            torch.cuda.synchronize()
+        p = dec.profile()["scatter"]
+        dec.set_profiling(False)
+        byt = 2 * rows * rec / max(p["launches"], 1)
+        us = 1e3 * p["ms"] / max(p["launches"], 1)
+        g = byt / (us * 1e-6) / 1e9
+        out[label] = {"us_per_launch": round(us, 3), "bytes_per_launch": int(byt), "gbs": round(g, 1)}
+
+    one(0, "full_set")
+    for t in range(1, 8):
+        dec.decode_token(xs[t].clone())
+    one(8, "steady")
+    dec.check_error()
+    dec.close()
+    return out
+
+
 def profile_case(args):
     """Small capture case for ncu: 8-step workload of --config (optionally
-    cut to --layers layers), 3 decoded steps, then standalone calls of every
-    kernel kind: two sparse FFNs, dense layer 0, the chained sparse FFNs,
-    predictor, delta, scatter."""
+    cut to --layers layers, host-link mode --h2d-mode), 3 decoded steps,
+    then standalone calls of every kernel kind: two sparse FFNs, dense layer
+    0, the chained sparse FFNs, predictor, delta, scatter."""
     import torch
     from sparse_activation_decode_gb300 import decoder_for
     from sparse_activation_decode_gb300.build import build
@@ -259,7 +302,7 @@ def profile_case(args):
     if args.layers:
         cfg = cfg.replace(n_layers=args.layers)
     wl = make_workload(cfg, device="cuda")
-    dec = decoder_for(wl)
+    dec = decoder_for(wl, h2d_mode=args.h2d_mode)
     xs = wl.x.cuda()
     for t in range(3):
         dec.decode_token(xs[t].clone())
@@ -401,6 +444,7 @@ def run_cuda(args):
         e2e = {"value": round(world * K * B / (ms_e * 1e-3), 2), "unit": "tok/s",
                "h2d_bytes_per_step": B * D * 4, "d2h_bytes_per_step": B * D * 4}
     dec.close()
+    scat = scatter_isolated(wl, torch, xs, decoder_for) if rank == 0 else None
 
     if rank != 0:
         return None
@@ -440,6 +484,12 @@ def run_cuda(args):
                                     "frac_of_measured_hbm": round(g / peaks["hbm_gbs"], 4),
                                     "frac_of_nominal_8tbs": round(g / 8000.0, 4),
                                     "traffic_per_layer": traffic_for("ffn_chain", cfg.name)}
+    if scat:
+        for lab, v in scat.items():
+            hbm_kernels["scatter_" + lab] = {"isolated_gbs": v["gbs"], "isolated_us_per_launch": v["us_per_launch"],
+                                             "bytes_per_launch": v["bytes_per_launch"],
+                                             "frac_of_measured_hbm": round(v["gbs"] / peaks["hbm_gbs"], 4),
+                                             "note": "staged host-link mode (not the default fused path)"}
     if "predictor" in iso:
         g = iso["predictor"]["gbs"]
         hbm_kernels["predictor"] = {"isolated_gbs": g, "frac_of_measured_hbm": round(g / peaks["hbm_gbs"], 4),

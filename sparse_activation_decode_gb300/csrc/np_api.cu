@@ -156,6 +156,15 @@ np_status dev_alloc(np_model* m, T** p, size_t count, int fill_byte = 0) {
   return NP_OK;
 }
 
+// An empty one-warp kernel (profiling: orders a timing event after the
+// stream's pending waits).
+__global__ void marker_kernel() {}
+
+cudaError_t launch_marker(cudaStream_t st) {
+  marker_kernel<<<1, 32, 0, st>>>();
+  return cudaGetLastError();
+}
+
 np_status prof_begin(np_model* m, int kind, cudaStream_t st, EventPair* ep) {
   (void)kind;
   if (m->prof_free.empty()) {
@@ -166,6 +175,10 @@ np_status prof_begin(np_model* m, int kind, cudaStream_t st, EventPair* ep) {
   }
   *ep = m->prof_free.back();
   m->prof_free.pop_back();
+  // A start event placed right after a wait on another stream's event is
+  // stamped before that wait is satisfied; an empty kernel in front of it
+  // makes the stamp follow everything the launch depends on.
+  CUDA_TRY(launch_marker(st));
   CUDA_TRY(cudaEventRecord(ep->a, st));
   return NP_OK;
 }

@@ -14,7 +14,8 @@
 // limited by per-call overhead, so the read is a gather kernel: one CTA per
 // record, every thread keeping eight 16-byte loads in flight, which
 // saturates the link with a few dozen CTAs.  The scatter kernel works in
-// device memory and is HBM-bound: one CTA per (record, projection row).
+// device memory and is HBM-bound: one warp per (record, projection row), 16
+// loads in flight per lane.
 #include "np_common.cuh"
 #include "np_kernels.h"
 
@@ -34,6 +35,24 @@ __device__ __forceinline__ void copy_vecs(const uint4* __restrict__ src, uint4* 
 #pragma unroll
     for (int u = 0; u < kIlp; ++u) {
       const int j = base + u * kMoveThreads;
+      if (j < n) dst[j] = v[u];
+    }
+  }
+}
+
+// One warp copies n 16-byte vectors, 16 loads in flight per lane.
+constexpr int kWarpIlp = 16;
+__device__ __forceinline__ void warp_copy(const uint4* __restrict__ src, uint4* __restrict__ dst, int n, int lane) {
+  for (int base = lane; base < n; base += 32 * kWarpIlp) {
+    uint4 v[kWarpIlp];
+#pragma unroll
+    for (int u = 0; u < kWarpIlp; ++u) {
+      const int j = base + u * 32;
+      if (j < n) v[u] = src[j];
+    }
+#pragma unroll
+    for (int u = 0; u < kWarpIlp; ++u) {
+      const int j = base + u * 32;
       if (j < n) dst[j] = v[u];
     }
   }
@@ -61,21 +80,22 @@ __global__ void __launch_bounds__(kMoveThreads) gather_kernel(MoveLaunch a) {
   }
 }
 
-// bufs[p][din_s[i]] = staging[i - begin].row[p]: one CTA per (record, row)
+// bufs[p][din_s[i]] = staging[i - begin].row[p]: one warp per (record, row)
 __global__ void __launch_bounds__(kMoveThreads) scatter_kernel(MoveLaunch a) {
   const int end = chunk_end(a);
   const int units = (end - a.chunk_begin) * a.n_proj;
   const uint4* stg = static_cast<const uint4*>(a.staging);
   uint4* bufs = static_cast<uint4*>(a.bufs_layer);
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+  const int lane = threadIdx.x & 31, wpb = kMoveThreads / 32;
+  for (int u = blockIdx.x * wpb + (threadIdx.x >> 5); u < units; u += gridDim.x * wpb) {
     const int r = u / a.n_proj, p = u - r * a.n_proj;
     const int slot = a.din_s[a.chunk_begin + r];
     if ((unsigned)slot >= (unsigned)a.K) {
-      if (threadIdx.x == 0) atomicExch(a.err, kDevErrBounds);
+      if (lane == 0) atomicExch(a.err, kDevErrBounds);
       continue;
     }
-    copy_vecs(stg + (size_t)r * a.rec_vec + (size_t)p * a.row_vec,
-              bufs + ((size_t)p * a.K + slot) * a.row_vec, a.row_vec);
+    warp_copy(stg + (size_t)r * a.rec_vec + (size_t)p * a.row_vec, bufs + ((size_t)p * a.K + slot) * a.row_vec,
+              a.row_vec, lane);
   }
 }
 
@@ -96,7 +116,7 @@ __global__ void __launch_bounds__(kMoveThreads) fused_kernel(MoveLaunch a) {
   }
 }
 
-// Compact placement: bufs[p][mv_dst[i]] = bufs[p][mv_src[i]], one CTA per
+// Compact placement: bufs[p][mv_dst[i]] = bufs[p][mv_src[i]], one warp per
 // (move, projection row).  Sources lie at or above the region's new end and
 // targets below it, so no copy reads a row another one writes.
 __global__ void __launch_bounds__(kMoveThreads) move_rows_kernel(MoveLaunch a) {
@@ -104,14 +124,16 @@ __global__ void __launch_bounds__(kMoveThreads) move_rows_kernel(MoveLaunch a) {
   if (cnt > a.K) cnt = a.K;
   const int units = cnt * a.n_proj;
   uint4* bufs = static_cast<uint4*>(a.bufs_layer);
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+  const int lane = threadIdx.x & 31, wpb = kMoveThreads / 32;
+  for (int u = blockIdx.x * wpb + (threadIdx.x >> 5); u < units; u += gridDim.x * wpb) {
     const int i = u / a.n_proj, p = u - i * a.n_proj;
     const int src = a.mv_src[i], dst = a.mv_dst[i];
     if ((unsigned)src >= (unsigned)a.K || (unsigned)dst >= (unsigned)a.K) {
-      if (threadIdx.x == 0) atomicExch(a.err, kDevErrBounds);
+      if (lane == 0) atomicExch(a.err, kDevErrBounds);
       continue;
     }
-    copy_vecs(bufs + ((size_t)p * a.K + src) * a.row_vec, bufs + ((size_t)p * a.K + dst) * a.row_vec, a.row_vec);
+    warp_copy(bufs + ((size_t)p * a.K + src) * a.row_vec, bufs + ((size_t)p * a.K + dst) * a.row_vec, a.row_vec,
+              lane);
   }
 }
 
