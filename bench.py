@@ -35,7 +35,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # (profiles/*.md), keyed by (kind, workload); valid only while the kernel's
 # source file still has the recorded hash.
 NCU_TRAFFIC = {
-    ("gather", "llama2-7b-relu"): {"src": "np_scatter.cu", "src_hash": "785fcdae10bbda3b", "bytes_per_launch": 7552},
+    ("gather", "llama2-7b-relu"): {"src": "np_scatter.cu", "src_hash": "92078b0e6f793061", "bytes_per_launch": 113408},
     ("ffn", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "b519a23ae1071319", "bytes_per_launch": 50407040},
     ("dense", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "b519a23ae1071319", "bytes_per_launch": 273550080},
     # one persistent launch over the 31 sparse layers, per layer
@@ -268,7 +268,7 @@ def scatter_isolated(wl, torch, xs, decoder_for):
         torch.cuda.synchronize()
         rows = sum(c[1] for c in dec.counts())
         dec.profile()
-        dec.set_profiling(True)
+        dec.set_profiling(True, exact=True)
         for l in range(cfg.n_dense, cfg.n_layers):
             dec.scatter(l)
             torch.cuda.synchronize()

@@ -289,7 +289,12 @@ np_status np_check_error(np_model* m);
 
 /* Per-kernel timing with CUDA events recorded on each kernel's own stream.
  * When enabled, every launch of the kinds below is bracketed by events and
- * the summed durations are available from np_get_profile (synchronous). */
+ * the summed durations are available from np_get_profile (synchronous).
+ * enable = 1: plain events; a launch that waits on another stream may be
+ * stamped as starting before its wait is over (an upper bound of its
+ * duration).  enable = 2: an empty kernel is launched in front of each start
+ * event so that it follows the launch's dependencies (exact durations, one
+ * extra launch per kernel).  0 turns timing off. */
 #define NP_KIND_DENSE 0
 #define NP_KIND_PRED 1
 #define NP_KIND_SET 2

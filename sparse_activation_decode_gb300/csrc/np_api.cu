@@ -120,6 +120,7 @@ struct np_model {
   std::vector<cudaEvent_t> ev_g, ev_layer;  // per sparse layer: gathered, ready
   // profiling
   bool prof = false;
+  bool prof_markers = false;  // an empty kernel before each start event
   std::vector<EventPair> prof_free;
   double prof_ms[NP_N_KINDS] = {};
   int64_t prof_launches[NP_N_KINDS] = {};
@@ -178,7 +179,7 @@ np_status prof_begin(np_model* m, int kind, cudaStream_t st, EventPair* ep) {
   // A start event placed right after a wait on another stream's event is
   // stamped before that wait is satisfied; an empty kernel in front of it
   // makes the stamp follow everything the launch depends on.
-  CUDA_TRY(launch_marker(st));
+  if (m->prof_markers) CUDA_TRY(launch_marker(st));
   CUDA_TRY(cudaEventRecord(ep->a, st));
   return NP_OK;
 }
@@ -1323,7 +1324,9 @@ np_status np_check_error(np_model* m) {
 
 np_status np_set_profiling(np_model* m, int32_t enable) {
   if (!m) return arg_fail("model is null");
+  if (enable < 0 || enable > 2) return arg_fail("profiling mode must be 0, 1 or 2");
   m->prof = enable != 0;
+  m->prof_markers = enable == 2;
   return NP_OK;
 }
 

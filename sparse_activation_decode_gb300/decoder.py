@@ -234,8 +234,10 @@ class SparseDecoder:
     def check_error(self) -> None:
         L.check(self.lib.np_check_error(self.model), "np_check_error")
 
-    def set_profiling(self, on: bool) -> None:
-        L.check(self.lib.np_set_profiling(self.model, int(on)), "np_set_profiling")
+    def set_profiling(self, on: bool, exact: bool = False) -> None:
+        """Per-launch event timing; exact=True orders each start event after
+        the launch's cross-stream waits (one extra empty launch per kernel)."""
+        L.check(self.lib.np_set_profiling(self.model, (2 if exact else 1) if on else 0), "np_set_profiling")
 
     def profile(self) -> dict:
         ms = (ctypes.c_double * L.NP_N_KINDS)()
