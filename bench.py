@@ -311,11 +311,17 @@ def profile_case(args):
     l1, l2 = (7, 8) if cfg.n_layers > 8 else (cfg.n_dense + 1, cfg.n_dense + 2)
     dec.sparse_mlp(l1, h)
     dec.sparse_mlp(l2, h)
-    dec.dense_mlp(0, h)
+    if cfg.n_dense > 0:
+        dec.dense_mlp(0, h)
     dec.ffn_layers(cfg.n_dense, cfg.n_sparse, h.clone())  # chained sparse FFNs
-    ids = dec.predict(h)
-    dec.delta(ids, -1)
-    dec.scatter(-1)
+    if cfg.pred_kind == "shared_argmax":
+        ids = dec.predict(h)
+        dec.delta(ids, -1)
+        dec.scatter(-1)
+    else:  # per-layer predictor: one layer's prediction, delta and reads
+        fire = dec.predict(h, cfg.n_dense)
+        dec.delta(fire, cfg.n_dense)
+        dec.scatter(cfg.n_dense)
     torch.cuda.synchronize()
     dec.check_error()
     dec.close()

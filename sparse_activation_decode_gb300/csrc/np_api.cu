@@ -121,6 +121,16 @@ struct np_model {
   // profiling
   bool prof = false;
   bool prof_markers = false;  // an empty kernel before each start event
+  // token counter on the device (the set kernel's window ages), and the
+  // captured token: replayed with the caller's h staged through h_io
+  int* token_dev = nullptr;
+  float* h_io = nullptr;
+  cudaGraphExec_t graph = nullptr;
+  cudaStream_t gs = nullptr;    // capture and replay stream (the caller's main stream may be the legacy one)
+  cudaEvent_t ev_gin = nullptr, ev_gout = nullptr;
+  bool graph_off = false;       // disabled, or the capture failed
+  int64_t graph_launches = 0;   // kernels in one replay
+  int64_t eager_tokens = 0;     // tokens issued launch by launch (the first one sets kernel attributes)
   std::vector<EventPair> prof_free;
   double prof_ms[NP_N_KINDS] = {};
   int64_t prof_launches[NP_N_KINDS] = {};
@@ -164,6 +174,11 @@ __global__ void marker_kernel() {}
 cudaError_t launch_marker(cudaStream_t st) {
   marker_kernel<<<1, 32, 0, st>>>();
   return cudaGetLastError();
+}
+
+// The device token counter advances once a token's deltas are all committed.
+__global__ void bump_kernel(int* counter) {
+  if (threadIdx.x == 0) *counter += 1;
 }
 
 np_status prof_begin(np_model* m, int kind, cudaStream_t st, EventPair* ep) {
@@ -551,6 +566,7 @@ SetLaunch set_args(np_model* m, int first_sparse, int n_layers) {
   a.batch = m->B;
   a.n_heads = m->NH;
   a.token = (int)m->token;
+  a.token_dev = m->token_dev;
   a.centroids = m->d.centroids;
   a.slotmap = m->slotmap;
   a.inv = m->inv;
@@ -613,13 +629,23 @@ np_status move_layers(np_model* m, const std::vector<int>& layers, size_t* n_mov
   return NP_OK;
 }
 
-void commit(np_model* m, uint64_t bits) {
+np_status bump_token(np_model* m) {
+  cudaStream_t st = m->main;
+  return launch(m, NP_KIND_FINISH, st, 0, [&] {
+    bump_kernel<<<1, 32, 0, st>>>(m->token_dev);
+    return cudaGetLastError();
+  });
+}
+
+np_status commit(np_model* m, uint64_t bits) {
   m->pending_bits &= ~bits;
   m->committed_since_token |= bits;
   if ((m->committed_since_token & all_layers(m)) == all_layers(m)) {
     m->committed_since_token = 0;
     m->token += 1;
+    return bump_token(m);
   }
+  return NP_OK;
 }
 
 np_status read_device_error(np_model* m) {
@@ -828,6 +854,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   // Host-link gathers need only a few MB in flight to fill the link; keeping
   // their grids small leaves the SMs to the FFN running beside them.
   // NP_TUNE_GATHER_CTAS / NP_TUNE_SCATTER_CTAS override the defaults.
+  m->graph_off = env_int("NP_TUNE_GRAPH", 1) == 0;
   m->gather_grid = env_int("NP_TUNE_GATHER_CTAS", 32);
   m->scatter_grid = env_int("NP_TUNE_SCATTER_CTAS", 4 * m->sms);
   m->pred_grid = 2 * m->sms;
@@ -864,6 +891,8 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if ((st = dev_alloc(m, &m->dout_s, Sa * K)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->ls_old, Sa * K)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->slot_hw, Sa)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->token_dev, 1)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->h_io, (size_t)m->B * m->D)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->mv_count, Sa)) != NP_OK) return fail(st);
   if (m->compact && ((st = dev_alloc(m, &m->mv_src, Sa * K)) != NP_OK || (st = dev_alloc(m, &m->mv_dst, Sa * K)) != NP_OK ||
                      (st = dev_alloc(m, &m->mv_oldct, Sa * K)) != NP_OK))
@@ -932,6 +961,9 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->fs, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_pre, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_ffn, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->gs, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_gin, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_gout, cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(cuda_fail(e, "cudaStreamCreate"));
   }
   e = cudaDeviceSynchronize();
@@ -951,7 +983,11 @@ np_status np_free_model(np_model* m) {
   if (m->g1) cudaStreamDestroy(m->g1);
   if (m->xs) cudaStreamDestroy(m->xs);
   if (m->fs) cudaStreamDestroy(m->fs);
+  if (m->gs) cudaStreamDestroy(m->gs);
+  if (m->ev_gin) cudaEventDestroy(m->ev_gin);
+  if (m->ev_gout) cudaEventDestroy(m->ev_gout);
   if (m->ev_pre) cudaEventDestroy(m->ev_pre);
+  if (m->graph) cudaGraphExecDestroy(m->graph);
   if (m->ev_ffn) cudaEventDestroy(m->ev_ffn);
   for (cudaEvent_t ev : m->ev_j)
     if (ev) cudaEventDestroy(ev);
@@ -984,6 +1020,7 @@ np_status np_reset_sequence(np_model* m) {
   if (m->S == 0) return NP_OK;
   cudaStream_t st = m->main;
   NP_TRY(join_side(m, st));
+  CUDA_TRY(cudaMemsetAsync(m->token_dev, 0, sizeof(int), st));
   return launch(m, NP_KIND_SET, st, 0, [&] {
     return launch_reset_state(m->slotmap, m->inv, m->resbits, m->slot_hw, m->frequency ? m->last_seen : nullptr, m->S,
                               m->F, m->K, m->W, st);
@@ -1077,8 +1114,7 @@ np_status np_scatter(np_model* m, int32_t layer) {
   NP_TRY(join_side(m, m->main));
   uint64_t bits = 0;
   for (int s : layers) bits |= 1ull << s;
-  commit(m, bits);
-  return NP_OK;
+  return commit(m, bits);
 }
 
 np_status np_sparse_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_dev) {
@@ -1151,14 +1187,10 @@ np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev)
                 [&] { return launch_add(h_dev, hb, chain_y(m, count - 1), m->B * m->D, st); });
 }
 
-np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
-  if (!m || !h_dev) return arg_fail("null argument");
-  if (!aligned16(h_dev)) return arg_fail("h_dev must be 16-byte aligned");
-  if (m->pending_bits) {
-    g_last_err = "a delta is pending; call np_scatter first";
-    return NP_ERR_STATE;
-  }
-  const int64_t token = m->token;
+// Everything one token enqueues, with h_dev as the residual stream (in and
+// out).  On a failed read the token's deltas are rolled back and NP_ERR_IO
+// returned.  Ends with the device token counter advanced.
+np_status enqueue_token(np_model* m, float* h_dev) {
   const bool shared = m->d.pred_kind == NP_PRED_SHARED_ARGMAX;
   // Residual chaining: layer l reads base(l) + y(l-1) and adds its y into
   // y(l); the residual stream after the last layer is written back by a
@@ -1254,6 +1286,74 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
   if (fin != m->main) {
     CUDA_TRY(cudaEventRecord(m->ev_ffn, fin));
     CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_ffn, 0));
+  }
+  if (m->S > 0) NP_TRY(bump_token(m));
+  return NP_OK;
+}
+
+// Capture one token's launches (every stream, forked from and joined back to
+// the main stream) as a graph over h_io.  A failed capture leaves the model
+// on eager launches.
+np_status capture_token(np_model* m) {
+  const int64_t l0 = m->launches;
+  cudaStream_t user_main = m->main;
+  m->main = m->gs;  // the capture runs on the library's own stream
+  cudaError_t e = cudaStreamBeginCapture(m->main, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) {
+    if (env_int("NP_TUNE_VERBOSE", 0) == 1) std::fprintf(stderr, "np: no capture: %s\n", cudaGetErrorString(e));
+    cudaGetLastError();
+    m->main = user_main;
+    m->graph_off = true;
+    return NP_OK;
+  }
+  const np_status st = enqueue_token(m, m->h_io);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(m->main, &g);
+  m->main = user_main;
+  m->pending_bits = 0;  // the capture only recorded the work
+  m->committed_since_token = 0;
+  if (st == NP_OK && e == cudaSuccess && g) e = cudaGraphInstantiate(&m->graph, g, 0);
+  if (g) cudaGraphDestroy(g);
+  if (st != NP_OK || e != cudaSuccess || !m->graph) {
+    if (env_int("NP_TUNE_VERBOSE", 0) == 1)
+      std::fprintf(stderr, "np: token capture failed (status %d, %s; %s)\n", (int)st, cudaGetErrorString(e),
+                   g_last_err.c_str());
+    cudaGetLastError();
+    m->graph = nullptr;
+    m->graph_off = true;
+  }
+  m->graph_launches = m->launches - l0;
+  m->launches = l0;
+  if (m->graph && env_int("NP_TUNE_VERBOSE", 0) == 1)
+    std::fprintf(stderr, "np: token captured (%lld kernels)\n", (long long)m->graph_launches);
+  return NP_OK;
+}
+
+np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
+  if (!m || !h_dev) return arg_fail("null argument");
+  if (!aligned16(h_dev)) return arg_fail("h_dev must be 16-byte aligned");
+  if (m->pending_bits) {
+    g_last_err = "a delta is pending; call np_scatter first";
+    return NP_ERR_STATE;
+  }
+  const int64_t token = m->token;
+  // Replay the captured token unless a read hook (a host call per layer) or
+  // the per-launch profiler needs the launches issued one by one.
+  const bool replay = !m->graph_off && !m->d.read_hook && !m->prof && m->S > 0 && m->eager_tokens > 0;
+  if (replay && !m->graph) NP_TRY(capture_token(m));
+  if (replay && m->graph) {
+    const size_t bytes = sizeof(float) * m->B * m->D;
+    CUDA_TRY(cudaMemcpyAsync(m->h_io, h_dev, bytes, cudaMemcpyDeviceToDevice, m->main));
+    CUDA_TRY(cudaEventRecord(m->ev_gin, m->main));
+    CUDA_TRY(cudaStreamWaitEvent(m->gs, m->ev_gin, 0));
+    CUDA_TRY(cudaGraphLaunch(m->graph, m->gs));
+    CUDA_TRY(cudaEventRecord(m->ev_gout, m->gs));
+    CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_gout, 0));
+    CUDA_TRY(cudaMemcpyAsync(h_dev, m->h_io, bytes, cudaMemcpyDeviceToDevice, m->main));
+    m->launches += m->graph_launches;
+  } else {
+    NP_TRY(enqueue_token(m, h_dev));
+    m->eager_tokens += 1;
   }
   if (m->S > 0) {
     m->committed_since_token = 0;

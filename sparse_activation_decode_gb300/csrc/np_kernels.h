@@ -112,6 +112,7 @@ struct SetLaunch {
   int batch;
   int n_heads;
   int token;
+  const int* token_dev;   // device token counter, read instead of `token` when set
   const int* ids;         // [batch][n_heads] or null
   const unsigned long long* keys;  // packed argmax keys [batch][n_heads] (used if ids null)
   int* ids_out;           // with keys: CTA 0 also writes the decoded IDs here

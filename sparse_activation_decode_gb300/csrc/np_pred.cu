@@ -164,10 +164,13 @@ size_t rowdot_smem_bytes(int len, int dtype_bytes, int rows_per_stage, int n_sta
 }
 
 template <typename T, int RPS>
+struct RowdotSmemTag {};
+
+template <typename T, int RPS>
 static cudaError_t launch_t(const RowdotLaunch& a, cudaStream_t st) {
   const size_t smem = rowdot_smem_bytes(a.len, a.dtype_bytes, RPS, a.n_stages);
   auto kern = rowdot_kernel<T, RPS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dyn_smem<RowdotSmemTag<T, RPS>>(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   kern<<<a.grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();

@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   int* __restrict__ out_outs = a.dout_s + (size_t)s * K;
   int* __restrict__ out_lsold = a.ls_old + (size_t)s * K;
   const bool compact = a.compact != 0;
+  const int token = a.token_dev ? *a.token_dev : a.token;
 
   if (a.keys && a.ids_out && blockIdx.x == 0)
     for (int h = tid; h < a.batch * a.n_heads; h += kSetThreads)
@@ -225,16 +226,24 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     else if (excl + __popc(aw) > K) aw = lowest_bits(aw, K - excl);
   }
 
-  // 3. resident set after this token
+  // 3. resident set after this token.  The history (last use or count) of
+  // this word's resident and active neurons is read once, all 32 loads in
+  // flight together, and kept in registers (bit loops below are unrolled so
+  // the array stays in registers).
   uint32_t nw = aw;
+  int lsv[32];
+  if (ls) {
+    const uint32_t need_ls = rw | aw;
+#pragma unroll
+    for (int b = 0; b < 32; ++b) lsv[b] = ((need_ls >> b) & 1u) ? ls[i * 32 + b] : 0;
+  }
   if (a.window > 1) {
     const uint32_t old = rw & ~aw;  // resident, not active now
     uint32_t keep_old = 0;
-    for (uint32_t w = old; w;) {
-      const int b = __ffs(w) - 1;
-      w &= w - 1;
-      const int age = a.token - ls[i * 32 + b];
-      if (age >= 0 && age < a.window) keep_old |= 1u << b;
+#pragma unroll
+    for (int b = 0; b < 32; ++b) {
+      const int age = token - lsv[b];
+      if (((old >> b) & 1u) && age >= 0 && age < a.window) keep_old |= 1u << b;
     }
     uint32_t cand = aw | keep_old;
     int ctot;
@@ -242,11 +251,9 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     if (ctot > K) {
       if (tid < 33) hist[tid] = 0;
       __syncthreads();
-      for (uint32_t w = keep_old; w;) {
-        const int b = __ffs(w) - 1;
-        w &= w - 1;
-        atomicAdd(&hist[a.token - ls[i * 32 + b]], 1);
-      }
+#pragma unroll
+      for (int b = 0; b < 32; ++b)
+        if ((keep_old >> b) & 1u) atomicAdd(&hist[token - lsv[b]], 1);
       __syncthreads();
       if (tid == 0) {
         int excess = ctot - K, age = a.window - 1;
@@ -259,10 +266,10 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
       }
       __syncthreads();
       uint32_t bucket = 0, older = 0;
-      for (uint32_t w = keep_old; w;) {
-        const int b = __ffs(w) - 1;
-        w &= w - 1;
-        const int age = a.token - ls[i * 32 + b];
+#pragma unroll
+      for (int b = 0; b < 32; ++b) {
+        if (!((keep_old >> b) & 1u)) continue;
+        const int age = token - lsv[b];
         if (age > cut_age) older |= 1u << b;
         else if (age == cut_age) bucket |= 1u << b;
       }
@@ -285,10 +292,10 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
       for (int pass = 0; pass < 2; ++pass) {
         if (tid < 256) hist[tid] = 0;
         __syncthreads();
-        for (uint32_t w = old; w;) {
-          const int b = __ffs(w) - 1;
-          w &= w - 1;
-          const int key = min(ls[i * 32 + b], 65535);
+#pragma unroll
+        for (int b = 0; b < 32; ++b) {
+          if (!((old >> b) & 1u)) continue;
+          const int key = min(lsv[b], 65535);
           if (pass == 0) atomicAdd(&hist[key >> 8], 1);
           else if ((key >> 8) == prefix) atomicAdd(&hist[key & 255], 1);
         }
@@ -304,10 +311,10 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
         need = cut_need;
       }
       uint32_t bucket = 0, lower = 0;
-      for (uint32_t w = old; w;) {
-        const int b = __ffs(w) - 1;
-        w &= w - 1;
-        const int key = min(ls[i * 32 + b], 65535);
+#pragma unroll
+      for (int b = 0; b < 32; ++b) {
+        if (!((old >> b) & 1u)) continue;
+        const int key = min(lsv[b], 65535);
         if (key < prefix) lower |= 1u << b;
         else if (key == prefix) bucket |= 1u << b;
       }
@@ -352,9 +359,19 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   const int n_keep = n_old - n_out;  // compact: rows that stay below this count
 
   // 5. one pass over the slots: occupied = holds a neuron that stays;
-  //    kept active neurons get their slot, outgoing neurons record theirs
-  for (int k = tid; k < K; k += kSetThreads) {
-    const int n = inv[k];
+  //    kept active neurons get their slot, outgoing neurons record theirs.
+  //    The thread's inverse-map entries are loaded first, all in flight.
+  constexpr int kSlotsPerThread = kMaxKmax / kSetThreads;
+  int invv[kSlotsPerThread];
+#pragma unroll
+  for (int q = 0; q < kSlotsPerThread; ++q) {
+    const int k = tid + q * kSetThreads;
+    invv[q] = k < K ? inv[k] : -1;
+  }
+#pragma unroll
+  for (int q = 0; q < kSlotsPerThread; ++q) {
+    const int k = tid + q * kSetThreads;
+    const int n = invv[q];
     if ((unsigned)n >= (unsigned)F) continue;
     const uint32_t bit = 1u << (n & 31);
     const int w = n >> 5;
@@ -418,12 +435,16 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     out_as[bit_rank(s_a, s_ea, n)] = k;
   }
   if (has_word) res[i] = nw;
-  if (ls)
-    for (int r = tid; r < n_a; r += kSetThreads) {
-      const int n = out_a[r];
-      out_lsold[r] = ls[n];
-      ls[n] = a.frequency ? ls[n] + 1 : a.token;
+  if (ls && has_word) {  // this word's active neurons, history from registers
+    int r = ea;
+#pragma unroll
+    for (int b = 0; b < 32; ++b) {
+      if (!((aw >> b) & 1u)) continue;
+      const int n = i * 32 + b;
+      out_lsold[r++] = lsv[b];
+      ls[n] = a.frequency ? lsv[b] + 1 : token;
     }
+  }
   if (tid == 0) {
     int* c = a.counts + (size_t)s * 4;
     c[0] = n_a;
@@ -525,7 +546,7 @@ __global__ void reset_state_kernel(int* slotmap, int* inv, uint32_t* resbits, in
 cudaError_t launch_set(const SetLaunch& a, cudaStream_t st) {
   if (a.words > kMaxWords || a.K > kMaxKmax) return cudaErrorInvalidValue;
   const size_t dyn = (size_t)a.K * sizeof(int);
-  cudaError_t e = cudaFuncSetAttribute(set_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  cudaError_t e = ensure_dyn_smem<SetLaunch>(reinterpret_cast<const void*>(set_kernel), dyn);
   if (e != cudaSuccess) return e;
   set_kernel<<<a.n_layers_launch, kSetThreads, dyn, st>>>(a);
   return cudaGetLastError();
