@@ -664,6 +664,7 @@ np_status sync_model(np_model* m) {
   CUDA_TRY(cudaStreamSynchronize(m->g1));
   CUDA_TRY(cudaStreamSynchronize(m->xs));
   CUDA_TRY(cudaStreamSynchronize(m->fs));
+  if (m->gs) CUDA_TRY(cudaStreamSynchronize(m->gs));
   CUDA_TRY(cudaStreamSynchronize(m->main));
   return NP_OK;
 }

@@ -279,3 +279,29 @@ def test_ffn_layers_equals_layer_by_layer(cfg):
     with pytest.raises(NpError):
         dec.ffn_layers(0, cfg.n_layers + 1, h0.clone())
     dec.close()
+
+
+@pytest.mark.parametrize("cfg", [SMALL_F16, SMALL_OPT.replace(lookahead=2), SMALL_BATCHED],
+                         ids=["small-f16", "small-opt-lookahead2", "small-batched"])
+def test_graph_replay_matches_eager(cfg, monkeypatch):
+    # tokens after the first are replayed from a captured graph; with graphs
+    # switched off every launch is issued one by one: the integer state must
+    # agree bit for bit and h up to the order of the FFN's split-K additions
+    wl = make_workload(cfg)
+    outs = []
+    for graph in ("1", "0"):
+        monkeypatch.setenv("NP_TUNE_GRAPH", graph)
+        dec = build_decoder(wl)
+        hs, states = [], []
+        for t in range(6):
+            h = wl.x[t].cuda().clone()
+            dec.decode_token(h)
+            hs.append(h.cpu())
+            states.append([dec.get_state(cfg.n_dense + s) for s in range(cfg.n_sparse)])
+        dec.check_error()
+        outs.append((hs, states))
+        dec.close()
+    (h1, s1), (h0, s0) = outs
+    assert s1 == s0
+    for a, b in zip(h1, h0):
+        assert oracle.rel_l2(a.numpy().ravel(), b.numpy().ravel()) < 1e-5
