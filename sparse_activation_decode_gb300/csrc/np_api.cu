@@ -107,6 +107,7 @@ struct np_model {
   // launch shapes
   int ffn_grid = 0, ffn_stages = 0;
   int chain_grid = 0, chain_stages = 0;  // persistent FFN chain (batch 1)
+  int pdl_mask = 1;                      // programmatic dependent launch: 1 predictor, 2 set kernel
   unsigned* arrive = nullptr;            // [2L] arrival counters of the chain
   float* chain_part = nullptr;           // [chain_grid][D] partial y of the chain
   int gather_grid = 0, scatter_grid = 0, pred_grid = 0;
@@ -404,6 +405,7 @@ np_status enqueue_rowdot(np_model* m, const void* W, int n_rows, int len, const 
   a.dtype_bytes = m->esz;
   a.rows_per_stage = rps;
   a.n_stages = ns;
+  a.pdl = (m->pdl_mask & 1) != 0;
   a.grid = m->pred_grid;
   a.err = m->err;
   cudaStream_t st = m->main;
@@ -585,6 +587,7 @@ SetLaunch set_args(np_model* m, int first_sparse, int n_layers) {
   a.ls_old = m->ls_old;
   a.totals = m->totals;
   a.slot_hw = m->slot_hw;
+  a.pdl = (m->pdl_mask & 2) != 0;
   a.compact = m->compact;
   a.mv_src = m->mv_src;
   a.mv_dst = m->mv_dst;
@@ -856,6 +859,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   // their grids small leaves the SMs to the FFN running beside them.
   // NP_TUNE_GATHER_CTAS / NP_TUNE_SCATTER_CTAS override the defaults.
   m->graph_off = env_int("NP_TUNE_GRAPH", 1) == 0;
+  m->pdl_mask = env_int("NP_TUNE_PDL", 1);
   m->gather_grid = env_int("NP_TUNE_GATHER_CTAS", 32);
   m->scatter_grid = env_int("NP_TUNE_SCATTER_CTAS", 4 * m->sms);
   m->pred_grid = 2 * m->sms;

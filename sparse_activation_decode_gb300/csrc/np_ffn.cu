@@ -44,7 +44,7 @@ constexpr int kFfnWarps = kFfnThreads / 32;      // consumer warps
 constexpr int kFfnBlock = kFfnThreads + 32;      // plus one producer warp
 constexpr int kChainThreads = 512;               // consumer threads of the persistent chain
 constexpr int kChainBlock = kChainThreads + 32;
-constexpr int kChainGroup = 4;                   // rows per block barrier in the chain
+constexpr int kChainGroup = 4;                   // rows per block barrier in the chain (2 for wide rows)
 constexpr int kRowCache = 64;                    // row indices cached per CTA
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -108,10 +108,6 @@ template <int NT> __device__ __forceinline__ bool consumer_sync_or(bool pred) {
 // silu(v) = v * sigmoid(v), the SwiGLU gate
 __device__ __forceinline__ float silu(float v) { return v / (1.f + expf(-v)); }
 
-__device__ __forceinline__ void grid_dependents_launch() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // Pieces shared by the per-layer kernel and the persistent chain kernel.
@@ -569,6 +565,9 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
   constexpr int P = Pairs<T>::N;
   constexpr int E = 2 * P;
   constexpr int NPROJ = GATED ? 3 : 2;
+  // rows per block barrier: a group's rows sit in registers, so rows of
+  // several chunks per thread come two or one at a time
+  constexpr int GRP = MAXC == 1 ? kChainGroup : (MAXC == 2 ? 2 : 1);
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // [16]
   uint64_t* empty = full + 16;                           // [16]
@@ -708,12 +707,12 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
       int limit;
       const int my_n = layer_rows(i, &wg, &wu, &wd, &list, &limit);
       bool aborted = false;
-      for (int jj = 0; jj < my_n; jj += kChainGroup) {
-        const int nrow = my_n - jj < kChainGroup ? my_n - jj : kChainGroup;
-        int off[kChainGroup], slot[kChainGroup];
-        uint32_t par[kChainGroup];
+      for (int jj = 0; jj < my_n; jj += GRP) {
+        const int nrow = my_n - jj < GRP ? my_n - jj : GRP;
+        int off[GRP], slot[GRP];
+        uint32_t par[GRP];
 #pragma unroll
-        for (int r = 0; r < kChainGroup; ++r) {
+        for (int r = 0; r < GRP; ++r) {
           slot[r] = cs;
           par[r] = cwrap & 1u;
           off[r] = (int)((512 + (size_t)cs * slot_bytes) >> 4);
@@ -724,8 +723,8 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
             }
           }
         }
-        if (!consume_group_early<T, GATED, MAXC, kChainThreads, kChainGroup>(
-                reinterpret_cast<const uint4*>(smem), off, slot, par, full, empty, nrow, a.err, jj / kChainGroup, NC,
+        if (!consume_group_early<T, GATED, MAXC, kChainThreads, GRP>(
+                reinterpret_cast<const uint4*>(smem), off, slot, par, full, empty, nrow, a.err, jj / GRP, NC,
                 xr, acc, red, a.swiglu != 0)) {
           aborted = true;
           break;

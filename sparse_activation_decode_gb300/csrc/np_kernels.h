@@ -87,13 +87,14 @@ struct RowdotLaunch {
   unsigned long long* keys;  // mode 1: [n_rows / C]
   int C;
   uint32_t* fire_bits;    // mode 2
-  uint32_t* zero_ptr;     // words cleared by CTA 0 before anything else (may be null)
+  uint32_t* zero_ptr;     // words cleared by CTA 0 once the previous kernel has completed (may be null)
   int zero_words;
   int dtype;
   int dtype_bytes;
   int rows_per_stage;
   int n_stages;
   int grid;
+  int pdl;                // launch with programmatic dependent launch
   int* err;
 };
 size_t rowdot_smem_bytes(int len, int dtype_bytes, int rows_per_stage, int n_stages);
@@ -136,6 +137,7 @@ struct SetLaunch {
   int* dout_s;            // [S][K] slot each outgoing neuron held
   int* ls_old;            // [S][K] previous last use of each active neuron
   unsigned long long* totals;  // running sums: |A|, |D_in|, |D_out|, dropped
+  int pdl;                // launch with programmatic dependent launch
   int* slot_hw;           // [S] one past the highest occupied slot (an upper bound), or null;
                           // exactly |R| under the compact placement
   // compact placement: rows stay in [0, |R|); freed slots below the new count

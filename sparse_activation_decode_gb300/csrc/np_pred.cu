@@ -51,8 +51,7 @@ __global__ void __launch_bounds__(kThreads, 2) rowdot_kernel(RowdotLaunch a) {
   const int my_n = (n_groups > (int)blockIdx.x) ? (n_groups - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const T* W = static_cast<const T*>(a.W);
 
-  if (blockIdx.x == 0 && a.zero_ptr)
-    for (int i = tid; i < a.zero_words; i += kThreads) a.zero_ptr[i] = 0u;
+  grid_dependents_launch();  // the next kernel may start its own prologue
   if (tid == 0) {
     for (int s = 0; s < a.n_stages; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
@@ -76,6 +75,11 @@ __global__ void __launch_bounds__(kThreads, 2) rowdot_kernel(RowdotLaunch a) {
     const int pre = my_n < a.n_stages ? my_n : a.n_stages;
     for (int j = 0; j < pre; ++j) issue(j);
   }
+  // the weights are constant; the input and the buffer cleared here belong
+  // to the kernels before this one
+  grid_dependency_wait();
+  if (blockIdx.x == 0 && a.zero_ptr)
+    for (int i = tid; i < a.zero_words; i += kThreads) a.zero_ptr[i] = 0u;
 
   if (a.vec_rmsnorm) {
     rmsnorm_to_smem(a.vec, a.vec2, xs, len, red1);
@@ -172,8 +176,9 @@ static cudaError_t launch_t(const RowdotLaunch& a, cudaStream_t st) {
   auto kern = rowdot_kernel<T, RPS>;
   cudaError_t e = ensure_dyn_smem<RowdotSmemTag<T, RPS>>(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  PdlConfig c(dim3(a.grid), dim3(kThreads), smem, st);
+  c.cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&c.cfg, kern, a);
 }
 
 template <typename T>

@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   __shared__ int cut_age, cut_need, s_hw, s_nfree;
   __shared__ uint32_t s_a[kMaxWords], s_out[kMaxWords], s_keep[kMaxWords];
   __shared__ int s_ea[kMaxWords], s_eout[kMaxWords];
-  extern __shared__ int free_list[];  // [K]
+  extern __shared__ int free_list[];  // [K] free slots, then [K] a copy of the inverse map
+  int* inv_s = free_list + a.K;
 
   const int tid = threadIdx.x;
   const int s = a.first_sparse + blockIdx.x;
@@ -177,20 +178,34 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   int* __restrict__ out_outs = a.dout_s + (size_t)s * K;
   int* __restrict__ out_lsold = a.ls_old + (size_t)s * K;
   const bool compact = a.compact != 0;
-  const int token = a.token_dev ? *a.token_dev : a.token;
-
-  if (a.keys && a.ids_out && blockIdx.x == 0)
-    for (int h = tid; h < a.batch * a.n_heads; h += kSetThreads)
-      a.ids_out[h] = (int)(0xFFFFFFFFu - (uint32_t)(a.keys[h] & 0xFFFFFFFFull));
 
   const int i = tid;
   const bool has_word = i < W;
   const uint32_t word_mask =
       (has_word && i == W - 1 && (F & 31)) ? ((1u << (F & 31)) - 1u) : (has_word ? 0xffffffffu : 0u);
 
-  // 1. active set words and resident words
-  uint32_t aw = 0;
+  // The layer's own state does not depend on the prediction: read it while
+  // the kernel before this one (the predictor) finishes.  Resident words,
+  // the history (last use or count) of this word's 32 neurons, all loads in
+  // flight together, and a copy of the inverse map in shared memory.
+  grid_dependents_launch();
   const uint32_t rw = has_word ? res[i] : 0u;
+  int lsv[32];
+  if (ls) {
+#pragma unroll
+    for (int b = 0; b < 32; ++b) lsv[b] = (has_word && i * 32 + b < F) ? ls[i * 32 + b] : 0;
+  }
+  for (int k = tid; k < K; k += kSetThreads) inv_s[k] = inv[k];
+  // the prediction and the token counter come from earlier kernels
+  grid_dependency_wait();
+  const int token = a.token_dev ? *a.token_dev : a.token;
+
+  if (a.keys && a.ids_out && blockIdx.x == 0)
+    for (int h = tid; h < a.batch * a.n_heads; h += kSetThreads)
+      a.ids_out[h] = (int)(0xFFFFFFFFu - (uint32_t)(a.keys[h] & 0xFFFFFFFFull));
+
+  // 1. active set words
+  uint32_t aw = 0;
   if (has_word) {
     if (a.ids || a.keys) {
       for (int b = 0; b < a.batch; ++b) {
@@ -226,17 +241,9 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     else if (excl + __popc(aw) > K) aw = lowest_bits(aw, K - excl);
   }
 
-  // 3. resident set after this token.  The history (last use or count) of
-  // this word's resident and active neurons is read once, all 32 loads in
-  // flight together, and kept in registers (bit loops below are unrolled so
-  // the array stays in registers).
+  // 3. resident set after this token (bit loops are unrolled so that the
+  //    history stays in registers)
   uint32_t nw = aw;
-  int lsv[32];
-  if (ls) {
-    const uint32_t need_ls = rw | aw;
-#pragma unroll
-    for (int b = 0; b < 32; ++b) lsv[b] = ((need_ls >> b) & 1u) ? ls[i * 32 + b] : 0;
-  }
   if (a.window > 1) {
     const uint32_t old = rw & ~aw;  // resident, not active now
     uint32_t keep_old = 0;
@@ -360,18 +367,9 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
 
   // 5. one pass over the slots: occupied = holds a neuron that stays;
   //    kept active neurons get their slot, outgoing neurons record theirs.
-  //    The thread's inverse-map entries are loaded first, all in flight.
-  constexpr int kSlotsPerThread = kMaxKmax / kSetThreads;
-  int invv[kSlotsPerThread];
-#pragma unroll
-  for (int q = 0; q < kSlotsPerThread; ++q) {
-    const int k = tid + q * kSetThreads;
-    invv[q] = k < K ? inv[k] : -1;
-  }
-#pragma unroll
-  for (int q = 0; q < kSlotsPerThread; ++q) {
-    const int k = tid + q * kSetThreads;
-    const int n = invv[q];
+  //    (from the shared copy of the inverse map)
+  for (int k = tid; k < K; k += kSetThreads) {
+    const int n = inv_s[k];
     if ((unsigned)n >= (unsigned)F) continue;
     const uint32_t bit = 1u << (n & 31);
     const int w = n >> 5;
@@ -545,11 +543,12 @@ __global__ void reset_state_kernel(int* slotmap, int* inv, uint32_t* resbits, in
 
 cudaError_t launch_set(const SetLaunch& a, cudaStream_t st) {
   if (a.words > kMaxWords || a.K > kMaxKmax) return cudaErrorInvalidValue;
-  const size_t dyn = (size_t)a.K * sizeof(int);
+  const size_t dyn = 2 * (size_t)a.K * sizeof(int);
   cudaError_t e = ensure_dyn_smem<SetLaunch>(reinterpret_cast<const void*>(set_kernel), dyn);
   if (e != cudaSuccess) return e;
-  set_kernel<<<a.n_layers_launch, kSetThreads, dyn, st>>>(a);
-  return cudaGetLastError();
+  PdlConfig c(dim3(a.n_layers_launch), dim3(kSetThreads), dyn, st);
+  c.cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&c.cfg, set_kernel, a);
 }
 
 cudaError_t launch_rollback(const SetLaunch& a, cudaStream_t st) {

@@ -252,9 +252,11 @@ def test_full_size_sampled(cfg, tokens):
 
 
 @pytest.mark.parametrize("cfg", [SMALL_F16, SMALL_BATCHED, SMALL_F16.replace(activation="swiglu"),
-                                 SMALL_F16.replace(slots="compact"), SMALL_OPT.replace(slots="compact")],
+                                 SMALL_F16.replace(slots="compact"), SMALL_OPT.replace(slots="compact"),
+                                 SMALL_BF16.replace(name="wide-bf16", d_model=5120, d_ff=1024, k_max=256,
+                                                    n_layers=4, n_dense=1)],
                          ids=["small-f16", "small-batched", "small-f16-swiglu", "small-f16-compact",
-                              "small-opt-window-compact"])
+                              "small-opt-window-compact", "wide-rows-bf16"])
 def test_ffn_layers_equals_layer_by_layer(cfg):
     # the chained FFN entry point equals h += FFN_l(h) applied layer by layer
     # through the standalone entry points, over dense and sparse layers
