@@ -202,7 +202,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out);
 np_status np_free_model(np_model* m);
 
 /* Forget the resident sets: the next token loads its full predicted set, as
- * at the first token of a sequence (NeuroPrefetcher section 3.4 cold start).
+ * at a sequence's first token (NeuroPrefetcher section 3.4 cold start).
  * Resident buffer bytes are kept. */
 np_status np_reset_sequence(np_model* m);
 

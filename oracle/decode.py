@@ -85,9 +85,9 @@ def ffn_rows(gate: np.ndarray | None, up: np.ndarray, down_t: np.ndarray,
     """FFN over an explicit list of neurons.
 
     gate, up, down_t: [n, D] rows (row n of the gate, up and down^T
-    projections of neuron n: NeuroPrefetcher full text, delta runtime: "for
-    each active neuron i, the runtime uses row i of the gate, up, and down^T
-    projections").  Returns (y[D], h[n]) with
+    projections of neuron n: NeuroPrefetcher full text, delta runtime, where
+    each active neuron's output comes from its own three rows).  Returns
+    (y[D], h[n]) with
         h_n = relu(gate_n . x) * (up_n . x)   (ReLU-fied Llama)
         h_n = silu(gate_n . x) * (up_n . x)   (activation "swiglu": the
                                                SwiGLU MLP of the pages'
@@ -123,8 +123,8 @@ def predictor_logits(w1: np.ndarray, w2: np.ndarray, b2: np.ndarray | None,
 
 def head_argmax(logits: np.ndarray, n_heads: int, n_centroids: int) -> np.ndarray:
     """Per head, the centroid with the highest logit; ties go to the lowest
-    index ("selecting the highest-probability centroid for each layer",
-    NeuroPrefetcher "Shared Activation Predictor")."""
+    index (NeuroPrefetcher "Shared Activation Predictor": each head picks its
+    most probable centroid)."""
     return np.argmax(logits.reshape(n_heads, n_centroids), axis=1).astype(np.int64)
 
 
@@ -155,9 +155,9 @@ def combine_sets(gate_ids: list[int], up_ids: list[int], mode: str) -> list[int]
 
 
 def cap_set(active: list[int], k_max: int) -> tuple[list[int], int]:
-    """Keep the k_max lowest IDs ("K_max, the maximum number of active
-    intermediate neurons kept per sparse layer", NeuroPrefetcher full text,
-    evaluation budgets).  Returns (kept, number dropped)."""
+    """Keep the k_max lowest IDs (NeuroPrefetcher full text, evaluation
+    budgets: K_max bounds how many active neurons a sparse layer keeps).
+    Returns (kept, number dropped)."""
     active = sorted(active)
     if len(active) <= k_max:
         return active, 0
@@ -177,8 +177,8 @@ def assign_slots(slotmap: np.ndarray, inv: np.ndarray, d_in: list[int],
     """Release the slots of D_out and give free slots to D_in, in place.
 
     Per-layer slot map S[n] = slot of neuron n or -1 (NeuroPrefetcher full
-    text, delta runtime: "clears slot-map entries for outgoing rows, assigns
-    freed slots to incoming rows").  Reading: the i-th incoming neuron in
+    text, delta runtime: outgoing neurons give up their slots, which the
+    incoming ones then receive).  Reading: the i-th incoming neuron in
     ascending ID order takes the i-th free slot in ascending slot order.
     Returns the (neuron, slot) pairs of D_in."""
     for n in d_out:
@@ -198,9 +198,9 @@ def assign_slots(slotmap: np.ndarray, inv: np.ndarray, d_in: list[int],
 def assign_slots_compact(slotmap: np.ndarray, inv: np.ndarray, d_in: list[int],
                          d_out: list[int], n_rows: int) -> tuple[list[tuple[int, int]], list[tuple[int, int]], int]:
     """Compact placement, in place (LLM in a flash, 3.3 "Optimized Data
-    Management in DRAM": a removed neuron's row is replaced with a row from
-    the end of the occupied region; incoming rows are appended; the occupied
-    rows stay [0, num_rows)).
+    Management in DRAM": the hole a removed neuron leaves is filled by one of
+    the last occupied rows, new rows go after the occupied ones, and the
+    occupied rows stay [0, num_rows)).
 
     Reading: with n_new = num_rows - |D_out|, every removed neuron whose slot
     lies below n_new is replaced by a surviving row from the end region
@@ -243,8 +243,8 @@ def window_resident(resident_prev: list[int], active: list[int], last_seen: dict
                     t: int, window: int, k_max: int) -> list[int]:
     """Resident set after token t under windowing: the neurons active in the
     last `window` tokens (this one included) that were resident or are active
-    now (LLM in a flash, 3.1 "Windowing retains weights predicted to be active
-    for recent tokens").  If more than k_max remain, the ones whose last use is
+    now (LLM in a flash, 3.1 "Windowing": the rows predicted active for the
+    recent tokens stay in memory).  If more than k_max remain, the ones whose last use is
     oldest go first, ties by ascending ID; neurons active now never go
     (reading: the pages give no cap rule).  `last_seen` must already hold t
     for the active neurons."""

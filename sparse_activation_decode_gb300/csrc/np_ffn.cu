@@ -6,8 +6,8 @@
 //                                          or silu(g_r . x) * (u_r . x): SwiGLU)
 //     y  += h_r * d_r
 // with x = rmsnorm(h), h = h_base + y_prev (NeuroPrefetcher full text, delta
-// runtime: row i of the gate, up and down^T projections serves active neuron
-// i; ReLU-fied form of the activation).  Consecutive layers chain through the
+// runtime: an active neuron is computed from its own gate, up and down^T
+// rows; ReLU-fied form of the activation).  Consecutive layers chain through the
 // residual stream as base + previous y: the CTA that reads first stores h for
 // the next layer and clears the accumulator after next, so no separate
 // residual-add kernel runs between layers.

@@ -72,8 +72,8 @@ def test_ffn_matches_torch_linear_formulation():
 
 
 def test_ffn_permutation_invariance():
-    # LLM in a flash 3.3: reordering neurons preserves the FFN output when the
-    # up and down rows are reordered consistently.
+    # LLM in a flash 3.3: permuting the neurons, with their up and down rows
+    # moved together, leaves the FFN output unchanged.
     rng = np.random.default_rng(4)
     n, d = 50, 16
     g, u, dt = (rng.standard_normal((n, d)) for _ in range(3))
