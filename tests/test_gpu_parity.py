@@ -55,6 +55,10 @@ SMALL_CASES = {
     "small-opt-frequency": (SMALL_OPT.replace(residency="frequency", k_max=150), {}),
     "small-f16-frequency": (SMALL_F16.replace(residency="frequency", k_max=300), {}),
     "small-batched-frequency-compact": (SMALL_BATCHED.replace(residency="frequency", slots="compact"), {}),
+    # degenerate sets: intersections of two 2% masks are mostly empty (FFN over
+    # no rows, empty deltas); a K_max of one row
+    "tiny-intersect-sparse": (TINY.replace(combine="intersect", density=0.02), {}),
+    "tiny-kmax1": (TINY.replace(k_max=1), {}),
 }
 
 
@@ -307,3 +311,16 @@ def test_graph_replay_matches_eager(cfg, monkeypatch):
     assert s1 == s0
     for a, b in zip(h1, h0):
         assert oracle.rel_l2(a.numpy().ravel(), b.numpy().ravel()) < 1e-5
+
+
+def test_max_sizes():
+    # the largest shapes the ABI accepts: d_model 8192 (fp16 rows of 16 KiB,
+    # four chunks per FFN thread), d_ff 16384 (512 mask words, one per set
+    # thread) and K_max 8192, with the cap binding (union of two 30% masks)
+    from workloads.synth import Config
+    cfg = Config(name="max-shape", n_layers=3, n_dense=1, d_model=8192, d_ff=16384, k_max=8192,
+                 n_centroids=32, dtype="f16", density=0.30, persistence=0.83, pred_hidden=256,
+                 planted_scale=60.0, n_warm=0, n_decode=3, seed=2011)
+    wl = make_workload(cfg, device="cuda")
+    summ = run_and_compare(wl, 3, check_buffers=False, sample_slots=64, check_layer_y=True)
+    assert summ["max_h_rel"] < FFN_TOL
