@@ -65,6 +65,34 @@ __device__ __forceinline__ int block_scan(int v, int* wsum, int* total) {
   return base + x - v;
 }
 
+// The same scan over 64-bit values (three counts packed in 21-bit fields).
+__device__ __forceinline__ unsigned long long block_scan64(unsigned long long v, unsigned long long* wsum,
+                                                           unsigned long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = lane < kSetThreads / 32 ? wsum[lane] : 0ull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kSetThreads / 32) wsum[lane] = w;
+  }
+  __syncthreads();
+  const unsigned long long base = warp > 0 ? wsum[warp - 1] : 0ull;
+  *total = wsum[kSetThreads / 32 - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
 __device__ __forceinline__ uint32_t lowest_bits(uint32_t w, int m) {
   uint32_t r = 0;
   for (int t = 0; t < m && w; ++t) {
@@ -151,14 +179,21 @@ __device__ __forceinline__ void compact_assign(const SetLaunch& a, int s, int ti
 
 __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   __shared__ int wsum[32];
+  __shared__ unsigned long long wsum64[32];
   __shared__ uint32_t occ[kMaxKmax / 32];
   __shared__ uint32_t s_hole[kMaxKmax / 32], s_mov[kMaxKmax / 32];  // compact: slots to refill / to move
   __shared__ int hist[256];
   __shared__ int cut_age, cut_need, s_hw, s_nfree;
   __shared__ uint32_t s_a[kMaxWords], s_out[kMaxWords], s_keep[kMaxWords];
   __shared__ int s_ea[kMaxWords], s_eout[kMaxWords];
-  extern __shared__ int free_list[];  // [K] free slots, then [K] a copy of the inverse map
+  // [K] free slots, then [K] copies of the inverse map and the slot contents,
+  // then [K] each: outgoing neurons, their slots, incoming neurons
+  extern __shared__ int free_list[];
   int* inv_s = free_list + a.K;
+  int* ct_s = inv_s + a.K;
+  int* l_out = ct_s + a.K;
+  int* l_outs = l_out + a.K;
+  int* l_in = l_outs + a.K;
 
   const int tid = threadIdx.x;
   const int s = a.first_sparse + blockIdx.x;
@@ -190,12 +225,15 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   // flight together, and a copy of the inverse map in shared memory.
   grid_dependents_launch();
   const uint32_t rw = has_word ? res[i] : 0u;
-  int lsv[32];
+  int lsv[32];  // history of the resident neurons now, of the newly active ones below
   if (ls) {
 #pragma unroll
-    for (int b = 0; b < 32; ++b) lsv[b] = (has_word && i * 32 + b < F) ? ls[i * 32 + b] : 0;
+    for (int b = 0; b < 32; ++b) lsv[b] = ((rw >> b) & 1u) ? ls[i * 32 + b] : 0;
   }
-  for (int k = tid; k < K; k += kSetThreads) inv_s[k] = inv[k];
+  for (int k = tid; k < K; k += kSetThreads) {
+    inv_s[k] = inv[k];
+    ct_s[k] = ct[k];
+  }
   // the prediction and the token counter come from earlier kernels
   grid_dependency_wait();
   const int token = a.token_dev ? *a.token_dev : a.token;
@@ -244,6 +282,12 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   // 3. resident set after this token (bit loops are unrolled so that the
   //    history stays in registers)
   uint32_t nw = aw;
+  if (ls) {
+    const uint32_t fresh = aw & ~rw;
+#pragma unroll
+    for (int b = 0; b < 32; ++b)
+      if ((fresh >> b) & 1u) lsv[b] = ls[i * 32 + b];
+  }
   if (a.window > 1) {
     const uint32_t old = rw & ~aw;  // resident, not active now
     uint32_t keep_old = 0;
@@ -336,12 +380,19 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   const uint32_t dinw = aw & ~rw;
   const uint32_t doutw = rw & ~nw;
 
-  // 4. ranks within A, D_in, D_out; the lists in ascending ID order
-  int n_a, n_in, n_out, n_old = 0;
+  // 4. ranks within A, D_in, D_out (one scan of the three counts packed in
+  //    21-bit fields); the lists in ascending ID order, D_in and D_out also
+  //    in shared memory for the steps below
+  int n_old = 0;
   if (compact) (void)block_scan(__popc(rw), wsum, &n_old);
-  const int ea = block_scan(__popc(aw), wsum, &n_a);
-  const int ein = block_scan(__popc(dinw), wsum, &n_in);
-  const int eout = block_scan(__popc(doutw), wsum, &n_out);
+  constexpr unsigned long long kF21 = (1ull << 21) - 1;
+  unsigned long long tot3;
+  const unsigned long long ex3 = block_scan64(
+      (unsigned long long)__popc(aw) | ((unsigned long long)__popc(dinw) << 21) |
+          ((unsigned long long)__popc(doutw) << 42),
+      wsum64, &tot3);
+  const int ea = (int)(ex3 & kF21), ein = (int)((ex3 >> 21) & kF21), eout = (int)((ex3 >> 42) & kF21);
+  const int n_a = (int)(tot3 & kF21), n_in = (int)((tot3 >> 21) & kF21), n_out = (int)((tot3 >> 42) & kF21);
   if (has_word) {
     s_a[i] = aw;
     s_out[i] = doutw;
@@ -351,9 +402,17 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     int p = ea;
     for (uint32_t w = aw; w; w &= w - 1) out_a[p++] = i * 32 + __ffs(w) - 1;
     p = ein;
-    for (uint32_t w = dinw; w; w &= w - 1) out_in[p++] = i * 32 + __ffs(w) - 1;
+    for (uint32_t w = dinw; w; w &= w - 1, ++p) {
+      const int n = i * 32 + __ffs(w) - 1;
+      out_in[p] = n;
+      l_in[p] = n;
+    }
     p = eout;
-    for (uint32_t w = doutw; w; w &= w - 1) out_out[p++] = i * 32 + __ffs(w) - 1;
+    for (uint32_t w = doutw; w; w &= w - 1, ++p) {
+      const int n = i * 32 + __ffs(w) - 1;
+      out_out[p] = n;
+      l_out[p] = n;
+    }
   }
   const int KW = (K + 31) / 32;
   if (tid < KW) {
@@ -375,7 +434,9 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     const int w = n >> 5;
     const uint32_t kbit = 1u << (k & 31);
     if (s_out[w] & bit) {
-      out_outs[bit_rank(s_out, s_eout, n)] = k;
+      const int r = bit_rank(s_out, s_eout, n);
+      out_outs[r] = k;
+      l_outs[r] = k;
       if (compact && k < n_keep) atomicOr(&s_hole[k >> 5], kbit);
     } else if (s_keep[w] & bit) {
       atomicOr(&occ[k >> 5], kbit);
@@ -394,8 +455,8 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
 
   // 6. outgoing neurons leave (before incoming ones may take their slots)
   for (int r = tid; r < n_out; r += kSetThreads) {
-    const int n = out_out[r];
-    const int k = out_outs[r];
+    const int n = l_out[r];
+    const int k = l_outs[r];
     S[n] = -1;
     if ((unsigned)k < (unsigned)K) inv[k] = -1;
   }
@@ -423,10 +484,10 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   //    (compact); remember what the slots held
   const int n_free = s_nfree;
   for (int r = tid; r < n_in; r += kSetThreads) {
-    const int n = out_in[r];
+    const int n = l_in[r];
     const int k = r < n_free ? (compact ? n_keep + r : free_list[r]) : 0;
     out_ins[r] = k;
-    out_inct[r] = ct[k];
+    out_inct[r] = ct_s[k];  // untouched above: appended or free slots are not move targets
     ct[k] = n;
     inv[k] = n;
     S[n] = k;
@@ -543,7 +604,7 @@ __global__ void reset_state_kernel(int* slotmap, int* inv, uint32_t* resbits, in
 
 cudaError_t launch_set(const SetLaunch& a, cudaStream_t st) {
   if (a.words > kMaxWords || a.K > kMaxKmax) return cudaErrorInvalidValue;
-  const size_t dyn = 2 * (size_t)a.K * sizeof(int);
+  const size_t dyn = 6 * (size_t)a.K * sizeof(int);
   cudaError_t e = ensure_dyn_smem<SetLaunch>(reinterpret_cast<const void*>(set_kernel), dyn);
   if (e != cudaSuccess) return e;
   PdlConfig c(dim3(a.n_layers_launch), dim3(kSetThreads), dyn, st);
