@@ -267,7 +267,13 @@ np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev)
  * suffix; h_dev [batch][D] float32 is the residual stream in and out.
  * stats_host may be NULL; when given, the call synchronises and fills it.
  * On an error return the contents of h_dev are unspecified; the committed
- * decode state is unchanged. */
+ * decode state is unchanged.
+ * The first call issues its kernels one by one; later calls replay a CUDA
+ * graph of one token captured once (h_dev is copied into and out of an
+ * internal buffer on main_stream), except while a read hook is set or
+ * profiling is on, which issue the kernels one by one.  Both ways enqueue the
+ * same kernels on the same data.  The environment variable NP_TUNE_GRAPH=0
+ * (read at np_init_model) turns replay off. */
 np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host);
 
 /* Copy the committed slot map [F] and inverse map [K] of sparse layer
