@@ -920,10 +920,11 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     const int dt = m->d.dtype;
     const size_t optin = m->smem_optin - 1024;
     const int want = env_int("NP_TUNE_MMA_CLUSTERS", 0);
+    const int max_st = env_int("NP_TUNE_MMA_STAGES", 0);
     const int ffn_mode = m->d.has_gate ? kMmaFfnGated : kMmaFfnUp;
-    if ((e = mma_plan(ffn_mode, dt == NP_BF16, m->D, optin, m->sms, want, &m->plan_ffn)) != cudaSuccess ||
-        (e = mma_plan(kMmaHidden, dt == NP_BF16, m->D, optin, m->sms, want, &m->plan_hid)) != cudaSuccess ||
-        (e = mma_plan(kMmaHeads, dt == NP_BF16, m->H, optin, m->sms, want, &m->plan_heads)) != cudaSuccess)
+    if ((e = mma_plan(ffn_mode, dt == NP_BF16, m->D, optin, m->sms, want, max_st, &m->plan_ffn)) != cudaSuccess ||
+        (e = mma_plan(kMmaHidden, dt == NP_BF16, m->D, optin, m->sms, want, max_st, &m->plan_hid)) != cudaSuccess ||
+        (e = mma_plan(kMmaHeads, dt == NP_BF16, m->H, optin, m->sms, want, max_st, &m->plan_heads)) != cudaSuccess)
       return fail(cuda_fail(e, "mma_plan"));
     if (m->S > 0 && (e = make_row_maps(&m->map_bufs, m->bufs, dt, (uint64_t)m->S * m->nproj * K, m->D)) != cudaSuccess)
       return fail(cuda_fail(e, "tensor map of the resident rows"));

@@ -229,7 +229,9 @@ struct RowMaps {
 };
 cudaError_t make_row_maps(RowMaps* out, const void* base, int dtype, uint64_t rows, uint64_t cols);
 size_t mma_smem_bytes(int mode, int ks_len, int n_stages);
-cudaError_t mma_plan(int mode, int bf16, int Kdim, size_t smem_optin, int n_sms, int want_clusters, MmaPlan* p);
+// want_clusters > 0 caps the clusters; max_stages > 1 caps the ring depth.
+cudaError_t mma_plan(int mode, int bf16, int Kdim, size_t smem_optin, int n_sms, int want_clusters, int max_stages,
+                     MmaPlan* p);
 cudaError_t launch_mma_rows(int mode, int bf16, const RowMaps& maps, const MmaArgs& a, const MmaPlan& p,
                             cudaStream_t st);
 // out[i] = x[i] + y[i] (the residual stream after the last layer)

@@ -690,7 +690,8 @@ size_t mma_smem_bytes(int mode, int ks_len, int n_stages) {
   return 1024 + kSmemHeader + (size_t)(ks_len / 64) * 2048 + (size_t)n_stages * stage;
 }
 
-cudaError_t mma_plan(int mode, int bf16, int Kdim, size_t smem_optin, int n_sms, int want_clusters, MmaPlan* p) {
+cudaError_t mma_plan(int mode, int bf16, int Kdim, size_t smem_optin, int n_sms, int want_clusters, int max_stages,
+                     MmaPlan* p) {
   const bool ffn = mode == kMmaFfnGated || mode == kMmaFfnUp;
   const int unit = ffn ? 128 : 64;
   int cs = 0;
@@ -707,6 +708,7 @@ cudaError_t mma_plan(int mode, int bf16, int Kdim, size_t smem_optin, int n_sms,
   if (fixed + 2 * stage > smem_optin) return cudaErrorInvalidValue;
   int ns = (int)((smem_optin - fixed) / stage);
   if (ns > kMaxStages) ns = kMaxStages;
+  if (max_stages > 1 && ns > max_stages) ns = max_stages;  // fewer stages: more CTAs per SM
   const size_t smem = mma_smem_bytes(mode, ks, ns);
   int nc = 0;
   cudaError_t e = cudaSuccess;
