@@ -36,13 +36,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # source file still has the recorded hash.
 NCU_TRAFFIC = {
     ("gather", "llama2-7b-relu"): {"src": "np_scatter.cu", "src_hash": "92078b0e6f793061", "bytes_per_launch": 113408},
-    ("ffn", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "b519a23ae1071319", "bytes_per_launch": 50407040},
-    ("dense", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "b519a23ae1071319", "bytes_per_launch": 273550080},
+    ("ffn", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "671f6969c46ddbcd", "bytes_per_launch": 50406656},
+    ("dense", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "671f6969c46ddbcd", "bytes_per_launch": 273913600},
     # one persistent launch over the 31 sparse layers, per layer
-    ("ffn_chain", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "b519a23ae1071319",
-                                      "bytes_per_launch": 50486998},
-    ("ffn", "llama2-7b-batch8"): {"src": "np_mma.cu", "src_hash": "a6395d2f54e8c479", "bytes_per_launch": 85350656},
-    ("dense", "llama2-7b-batch8"): {"src": "np_mma.cu", "src_hash": "a6395d2f54e8c479", "bytes_per_launch": 281533696},
+    ("ffn_chain", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "671f6969c46ddbcd",
+                                      "bytes_per_launch": 50491408},
+    ("ffn", "llama2-7b-batch8"): {"src": "np_mma.cu", "src_hash": "4ea4798e917ae3cc", "bytes_per_launch": 85347456},
+    ("dense", "llama2-7b-batch8"): {"src": "np_mma.cu", "src_hash": "4ea4798e917ae3cc", "bytes_per_launch": 281494272},
 }
 SRC_DIR = os.path.join(ROOT, "sparse_activation_decode_gb300", "csrc")
 
