@@ -74,6 +74,25 @@ def parse():
     return p.parse_args()
 
 
+def replica_seed(seed: int, rank: int) -> int:
+    """Each rank decodes its own independent sequence (its own inputs)."""
+    return seed + 7919 * rank
+
+
+def job_throughput(ms_local: float, steps: int, batch: int, world: int, device: str):
+    """The timed region's length as the maximum over ranks (barrier, then an
+    all-reduce MAX; one rank: its own) and the whole job's tokens per second:
+    every rank decodes `steps` tokens of `batch` sequences."""
+    import torch
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, world * steps * batch / (ms_max * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -359,7 +378,7 @@ def run_cuda(args):
         base = base.replace(lookahead=args.lookahead)
     span = (base.batch - 1) * base.phase_step + 24
     T = min(W + 3 * K, base.n_centroids - span if base.n_centroids else 10 ** 9)
-    cfg = base.replace(n_warm=0, n_decode=T, seed=base.seed + 7919 * rank)
+    cfg = base.replace(n_warm=0, n_decode=T, seed=replica_seed(base.seed, rank))
     B = cfg.batch
     t0 = time.time()
     # the host weight store in page-locked memory from the start
@@ -395,12 +414,7 @@ def run_cuda(args):
     # the host link is shared with other tenants of the machine: measure it
     # again right after the timed region
     h2d_after = h2d_peak_gbs(torch) if rank == 0 else None
-    ms_t = torch.tensor([ms], device="cuda")
-    if world > 1:
-        dist.barrier()
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = world * K * B / (ms_max * 1e-3)     # tokens: sequences x steps
+    ms_max, value = job_throughput(ms, K, B, world, "cuda")
 
     # live per-kernel durations (events on each kernel's own stream); few
     # enough tokens that the library keeps every launch in its timeline
