@@ -63,7 +63,8 @@ def parse():
                    help="residency policy (default: the workload's)")
     p.add_argument("--lookahead", type=int, default=None,
                    help="per-layer predictor: predict layer l from the input of layer l - k")
-    p.add_argument("--cpu-sample-tokens", type=int, default=3)
+    p.add_argument("--cpu-sample-tokens", type=int, default=16,
+                   help="oracle tokens timed for cpu_baseline (after a cold-start token; capped at ~30 s)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--profile-case", action="store_true",
@@ -434,16 +435,19 @@ def run_cuda(args):
     iso = isolated_kernels(dec, torch, cfg)
     # rows read over the host link and rows moved inside HBM per token
     # (synchronising stats calls, after every timed region of the decode)
-    n_st, din_rows, moved_rows = 16, 0, 0
+    n_st, din_rows, moved_rows, act_rows = 16, 0, 0, 0
     for k in range(n_st):
         st = dec.decode_token(tok(W + K + KP + k), stats=True)
         din_rows += st["din_rows"]
         moved_rows += st["moved_rows"]
+        act_rows += st["active_rows"]
     rec_b = cfg.n_proj * cfg.d_model * cfg.elem_bytes
     movement = {"tokens": n_st, "h2d_records_per_token": round(din_rows / n_st, 1),
                 "h2d_bytes_per_token": int(din_rows * rec_b / n_st),
                 "hbm_moved_records_per_token": round(moved_rows / n_st, 1),
-                "hbm_move_bytes_per_token": int(2 * moved_rows * rec_b / n_st)}
+                "hbm_move_bytes_per_token": int(2 * moved_rows * rec_b / n_st),
+                # rows reused from the previous token: 1 - |D_in| / |A| (the pages' persistence)
+                "measured_persistence": round(1.0 - din_rows / act_rows, 4) if act_rows else None}
 
     # end to end through host buffers (pinned), copies inside the timed region
     e2e = None
@@ -569,7 +573,7 @@ def main():
         return
     line, wl = res
     if not args.no_cpu_baseline and args.gpus == 1 and int(os.environ.get("WORLD_SIZE", "1")) == 1:
-        n, sec = run_oracle_tokens(wl, args.cpu_sample_tokens, budget_s=45)
+        n, sec = run_oracle_tokens(wl, args.cpu_sample_tokens, budget_s=30)
         nb = wl.cfg.batch
         line["cpu_baseline"] = {"value": round(n * nb / sec, 4), "unit": "tok/s", "cores": cores_used(),
                                 "kind": "oracle",
@@ -589,7 +593,7 @@ def run_reference(args):
     base = CONFIGS[args.config]
     if args.persistence is not None:
         base = base.replace(persistence=args.persistence)
-    n_tok = max(1, min(args.steps, 8))
+    n_tok = max(1, min(args.steps, 16))
     cfg = base.replace(n_warm=0, n_decode=n_tok + 1)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     wl = make_workload(cfg, device=dev)
