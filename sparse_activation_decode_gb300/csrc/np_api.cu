@@ -116,7 +116,7 @@ struct np_model {
   uint64_t pending_bits = 0, committed_since_token = 0;
   int64_t token = 0;
   int64_t launches = 0;
-  cudaEvent_t ev_set = nullptr, ev_side_done = nullptr, ev_j[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t ev_set = nullptr, ev_side_done = nullptr, ev_j[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
   cudaEvent_t ev_pre = nullptr, ev_ffn = nullptr;
   std::vector<cudaEvent_t> ev_g, ev_layer;  // per sparse layer: gathered, ready
   // profiling
@@ -129,6 +129,11 @@ struct np_model {
   cudaGraphExec_t graph = nullptr;
   cudaStream_t gs = nullptr;    // capture and replay stream (the caller's main stream may be the legacy one)
   cudaEvent_t ev_gin = nullptr, ev_gout = nullptr;
+  // per-layer predictor with a lookahead: predictor and set kernels on their
+  // own stream beside the FFNs (ev_pin: a source layer's input is final;
+  // ev_psrc: the predictions reading it are done)
+  cudaStream_t ps = nullptr;
+  cudaEvent_t ev_pin = nullptr, ev_psrc = nullptr;
   bool graph_off = false;       // disabled, or the capture failed
   int64_t graph_launches = 0;   // kernels in one replay
   int64_t eager_tokens = 0;     // tokens issued launch by launch (the first one sets kernel attributes)
@@ -497,8 +502,8 @@ cudaStream_t gather_stream(const np_model* m, int s) { return (s & 1) ? m->g1 : 
 
 // Make `st` wait for all work queued so far on the gather and scatter streams.
 np_status join_side(np_model* m, cudaStream_t st) {
-  const cudaStream_t src[4] = {m->side, m->g1, m->xs, m->fs};
-  for (int k = 0; k < 4; ++k) {
+  const cudaStream_t src[5] = {m->side, m->g1, m->xs, m->fs, m->ps};
+  for (int k = 0; k < 5; ++k) {
     CUDA_TRY(cudaEventRecord(m->ev_j[k], src[k]));
     CUDA_TRY(cudaStreamWaitEvent(st, m->ev_j[k], 0));
   }
@@ -945,7 +950,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
   e = cudaEventCreateWithFlags(&m->ev_side_done, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < 5; ++k) {
     e = cudaEventCreateWithFlags(&m->ev_j[k], cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
   }
@@ -968,6 +973,9 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_pre, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_ffn, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->gs, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->ps, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_pin, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_psrc, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_gin, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_gout, cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(cuda_fail(e, "cudaStreamCreate"));
@@ -990,6 +998,9 @@ np_status np_free_model(np_model* m) {
   if (m->xs) cudaStreamDestroy(m->xs);
   if (m->fs) cudaStreamDestroy(m->fs);
   if (m->gs) cudaStreamDestroy(m->gs);
+  if (m->ps) cudaStreamDestroy(m->ps);
+  if (m->ev_pin) cudaEventDestroy(m->ev_pin);
+  if (m->ev_psrc) cudaEventDestroy(m->ev_psrc);
   if (m->ev_gin) cudaEventDestroy(m->ev_gin);
   if (m->ev_gout) cudaEventDestroy(m->ev_gout);
   if (m->ev_pre) cudaEventDestroy(m->ev_pre);
@@ -1258,18 +1269,40 @@ np_status enqueue_token(np_model* m, float* h_dev) {
     // before that layer's FFN, so with a lookahead k > 0 the reads of layer
     // j run on the gather streams during the FFNs of layers j - k .. j - 1.
     // (A model with the shared predictor gets here only without sparse layers.)
+    // With a lookahead the predictor and set kernels run on their own stream
+    // (ps) beside the FFNs: the predictions reading the input of layer l wait
+    // for the FFN of layer l - 1, and the FFN of layer l + 1, which reuses the
+    // buffers holding that input, waits for them.
     const int k = m->lookahead;
-    int next = m->dn;  // next sparse layer to predict
+    const bool split = !shared && k > 0;
+    cudaStream_t main_st = m->main;
+    bool pred_pending = false;  // predictions of the previous source layer on ps
+    int next = m->dn;           // next sparse layer to predict
     for (int l = 0; l < m->L; ++l) {
+      if (split && pred_pending) {
+        CUDA_TRY(cudaStreamWaitEvent(main_st, m->ev_psrc, 0));
+        pred_pending = false;
+      }
       const int upto = l == 0 ? k : l + k;  // layers whose predictor reads the input of layer l
+      if (split && !shared && next < m->L && next <= upto) {
+        CUDA_TRY(cudaEventRecord(m->ev_pin, main_st));
+        CUDA_TRY(cudaStreamWaitEvent(m->ps, m->ev_pin, 0));
+      }
       for (; !shared && next < m->L && next <= upto; ++next) {
         const int s = next - m->dn;
         const int src = next - k > 0 ? next - k : 0;
-        NP_TRY(enqueue_predict(m, next, base_of(src), true, src == 0 ? nullptr : chain_y(m, src - 1)));
-        NP_TRY(enqueue_set(m, s, 1, nullptr, m->fire));
+        if (split) m->main = m->ps;
+        np_status rs = enqueue_predict(m, next, base_of(src), true, src == 0 ? nullptr : chain_y(m, src - 1));
+        if (rs == NP_OK) rs = enqueue_set(m, s, 1, nullptr, m->fire);
+        m->main = main_st;
+        NP_TRY(rs);
+        if (split) {
+          CUDA_TRY(cudaEventRecord(m->ev_psrc, m->ps));
+          pred_pending = true;
+        }
         m->pending_bits |= 1ull << s;
         size_t n_moved = 0;
-        const np_status rs = move_layers(m, std::vector<int>{s}, &n_moved);
+        rs = move_layers(m, std::vector<int>{s}, &n_moved);
         if (rs != NP_OK) {
           // earlier layers of this token already hold their new rows: put the
           // previous contents back and undo the whole token's delta
@@ -1282,6 +1315,7 @@ np_status enqueue_token(np_model* m, float* h_dev) {
       if (l >= m->dn) CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_layer[l - m->dn], 0));
       NP_TRY(ffn_layer(m->main, l));
     }
+    if (split && pred_pending) CUDA_TRY(cudaStreamWaitEvent(main_st, m->ev_psrc, 0));
   }
   if (m->L > 0) {
     const int l = m->L - 1;
