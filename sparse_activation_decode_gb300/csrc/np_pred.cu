@@ -35,6 +35,7 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
 
 template <typename T, int RPS>
 __global__ void __launch_bounds__(kThreads, 2) rowdot_kernel(RowdotLaunch a) {
+  static_assert(RPS <= 32 && 32 % RPS == 0, "a group's rows must share one mask word");
   constexpr int E = Elem<T>::E;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -134,20 +135,30 @@ __global__ void __launch_bounds__(kThreads, 2) rowdot_kernel(RowdotLaunch a) {
       issue(j - 1 + a.n_stages);
       ++issued_upto;
     }
-    if (tid < nr) {
+    const int row0 = ((int)blockIdx.x + j * (int)gridDim.x) * RPS;
+    if (a.mode == 2) {
+      // the group's RPS rows share one 32-bit word of the firing mask (RPS
+      // divides 32 and row0 is a multiple of RPS): one OR per group
+      if (warp == 0) {
+        bool fires = false;
+        if (tid < nr) {
+          float dot = 0.f;
+#pragma unroll
+          for (int w = 0; w < kThreads / 32; ++w) dot += rb[w * RPS + tid];
+          const float logit = dot + to_f32<T>(static_cast<const T*>(a.bias)[row0 + tid]);
+          if (a.out_f) a.out_f[row0 + tid] = logit;
+          fires = logit > 0.f;
+        }
+        const uint32_t bits = __ballot_sync(0xffffffffu, fires);
+        if (tid == 0 && bits) atomicOr(&a.fire_bits[row0 >> 5], bits << (row0 & 31));
+      }
+    } else if (tid < nr) {
       float dot = 0.f;
 #pragma unroll
       for (int w = 0; w < kThreads / 32; ++w) dot += rb[w * RPS + tid];
-      const int row = ((int)blockIdx.x + j * (int)gridDim.x) * RPS + tid;
-      if (a.mode == 0) {
-        a.out_f[row] = dot > 0.f ? dot : 0.f;
-      } else if (a.mode == 1) {
-        atomicMax(&a.keys[row / a.C], argmax_key(dot, row % a.C));
-      } else {
-        const float logit = dot + to_f32<T>(static_cast<const T*>(a.bias)[row]);
-        if (a.out_f) a.out_f[row] = logit;
-        if (logit > 0.f) atomicOr(&a.fire_bits[row >> 5], 1u << (row & 31));
-      }
+      const int row = row0 + tid;
+      if (a.mode == 0) a.out_f[row] = dot > 0.f ? dot : 0.f;
+      else atomicMax(&a.keys[row / a.C], argmax_key(dot, row % a.C));
     }
   }
   if (aborted && tid == 0) {
