@@ -45,12 +45,17 @@ def _digest() -> str:
     return h.hexdigest()
 
 
+def _read(path):
+    with open(path) as f:
+        return f.read()
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Build libnp.so if its sources changed; return its path."""
     os.makedirs(BUILD_DIR, exist_ok=True)
     stamp = os.path.join(BUILD_DIR, "stamp")
     dig = _digest()
-    if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == dig:
+    if not force and os.path.exists(LIB) and os.path.exists(stamp) and _read(stamp) == dig:
         return LIB
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []

@@ -58,7 +58,8 @@ def test_header_fields_all_mirrored():
     # every field the header declares in these structs has a ctypes twin
     import re
     from sparse_activation_decode_gb300 import _lib as L
-    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "np.h")).read(), flags=re.S)
+    with open(os.path.join(ROOT, "include", "np.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
     for cname, pyname in STRUCTS.items():
         body = re.search(r"typedef struct \{([^{}]*)\}\s*" + cname + ";", text).group(1)
         names = re.findall(r"(\w+)\s*(?:\[[^\]]*\])?\s*;", body)

@@ -11,7 +11,8 @@ HEADER = os.path.join(ROOT, "include", "np.h")
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:np_status|const char\*|int64_t)\s+(np_\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
