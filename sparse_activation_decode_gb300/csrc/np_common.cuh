@@ -12,15 +12,20 @@ namespace np {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
 
 // Raise a kernel's dynamic shared-memory limit only when a launch needs more
-// than it was last set to (the attribute call costs host time on every
-// launch otherwise).  One cache per kernel function (`Tag`); the attribute
-// is idempotent, so a race between threads only repeats the call.
+// than it was last set to on this device (the attribute call costs host time
+// on every launch otherwise).  One cache per kernel function (`Tag`) and
+// device; the attribute is idempotent, so a race between threads only
+// repeats the call.
 template <typename Tag>
 inline cudaError_t ensure_dyn_smem(const void* kern, size_t bytes) {
-  static size_t set_to = 0;
-  if (bytes <= set_to) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) set_to = bytes;
+  constexpr int kDevices = 64;
+  static size_t set_to[kDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kDevices && bytes <= set_to[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < kDevices) set_to[dev] = bytes;
   return e;
 }
 
