@@ -107,7 +107,12 @@ struct np_model {
   // launch shapes
   int ffn_grid = 0, ffn_stages = 0;
   int chain_grid = 0, chain_stages = 0;  // persistent FFN chain (batch 1)
-  int pdl_mask = 1;                      // programmatic dependent launch: 1 predictor, 2 set kernel
+  int pdl_mask = 1;                      // programmatic dependent launch: 1 predictor, 2 set kernel, 4 tensor-core kernels
+  // streams whose last operation is a kernel launched by the current API
+  // call (only the next kernel on such a stream may use programmatic
+  // dependent launch, see join())
+  cudaStream_t ours[8] = {};
+  int n_ours = 0;
   unsigned* arrive = nullptr;            // [2L] arrival counters of the chain
   float* chain_part = nullptr;           // [chain_grid][D] partial y of the chain
   int gather_grid = 0, scatter_grid = 0, pred_grid = 0;
@@ -229,6 +234,48 @@ np_status prof_end(np_model* m, int kind, cudaStream_t st, const EventPair& ep) 
   return NP_OK;
 }
 
+bool is_ours(const np_model* m, cudaStream_t st) {
+  for (int i = 0; i < m->n_ours; ++i)
+    if (m->ours[i] == st) return true;
+  return false;
+}
+
+// The next kernel on `st` follows something other than one of this call's
+// kernels (an event wait, a copy, or the caller's own work).
+void forget(np_model* m, cudaStream_t st) {
+  for (int i = 0; i < m->n_ours; ++i)
+    if (m->ours[i] == st) {
+      m->ours[i] = m->ours[--m->n_ours];
+      return;
+    }
+}
+
+// Programmatic dependent launch is used only between two kernels of one
+// call, back to back on one stream.  Kernels launched with it read data that
+// does not depend on the previous kernel (weights, the row count) before
+// their griddepcontrol.wait, which is sound only when the relaxed dependency
+// is that previous kernel.  Measured on this GPU and driver: eagerly, a
+// kernel after an event wait keeps full dependencies anyway; under stream
+// capture, a kernel whose only dependency is one kernel node gets a
+// programmatic edge even when that node comes from another stream through
+// the event, so the kernel could read rows before the copy that wrote them
+// is visible.  Hence every event wait, copy and API entry ends the chain.
+np_status join(np_model* m, cudaStream_t st, cudaEvent_t ev) {
+  CUDA_TRY(cudaStreamWaitEvent(st, ev, 0));
+  forget(m, st);
+  return NP_OK;
+}
+
+// Programmatic dependent launch for the next kernel on `st`: allowed by the
+// mask `bit` (0: always) and the stream's last operation is one of this
+// call's kernels.
+int pdl_for(const np_model* m, cudaStream_t st, int bit) {
+  return (bit == 0 || (m->pdl_mask & bit) != 0) && is_ours(m, st) ? 1 : 0;
+}
+
+// Start of a public call: no stream's last operation is one of its kernels.
+void begin_call(np_model* m) { m->n_ours = 0; }
+
 // Launch one kernel (a callable returning cudaError_t), optionally timed.
 template <typename Fn>
 np_status launch(np_model* m, int kind, cudaStream_t st, int64_t fixed_bytes, Fn fn) {
@@ -236,6 +283,7 @@ np_status launch(np_model* m, int kind, cudaStream_t st, int64_t fixed_bytes, Fn
   if (m->prof) NP_TRY(prof_begin(m, kind, st, &ep));
   cudaError_t e = fn();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  if (!is_ours(m, st) && m->n_ours < 8) m->ours[m->n_ours++] = st;
   m->launches += 1;
   if (m->prof) {
     m->prof_fixed_bytes[kind] += fixed_bytes;
@@ -277,6 +325,7 @@ np_status enqueue_ffn(np_model* m, cudaStream_t st, int kind, const unsigned cha
   a.n_stages = m->ffn_stages;
   a.grid = m->ffn_grid;
   a.err = m->err;
+  a.pdl = pdl_for(m, st, 0);
   return launch(m, kind, st, fixed_bytes, [&] { return launch_ffn_rows(a, st); });
 }
 
@@ -316,6 +365,7 @@ np_status enqueue_mma(np_model* m, cudaStream_t st, int kind, int mode, const Ro
                       MmaArgs& a, int64_t fixed_bytes) {
   a.B = m->B;
   a.swiglu = m->d.activation == NP_ACT_SWIGLU;
+  a.pdl = pdl_for(m, st, 4);
   a.err = m->err;
   const int bf16 = m->d.dtype == NP_BF16;
   return launch(m, kind, st, fixed_bytes, [&] { return launch_mma_rows(mode, bf16, map, a, p, st); });
@@ -410,10 +460,10 @@ np_status enqueue_rowdot(np_model* m, const void* W, int n_rows, int len, const 
   a.dtype_bytes = m->esz;
   a.rows_per_stage = rps;
   a.n_stages = ns;
-  a.pdl = (m->pdl_mask & 1) != 0;
   a.grid = m->pred_grid;
   a.err = m->err;
   cudaStream_t st = m->main;
+  a.pdl = pdl_for(m, st, 1);
   return launch(m, NP_KIND_PRED, st, (int64_t)n_rows * len * m->esz, [&] { return launch_rowdot(a, st); });
 }
 
@@ -470,6 +520,7 @@ np_status enqueue_set(np_model* m, int first_sparse, int n_layers, const int* id
   a.ids_out = keys ? m->ids : nullptr;
   a.fire = fire;
   cudaStream_t st = m->main;
+  a.pdl = pdl_for(m, st, 2);
   NP_TRY(launch(m, NP_KIND_SET, st, (int64_t)n_layers * m->W * 4 * 2 * m->B, [&] { return launch_set(a, st); }));
   CUDA_TRY(cudaEventRecord(m->ev_set, st));
   return NP_OK;
@@ -505,7 +556,7 @@ np_status join_side(np_model* m, cudaStream_t st) {
   const cudaStream_t src[5] = {m->side, m->g1, m->xs, m->fs, m->ps};
   for (int k = 0; k < 5; ++k) {
     CUDA_TRY(cudaEventRecord(m->ev_j[k], src[k]));
-    CUDA_TRY(cudaStreamWaitEvent(st, m->ev_j[k], 0));
+    NP_TRY(join(m, st, m->ev_j[k]));
   }
   return NP_OK;
 }
@@ -531,14 +582,14 @@ np_status enqueue_move(np_model* m, int s) {
   }
   for (int c = 0; c * m->staging_rows < m->K; ++c) {
     // staging buffer s%2 is free once the scatter that last read it is done
-    if (c > 0) CUDA_TRY(cudaStreamWaitEvent(g, m->ev_layer[s], 0));
-    else if (s >= 2) CUDA_TRY(cudaStreamWaitEvent(g, m->ev_layer[s - 2], 0));
+    if (c > 0) NP_TRY(join(m, g, m->ev_layer[s]));
+    else if (s >= 2) NP_TRY(join(m, g, m->ev_layer[s - 2]));
     a.chunk_begin = c * m->staging_rows;
     a.chunk_cap = m->staging_rows;
     a.grid = m->gather_grid;
     NP_TRY(launch(m, NP_KIND_GATHER, g, 0, [&] { return launch_gather(a, g); }));
     CUDA_TRY(cudaEventRecord(m->ev_g[s], g));
-    CUDA_TRY(cudaStreamWaitEvent(x, m->ev_g[s], 0));
+    NP_TRY(join(m, x, m->ev_g[s]));
     a.grid = m->scatter_grid;
     NP_TRY(launch(m, NP_KIND_SCATTER, x, 0, [&] { return launch_scatter(a, x); }));
     CUDA_TRY(cudaEventRecord(m->ev_layer[s], x));
@@ -549,7 +600,7 @@ np_status enqueue_move(np_model* m, int s) {
 // Restore the slots written for sparse layer s by the pending delta.
 np_status enqueue_restore(np_model* m, int s) {
   cudaStream_t st = m->xs;
-  CUDA_TRY(cudaStreamWaitEvent(st, m->ev_layer[s], 0));
+  NP_TRY(join(m, st, m->ev_layer[s]));
   MoveLaunch a = move_args(m, s);
   a.din_oldct = m->din_oldct + (size_t)s * m->K;
   a.chunk_begin = 0;
@@ -592,7 +643,6 @@ SetLaunch set_args(np_model* m, int first_sparse, int n_layers) {
   a.ls_old = m->ls_old;
   a.totals = m->totals;
   a.slot_hw = m->slot_hw;
-  a.pdl = (m->pdl_mask & 2) != 0;
   a.compact = m->compact;
   a.mv_src = m->mv_src;
   a.mv_dst = m->mv_dst;
@@ -623,8 +673,8 @@ np_status abort_pending(np_model* m, const std::vector<int>& moved) {
 // enqueued; the caller aborts the pending deltas.
 np_status move_layers(np_model* m, const std::vector<int>& layers, size_t* n_moved) {
   *n_moved = 0;
-  CUDA_TRY(cudaStreamWaitEvent(m->side, m->ev_set, 0));
-  CUDA_TRY(cudaStreamWaitEvent(m->g1, m->ev_set, 0));
+  NP_TRY(join(m, m->side, m->ev_set));
+  NP_TRY(join(m, m->g1, m->ev_set));
   for (size_t k = 0; k < layers.size(); ++k) {
     const int s = layers[k];
     if (m->d.read_hook && m->d.read_hook(m->d.read_ctx, m->dn + s, (int32_t)m->token) != 0) {
@@ -1029,6 +1079,7 @@ np_status np_free_model(np_model* m) {
 
 np_status np_reset_sequence(np_model* m) {
   if (!m) return arg_fail("model is null");
+  begin_call(m);
   // a delta that was never scattered already changed the slot contents
   if (m->pending_bits) NP_TRY(abort_pending(m, std::vector<int>()));
   m->pending_bits = 0;
@@ -1038,6 +1089,7 @@ np_status np_reset_sequence(np_model* m) {
   cudaStream_t st = m->main;
   NP_TRY(join_side(m, st));
   CUDA_TRY(cudaMemsetAsync(m->token_dev, 0, sizeof(int), st));
+  forget(m, st);
   return launch(m, NP_KIND_SET, st, 0, [&] {
     return launch_reset_state(m->slotmap, m->inv, m->resbits, m->slot_hw, m->frequency ? m->last_seen : nullptr, m->S,
                               m->F, m->K, m->W, st);
@@ -1046,16 +1098,19 @@ np_status np_reset_sequence(np_model* m) {
 
 np_status np_predict(np_model* m, int32_t layer, const float* h_dev, void* out_dev) {
   if (!m || !h_dev || !out_dev) return arg_fail("null argument");
+  begin_call(m);
   if (!aligned16(h_dev)) return arg_fail("h_dev must be 16-byte aligned");
   if (m->d.pred_kind == NP_PRED_SHARED_ARGMAX) {
     if (layer != 0) return arg_fail("the shared predictor takes layer 0");
     NP_TRY(enqueue_predict(m, 0, h_dev));
     CUDA_TRY(cudaMemcpyAsync(out_dev, m->ids, sizeof(int) * m->B * m->NH, cudaMemcpyDeviceToDevice, m->main));
+    forget(m, m->main);
     return NP_OK;
   }
   if (layer < m->dn || layer >= m->L) return arg_fail("layer is not a sparse layer");
   NP_TRY(enqueue_predict(m, layer, h_dev));
   CUDA_TRY(cudaMemcpyAsync(out_dev, m->fire, sizeof(uint32_t) * m->W, cudaMemcpyDeviceToDevice, m->main));
+  forget(m, m->main);
   return NP_OK;
 }
 
@@ -1082,6 +1137,7 @@ np_status np_last_delta(np_model* m, np_delta_view* out) {
 
 np_status np_delta(np_model* m, int32_t layer, const void* pred_dev, np_delta_view* out) {
   if (!m || !pred_dev) return arg_fail("null argument");
+  begin_call(m);
   if (m->S == 0) return arg_fail("model has no sparse layers");
   const bool shared = m->d.pred_kind == NP_PRED_SHARED_ARGMAX;
   if (layer == -1) {
@@ -1109,6 +1165,7 @@ np_status np_delta(np_model* m, int32_t layer, const void* pred_dev, np_delta_vi
 
 np_status np_scatter(np_model* m, int32_t layer) {
   if (!m) return arg_fail("model is null");
+  begin_call(m);
   std::vector<int> layers;
   if (layer == -1) {
     for (int s = 0; s < m->S; ++s)
@@ -1136,24 +1193,29 @@ np_status np_scatter(np_model* m, int32_t layer) {
 
 np_status np_sparse_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_dev) {
   if (!m || !h_dev || !y_dev) return arg_fail("null argument");
+  begin_call(m);
   if (!aligned16(h_dev) || !aligned16(y_dev)) return arg_fail("h_dev and y_dev must be 16-byte aligned");
   if (layer < m->dn || layer >= m->L) return arg_fail("layer is not a sparse layer");
   if (h_dev == y_dev) return arg_fail("y_dev may not alias h_dev");
   CUDA_TRY(cudaMemsetAsync(y_dev, 0, sizeof(float) * m->B * m->D, m->main));
+  forget(m, m->main);
   return enqueue_layer_ffn(m, m->main, layer, h_dev, nullptr, nullptr, y_dev, nullptr);
 }
 
 np_status np_dense_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_dev) {
   if (!m || !h_dev || !y_dev) return arg_fail("null argument");
+  begin_call(m);
   if (!aligned16(h_dev) || !aligned16(y_dev)) return arg_fail("h_dev and y_dev must be 16-byte aligned");
   if (layer < 0 || layer >= m->dn) return arg_fail("layer is not a dense layer");
   if (h_dev == y_dev) return arg_fail("y_dev may not alias h_dev");
   CUDA_TRY(cudaMemsetAsync(y_dev, 0, sizeof(float) * m->B * m->D, m->main));
+  forget(m, m->main);
   return enqueue_layer_ffn(m, m->main, layer, h_dev, nullptr, nullptr, y_dev, nullptr);
 }
 
 np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev) {
   if (!m || !h_dev) return arg_fail("null argument");
+  begin_call(m);
   if (!aligned16(h_dev)) return arg_fail("h_dev must be 16-byte aligned");
   if (first < 0 || count < 1 || first + count > m->L) return arg_fail("layer range out of bounds");
   for (int l = first; l < first + count; ++l)
@@ -1164,9 +1226,11 @@ np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev)
   // the same chaining as np_decode_token, relative to `first`
   cudaStream_t st = m->main;
   CUDA_TRY(cudaMemsetAsync(chain_y(m, 0), 0, sizeof(float) * m->B * m->D, st));
+  forget(m, st);
   if (!m->tc) {
     // batch 1: one persistent kernel streams the whole range
     CUDA_TRY(cudaMemsetAsync(m->arrive, 0, sizeof(unsigned) * 2 * (size_t)count, st));
+    forget(m, st);
     FfnChainLaunch a{};
     a.dense_w = m->d.dense_w;
     a.bufs = m->bufs;
@@ -1218,6 +1282,7 @@ np_status enqueue_token(np_model* m, float* h_dev) {
                              l >= 1 ? chain_base(m, l) : nullptr, chain_y(m, l), chain_y(m, l + 1));
   };
   CUDA_TRY(cudaMemsetAsync(chain_y(m, 0), 0, sizeof(float) * m->B * m->D, m->main));
+  forget(m, m->main);
   cudaStream_t fin = m->main;
   if (shared && m->S > 0) {
     // main: dense layer 0, the predictor's hidden layer, then per layer
@@ -1228,7 +1293,7 @@ np_status enqueue_token(np_model* m, float* h_dev) {
     NP_TRY(ffn_layer(m->main, 0));
     NP_TRY(enqueue_pred_hidden(m, h_dev, chain_y(m, 0)));
     CUDA_TRY(cudaEventRecord(m->ev_pre, m->main));
-    CUDA_TRY(cudaStreamWaitEvent(m->fs, m->ev_pre, 0));
+    NP_TRY(join(m, m->fs, m->ev_pre));
     for (int l = 1; l < m->dn; ++l) NP_TRY(ffn_layer(m->fs, l));
     m->pending_bits = all_layers(m);
     std::vector<int> moved;
@@ -1243,6 +1308,7 @@ np_status enqueue_token(np_model* m, float* h_dev) {
       sa.keys = m->keys;
       sa.ids_out = last ? m->ids : nullptr;
       cudaStream_t st = m->main;
+      sa.pdl = pdl_for(m, st, 2);
       NP_TRY(launch(m, NP_KIND_SET, st, (int64_t)cnt * m->W * 8, [&] { return launch_set(sa, st); }));
       CUDA_TRY(cudaEventRecord(m->ev_set, st));
       std::vector<int> layers;
@@ -1259,7 +1325,7 @@ np_status enqueue_token(np_model* m, float* h_dev) {
       s0 += cnt;
     }
     for (int s = 0; s < m->S; ++s) {
-      CUDA_TRY(cudaStreamWaitEvent(m->fs, m->ev_layer[s], 0));
+      NP_TRY(join(m, m->fs, m->ev_layer[s]));
       NP_TRY(ffn_layer(m->fs, m->dn + s));
     }
     fin = m->fs;
@@ -1280,13 +1346,13 @@ np_status enqueue_token(np_model* m, float* h_dev) {
     int next = m->dn;           // next sparse layer to predict
     for (int l = 0; l < m->L; ++l) {
       if (split && pred_pending) {
-        CUDA_TRY(cudaStreamWaitEvent(main_st, m->ev_psrc, 0));
+        NP_TRY(join(m, main_st, m->ev_psrc));
         pred_pending = false;
       }
       const int upto = l == 0 ? k : l + k;  // layers whose predictor reads the input of layer l
       if (split && !shared && next < m->L && next <= upto) {
         CUDA_TRY(cudaEventRecord(m->ev_pin, main_st));
-        CUDA_TRY(cudaStreamWaitEvent(m->ps, m->ev_pin, 0));
+        NP_TRY(join(m, m->ps, m->ev_pin));
       }
       for (; !shared && next < m->L && next <= upto; ++next) {
         const int s = next - m->dn;
@@ -1312,10 +1378,10 @@ np_status enqueue_token(np_model* m, float* h_dev) {
           return rs;
         }
       }
-      if (l >= m->dn) CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_layer[l - m->dn], 0));
+      if (l >= m->dn) NP_TRY(join(m, m->main, m->ev_layer[l - m->dn]));
       NP_TRY(ffn_layer(m->main, l));
     }
-    if (split && pred_pending) CUDA_TRY(cudaStreamWaitEvent(main_st, m->ev_psrc, 0));
+    if (split && pred_pending) NP_TRY(join(m, main_st, m->ev_psrc));
   }
   if (m->L > 0) {
     const int l = m->L - 1;
@@ -1325,7 +1391,7 @@ np_status enqueue_token(np_model* m, float* h_dev) {
   }
   if (fin != m->main) {
     CUDA_TRY(cudaEventRecord(m->ev_ffn, fin));
-    CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_ffn, 0));
+    NP_TRY(join(m, m->main, m->ev_ffn));
   }
   if (m->S > 0) NP_TRY(bump_token(m));
   return NP_OK;
@@ -1338,6 +1404,7 @@ np_status capture_token(np_model* m) {
   const int64_t l0 = m->launches;
   cudaStream_t user_main = m->main;
   m->main = m->gs;  // the capture runs on the library's own stream
+  begin_call(m);    // the graph's first kernels follow its input copy
   cudaError_t e = cudaStreamBeginCapture(m->main, cudaStreamCaptureModeThreadLocal);
   if (e != cudaSuccess) {
     if (env_int("NP_TUNE_VERBOSE", 0) == 1) std::fprintf(stderr, "np: no capture: %s\n", cudaGetErrorString(e));
@@ -1349,6 +1416,7 @@ np_status capture_token(np_model* m) {
   const np_status st = enqueue_token(m, m->h_io);
   cudaGraph_t g = nullptr;
   e = cudaStreamEndCapture(m->main, &g);
+  begin_call(m);
   m->main = user_main;
   m->pending_bits = 0;  // the capture only recorded the work
   m->committed_since_token = 0;
@@ -1371,6 +1439,7 @@ np_status capture_token(np_model* m) {
 
 np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
   if (!m || !h_dev) return arg_fail("null argument");
+  begin_call(m);
   if (!aligned16(h_dev)) return arg_fail("h_dev must be 16-byte aligned");
   if (m->pending_bits) {
     g_last_err = "a delta is pending; call np_scatter first";
@@ -1384,12 +1453,14 @@ np_status np_decode_token(np_model* m, float* h_dev, np_stats* stats_host) {
   if (replay && m->graph) {
     const size_t bytes = sizeof(float) * m->B * m->D;
     CUDA_TRY(cudaMemcpyAsync(m->h_io, h_dev, bytes, cudaMemcpyDeviceToDevice, m->main));
+    forget(m, m->main);
     CUDA_TRY(cudaEventRecord(m->ev_gin, m->main));
-    CUDA_TRY(cudaStreamWaitEvent(m->gs, m->ev_gin, 0));
+    NP_TRY(join(m, m->gs, m->ev_gin));
     CUDA_TRY(cudaGraphLaunch(m->graph, m->gs));
     CUDA_TRY(cudaEventRecord(m->ev_gout, m->gs));
-    CUDA_TRY(cudaStreamWaitEvent(m->main, m->ev_gout, 0));
+    NP_TRY(join(m, m->main, m->ev_gout));
     CUDA_TRY(cudaMemcpyAsync(h_dev, m->h_io, bytes, cudaMemcpyDeviceToDevice, m->main));
+    forget(m, m->main);
     m->launches += m->graph_launches;
   } else {
     NP_TRY(enqueue_token(m, h_dev));

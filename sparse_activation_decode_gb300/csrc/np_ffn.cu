@@ -932,7 +932,7 @@ cudaError_t launch_ffn_rows(const FfnLaunch& a, cudaStream_t st) {
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.pdl ? 1 : 0;
   FfnLaunch arg = a;
   void* params[] = {&arg};
   return cudaLaunchKernelExC(&cfg, k, params);

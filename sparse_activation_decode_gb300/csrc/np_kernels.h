@@ -37,6 +37,7 @@ struct FfnLaunch {
   int swiglu;             // gated: silu(g.x) instead of relu(g.x)
   int n_stages;
   int grid;
+  int pdl;                  // launch with programmatic dependent launch
   int* err;
 };
 size_t ffn_smem_bytes(int D, int dtype_bytes, int nproj, int n_stages);
@@ -215,6 +216,7 @@ struct MmaArgs {
   int swiglu;               // gated FFN: silu(g.x) instead of relu(g.x)
   int n_stages;
   uint32_t stage_bytes;
+  int pdl;                  // launch with programmatic dependent launch
   int* err;
 };
 struct MmaPlan {

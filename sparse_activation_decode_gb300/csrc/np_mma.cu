@@ -40,6 +40,14 @@
 // and the CTAs of cluster 0 store h and clear the next accumulator, so
 // consecutive layers chain without an extra kernel.
 //
+// Programmatic dependent launch: the weights and the row count do not depend
+// on the previous kernel in the stream (the set kernel and the reads that
+// fill the resident buffers reach this stream through events, which stay
+// full dependencies), so the producer streams as soon as the CTA is
+// resident; the epilogue warps wait for the previous kernel before they read
+// its outputs or write anything.  Every CTA waits, so a kernel that follows
+// this one also follows its predecessor.
+//
 // Every wait is bounded (about one second): a timeout records an error word,
 // lets the other roles of the CTA stop early, waits for the copies and MMAs
 // already in flight, frees the tensor memory and returns.
@@ -143,6 +151,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
   const int slice0 = (int)rank * ks;
   const int Kd = a.Kdim;
 
+  grid_dependents_launch();  // the next layer may start streaming its weights
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(reinterpret_cast<uint64_t*>(sm) + kBarFull + s, 1);
@@ -331,6 +340,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
     const int Q = warp & 3;
     const int t = 32 * Q + lane;  // tile row <-> tensor-memory lane
     const int B = a.B;
+    grid_dependency_wait();  // the previous kernel's outputs are visible from here on
 
     // prologue: input operand of this CTA's column slice
     if (MODE == kMmaHeads) {
@@ -593,23 +603,27 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
   cluster_sync_all();  // no CTA leaves while another may still write into its shared memory
 }
 
+template <int MODE, bool BF16> struct MmaSmemTag {};
+
 template <int MODE, bool BF16>
 cudaError_t launch_mode(const RowMaps& maps, const MmaArgs& a, size_t smem, cudaStream_t st) {
   auto kern = mma_rows_kernel<MODE, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dyn_smem<MmaSmemTag<MODE, BF16>>(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(a.n_clusters * a.cs));
   cfg.blockDim = dim3(kMmaThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)a.cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, maps.m32, maps.m8, a);
 }
 
