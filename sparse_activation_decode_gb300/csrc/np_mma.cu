@@ -152,6 +152,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
   const int Kd = a.Kdim;
 
   grid_dependents_launch();  // the next layer may start streaming its weights
+  // the row count is loaded while the barriers are set up
+  int n = a.n_rows_dev ? *a.n_rows_dev : a.n_rows_host;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(reinterpret_cast<uint64_t*>(sm) + kBarFull + s, 1);
@@ -183,7 +185,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
   volatile int* abort = misc + 1;
   cluster_sync_all();  // every barrier of the cluster is initialised
 
-  int n = a.n_rows_dev ? *a.n_rows_dev : a.n_rows_host;
   n = n < 0 ? 0 : (n > a.row_cap ? a.row_cap : n);
   const int G = a.n_clusters;
   const int r_begin = (int)((long long)cid * n / G), r_end = (int)((long long)(cid + 1) * n / G);
@@ -354,13 +355,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
     } else {
       // sum of squares of h = hb + yprev over this CTA's slice; the CTAs of
       // the cluster cover every column once, so the slice sums are exchanged
-      // and added in rank order
-      float ss[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) ss[b] = 0.f;
+      // and added in rank order.  A slice of at most 256 four-column groups
+      // (two per thread) stays in registers: every load is issued at once
+      // and the operand is written from the same values after the exchange.
       const int S4 = ks / 4;
-      for (int i = e; i < S4; i += 128) {
-        float4 v[8];
+      const bool resident = S4 <= 256;
+      auto load_h = [&](int i, float4 (&v)[8]) {
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
           v[b] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -374,12 +374,37 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
               v[b].x += w.x; v[b].y += w.y; v[b].z += w.z; v[b].w += w.w;
             }
         }
+      };
+      float ss[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) ss[b] = 0.f;
+      auto add_ss = [&](const float4 (&v)[8]) {
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
           ss[b] = fmaf(v[b].x, v[b].x, ss[b]);
           ss[b] = fmaf(v[b].y, v[b].y, ss[b]);
           ss[b] = fmaf(v[b].z, v[b].z, ss[b]);
           ss[b] = fmaf(v[b].w, v[b].w, ss[b]);
+        }
+      };
+      float4 hr[2][8];
+      if (resident) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          if (e + 128 * q < S4) {
+            load_h(e + 128 * q, hr[q]);
+          } else {
+#pragma unroll
+            for (int b = 0; b < 8; ++b) hr[q][b] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) add_ss(hr[q]);
+      } else {
+        for (int i = e; i < S4; i += 128) {
+          float4 v[8];
+          load_h(i, v);
+          add_ss(v);
         }
       }
 #pragma unroll
@@ -411,22 +436,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
       // x = h * inv as hi/lo operand rows (row b = hi, row 8 + b = lo), four
       // columns per step; cluster 0 also stores h and clears the next y
       uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kSmemHeader);
-      for (int i = e; i < S4; i += 128) {
+      auto emit = [&](int i, const float4 (&v)[8]) {
         const int k = 4 * i, d = slice0 + k;
-        float4 v[8];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          v[b] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (b < B) v[b] = *reinterpret_cast<const float4*>(a.hb + (size_t)b * Kd + d);
-        }
-        if (a.yprev) {
-#pragma unroll
-          for (int b = 0; b < 8; ++b)
-            if (b < B) {
-              const float4 w = *reinterpret_cast<const float4*>(a.yprev + (size_t)b * Kd + d);
-              v[b].x += w.x; v[b].y += w.y; v[b].z += w.z; v[b].w += w.w;
-            }
-        }
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
           if (cid == 0 && b < B) {
@@ -443,6 +454,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_rows_kernel(const __grid_c
           xw[kmajor_off(b, k + 2, 16) >> 2] = (uint32_t)hi[2] | ((uint32_t)hi[3] << 16);
           xw[kmajor_off(8 + b, k, 16) >> 2] = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
           xw[kmajor_off(8 + b, k + 2, 16) >> 2] = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);
+        }
+      };
+      if (resident) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (e + 128 * q < S4) emit(e + 128 * q, hr[q]);
+      } else {
+        for (int i = e; i < S4; i += 128) {
+          float4 v[8];
+          load_h(i, v);
+          emit(i, v);
         }
       }
       if (MODE == kMmaHidden && a.keys_zero && blockIdx.x == 0)
