@@ -255,6 +255,26 @@ def test_full_size_sampled(cfg, tokens):
     assert summ["max_h_rel"] < FFN_TOL
 
 
+@pytest.mark.parametrize("cfg,tokens,kw", [(SMALL_BATCHED.replace(slots="compact"), 6, {}),
+                                           (SMALL_OPT.replace(lookahead=2), 6, {"h2d_mode": "fused"}),
+                                           (BATCHED7B.replace(slots="compact"), 3,
+                                            {"check_buffers": False, "sample_slots": 64})],
+                         ids=["small-batched-compact", "small-opt-lookahead2-fused", "llama2-7b-batch8-compact"])
+def test_programmatic_launch_on_every_kernel(cfg, tokens, kw, monkeypatch):
+    # every kernel kind that supports programmatic dependent launch asks for
+    # it (predictor, set kernel, tensor-core kernels; the FFN always does);
+    # the library grants it only between two kernels of one call back to
+    # back on one stream, so the results must agree with the oracle as they
+    # do without it.  The full-size 8-sequence compact case changed h
+    # (rel-L2 3e-3) when a captured dependency on another stream's kernel
+    # was relaxed.
+    monkeypatch.setenv("NP_TUNE_PDL", "7")
+    wl = make_workload(cfg.replace(n_warm=0, n_decode=tokens), device="cuda")
+    summ = run_and_compare(wl, tokens, **kw)
+    assert summ["tokens"] == tokens
+    assert summ["max_h_rel"] < FFN_TOL
+
+
 @pytest.mark.parametrize("cfg", [SMALL_F16, SMALL_BATCHED, SMALL_F16.replace(activation="swiglu"),
                                  SMALL_F16.replace(slots="compact"), SMALL_OPT.replace(slots="compact"),
                                  SMALL_BF16.replace(name="wide-bf16", d_model=5120, d_ff=1024, k_max=256,
