@@ -107,7 +107,7 @@ struct np_model {
   // launch shapes
   int ffn_grid = 0, ffn_stages = 0;
   int chain_grid = 0, chain_stages = 0;  // persistent FFN chain (batch 1)
-  int pdl_mask = 1;                      // programmatic dependent launch: 1 predictor, 2 set kernel, 4 tensor-core kernels
+  int pdl_mask = 5;                      // programmatic dependent launch: 1 predictor, 2 set kernel, 4 tensor-core kernels
   // streams whose last operation is a kernel launched by the current API
   // call (only the next kernel on such a stream may use programmatic
   // dependent launch, see join())
@@ -914,7 +914,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   // their grids small leaves the SMs to the FFN running beside them.
   // NP_TUNE_GATHER_CTAS / NP_TUNE_SCATTER_CTAS override the defaults.
   m->graph_off = env_int("NP_TUNE_GRAPH", 1) == 0;
-  m->pdl_mask = env_int("NP_TUNE_PDL", 1);
+  m->pdl_mask = env_int("NP_TUNE_PDL", 5);
   m->gather_grid = env_int("NP_TUNE_GATHER_CTAS", 32);
   m->scatter_grid = env_int("NP_TUNE_SCATTER_CTAS", 4 * m->sms);
   m->pred_grid = 2 * m->sms;
