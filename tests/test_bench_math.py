@@ -59,3 +59,17 @@ def test_recorded_traffic_entries_name_existing_sources():
     for (kind, workload), ent in bench.NCU_TRAFFIC.items():
         assert bench.os.path.exists(bench.os.path.join(bench.SRC_DIR, ent["src"])), (kind, workload)
         assert len(ent["src_hash"]) == 16 and ent["bytes_per_launch"] > 0
+
+
+def test_clock_summary_parses_nvidia_smi_lines():
+    cs = bench.ClockSampler(0)
+    cs.lines = ["2070, 2070, 812.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+                "1980, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+                "garbage line",
+                "[N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+                "2040, 2070, 1100.1, 0x0000000000000008, Active, Not Active, Not Active, Not Active"]
+    s = cs.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2040.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    empty = bench.ClockSampler(0).summary()
+    assert empty == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
