@@ -102,3 +102,17 @@ def test_valid_description_reaches_cuda_and_fails_cleanly_without_a_gpu(lib):
     d = valid_desc(pred_kind=L.NP_PRED_PERLAYER_SIGMOID, n_dense=0, dense_w=None, pred_b2=FAKE,
                    residency=L.NP_RES_WINDOW, window=5, has_gate=0, lookahead=2, slots=L.NP_SLOTS_COMPACT)
     assert lib.np_init_model(ctypes.byref(d), ctypes.byref(out)) == L.NP_ERR_CUDA
+
+
+_INTS = (ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint32)
+
+
+@pytest.mark.parametrize("name", sorted(n for n, (res, args) in L.SIGNATURES.items()
+                                        if args and res is ctypes.c_int32 and n != "np_status_str"))
+def test_every_entry_point_rejects_null_arguments(lib, name):
+    # a null model (and null buffers, zero sizes) is an argument error, not a
+    # crash; freeing a null model is a no-op
+    res, args = L.SIGNATURES[name]
+    vals = [0 if a in _INTS else None for a in args]
+    expected = L.NP_OK if name == "np_free_model" else L.NP_ERR_ARG
+    assert getattr(lib, name)(*vals) == expected
