@@ -492,7 +492,9 @@ def run_cuda(args):
                 "peak": round(peak, 1), "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
                 "traffic": traffic_for(dk, cfg.name), "peak_source": peak_src,
                 "note": "host-link bound: records come from page-locked host memory; achieved = gathered bytes "
-                        "/ union of the gather launches' event intervals over the profiled region"
+                        "/ union of the gather launches' event intervals over the profiled region; traffic "
+                        "counts HBM bytes only (the link's bytes are not DRAM traffic and the written rows "
+                        "are still in L2 when the launch ends)"
                         if dv["bound"] == "host_link" else None}
     hbm_kernels = {}
     for k in ("ffn", "dense"):
