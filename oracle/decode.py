@@ -503,17 +503,51 @@ def rel_l2(got, ref) -> float:
     return float(num / den) if den > 0 else float(num)
 
 
-def fp32_dot_bound(w: np.ndarray, v: np.ndarray, v_rel_err: float) -> np.ndarray:
-    """Bound on |fp32 result - exact| for rows of w . v with fp32 accumulation
-    over k terms (error <= k * 2^-24 * sum |w_i v_i|, doubled for safety) plus
-    the propagated relative error of the input vector."""
+U32 = 2.0 ** -24   # unit roundoff of float32 (round to nearest)
+
+
+def gamma(n: int) -> float:
+    """gamma_n = n u / (1 - n u), u the float32 unit roundoff: the relative
+    error factor of n successive roundings (Higham, Accuracy and Stability of
+    Numerical Algorithms, Lemma 3.1)."""
+    return n * U32 / (1.0 - n * U32)
+
+
+def fp32_dot_bound(w: np.ndarray, v: np.ndarray, v_rel_err: float, depth: int | None = None) -> np.ndarray:
+    """Bound on |computed - exact| for each row of w . v evaluated in float32,
+    where the float32 inputs are exact copies of w and of a vector v' with
+    ||v' - v||_2 <= v_rel_err ||v||_2.
+
+    Rounding: any summation tree in which every product passes through at
+    most `depth` rounded additions (one rounding per fused multiply-add, two
+    for a multiply then an add) has |error| <= gamma_{depth+1} sum_i |w_i v'_i|
+    (Higham, Lemma 3.1 and the tree-height form of Section 4.2).  depth=None
+    takes the worst tree, a sequential sum over all k terms (depth k), so the
+    bound holds for every evaluation order.  Input: |w . (v' - v)| <=
+    ||w||_2 ||v' - v||_2 (Cauchy-Schwarz).  sum |w_i v'_i| is bounded by
+    sum |w_i| |v_i| + ||w||_2 ||v' - v||_2."""
     k = w.shape[-1]
-    mag = np.abs(w) @ np.abs(v)
-    return mag * (2.0 * k * 2.0 ** -24 + v_rel_err)
+    h = k if depth is None else int(depth)
+    wn = np.sqrt(np.sum(w * w, axis=-1))
+    din = wn * (v_rel_err * float(np.linalg.norm(v)))
+    mag = np.abs(w) @ np.abs(v) + din
+    return gamma(h + 1) * mag + din
 
 
-def argmax_tolerance(w1, w2, xhat, x_rel_err: float = 1e-5) -> np.ndarray:
-    """Per-logit error bound of an fp32 predictor evaluation."""
+def argmax_tolerance(w1, w2, xhat, x_rel_err: float = 1e-5, depth1: int | None = None,
+                     depth2: int | None = None, b2=None) -> np.ndarray:
+    """Per-logit error bound of a float32 evaluation of logits = W2 relu(W1 x)
+    (+ b2) whose input differs from x by at most x_rel_err (relative, 2-norm)
+    and whose two products accumulate in trees of height depth1 and depth2
+    (None: any order; with a bias, depth2 counts its addition as well).  relu
+    is 1-Lipschitz, so each hidden unit carries the bound of its
+    pre-activation, which W2 then propagates through |W2|.  The bias is a
+    term of the second sum with an exact factor 1."""
     z = np.maximum(w1 @ xhat, 0.0)
-    z_err = fp32_dot_bound(w1, xhat, x_rel_err)
-    return fp32_dot_bound(w2, z, 0.0) + np.abs(w2) @ z_err
+    z_err = fp32_dot_bound(w1, xhat, x_rel_err, depth1)
+    k2 = w2.shape[-1] + (0 if b2 is None else 1)
+    h2 = k2 if depth2 is None else int(depth2)
+    mag = np.abs(w2) @ (z + z_err)
+    if b2 is not None:
+        mag = mag + np.abs(np.asarray(b2, dtype=np.float64))
+    return gamma(h2 + 1) * mag + np.abs(w2) @ z_err

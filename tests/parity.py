@@ -18,6 +18,39 @@ from oracle import OracleDecoder
 
 FFN_TOL = 1e-3   # relative L2 of FFN outputs and of the residual stream
 
+# Near-tie acceptance (see oracle.argmax_tolerance).  The GPU's predictor
+# input is its own float32 residual stream, which differs from the oracle's by
+# accumulated rounding; X_REL bounds that difference (relative 2-norm) on the
+# CUDA-core path, X_REL_TC adds the 16+16-bit operand split of the tensor-core
+# path (hi + lo keeps about 17 significant bits: relative error <= 2^-17).
+# Whenever a near tie is accepted, the token's final residual stream must
+# itself be within X_REL of the oracle's, which checks the assumption.
+X_REL = 4e-6
+X_REL_TC = 1e-5
+
+
+def rowdot_depth(length: int, elem_bytes: int, bias: bool = False) -> int:
+    """Rounded additions on any product's path in the batch-1 predictor
+    kernel: a thread's chunks of 16 bytes (E elements each) by fused
+    multiply-adds, a 5-level warp tree, 8 warp partials added in order, and
+    the bias of the per-layer predictor."""
+    e = 16 // elem_bytes
+    chunks = -(-(length // e) // 256)
+    return e * chunks + 5 + 8 + (1 if bias else 0)
+
+
+def predictor_bound_args(cfg) -> dict:
+    """x_rel_err and accumulation depths of the predictor's two products on
+    the GPU path that decodes `cfg`.  The tensor-core path (batch > 1) is
+    given the any-order bound with twice the roundings (its accumulator's
+    rounding is not specified as round-to-nearest)."""
+    bias = cfg.pred_kind != "shared_argmax"
+    if cfg.batch > 1:
+        return {"x_rel_err": X_REL_TC, "depth1": 2 * (cfg.d_model + 1),
+                "depth2": 2 * (cfg.pred_hidden + 1)}
+    return {"x_rel_err": X_REL, "depth1": rowdot_depth(cfg.d_model, cfg.elem_bytes),
+            "depth2": rowdot_depth(cfg.pred_hidden, cfg.elem_bytes, bias)}
+
 
 def build_decoder(wl, **kw):
     from sparse_activation_decode_gb300 import decoder_for
@@ -27,12 +60,13 @@ def build_decoder(wl, **kw):
 def _ids_accept(rec, ids_gpu, cfg, w1, w2):
     """Per sequence and head, GPU id must be within the fp32 bound of the max."""
     near = 0
+    args = predictor_bound_args(cfg)
     for b in range(cfg.batch):
         lg = rec.logits[b].reshape(cfg.n_heads, cfg.n_centroids)
         own = lg.argmax(axis=1)
         if np.array_equal(own, ids_gpu[b]):
             continue
-        eps = oracle.argmax_tolerance(w1, w2, rec.pred_xhat[b]).reshape(cfg.n_heads, cfg.n_centroids)
+        eps = oracle.argmax_tolerance(w1, w2, rec.pred_xhat[b], **args).reshape(cfg.n_heads, cfg.n_centroids)
         for h in np.flatnonzero(own != ids_gpu[b]):
             g = int(ids_gpu[b][h])
             assert 0 <= g < cfg.n_centroids
@@ -43,12 +77,14 @@ def _ids_accept(rec, ids_gpu, cfg, w1, w2):
     return near
 
 
-def _fire_accept(rec, fire_gpu, s, w1, w2):
+def _fire_accept(rec, fire_gpu, s, w1, w2, b2, cfg):
+    """Firing decisions: where the GPU disagrees with logit > 0, the oracle's
+    logit must be within the fp32 bound of zero."""
     lg = rec.pred_logits_layer[s]
     ref = lg > 0.0
     diff = np.flatnonzero(ref != fire_gpu)
     if diff.size:
-        eps = oracle.argmax_tolerance(w1, w2, rec.pred_xhat[s])
+        eps = oracle.argmax_tolerance(w1, w2, rec.pred_xhat[s], b2=b2, **predictor_bound_args(cfg))
         for n in diff:
             assert abs(lg[n]) <= eps[n], f"neuron {n}: logit {lg[n]} bound {eps[n]}"
     return int(diff.size)
@@ -73,6 +109,7 @@ def run_and_compare(wl, n_tokens=None, *, h2d_mode="staged", staging_rows=None, 
     summary = {"max_h_rel": 0.0, "max_y_rel": 0.0, "near_ties": 0, "din_rows": 0, "tokens": 0}
     try:
         for t in range(start, start + T):
+            near_before = summary["near_ties"]
             x = (wl.x[t] if inputs is None else inputs[t - start])
             h = x.to("cuda", torch.float32).contiguous().clone()
             st = dec.decode_token(h, stats=True)
@@ -98,7 +135,8 @@ def run_and_compare(wl, n_tokens=None, *, h2d_mode="staged", staging_rows=None, 
                 for s in range(cfg.n_sparse):
                     layer = cfg.n_dense + s
                     summary["near_ties"] += _fire_accept(rec, fire[s], s, oracle.f64(wl.pred_w1[layer]),
-                                                         oracle.f64(wl.pred_w2[layer]))
+                                                         oracle.f64(wl.pred_w2[layer]),
+                                                         oracle.f64(wl.pred_b2[layer]), cfg)
             # ---- bit-exact integer state
             for s in range(cfg.n_sparse):
                 a_ref = rec.active[s]
@@ -132,6 +170,11 @@ def run_and_compare(wl, n_tokens=None, *, h2d_mode="staged", staging_rows=None, 
             rel = max(oracle.rel_l2(hg[b], rec.h[b]) for b in range(cfg.batch))
             summary["max_h_rel"] = max(summary["max_h_rel"], rel)
             assert rel <= FFN_TOL, f"token {t}: h rel-L2 {rel}"
+            if summary["near_ties"] > near_before:
+                # the acceptance bound assumed the GPU's input error stays
+                # within x_rel_err: check it on this token's residual stream
+                x_rel = predictor_bound_args(cfg)["x_rel_err"]
+                assert rel <= x_rel, f"token {t}: near tie accepted but h rel-L2 {rel} > {x_rel}"
             # ---- per-layer FFN outputs through the standalone entry points
             if check_layer_y:
                 for l in range(cfg.n_dense):
