@@ -334,19 +334,32 @@ np_status np_host_unregister(void* ptr);
  * Computes y = sum over the listed rows r of relu(g_r . x)(u_r . x) d_r
  * (relu(u_r . x) d_r when has_gate = 0) with x = rmsnorm(h) — the kernel of
  * np_sparse_mlp — and writes y_dev [d_model].  Rows: rows_dev[0..n_rows) are
- * row indices into w_gate/w_up/w_down ([row_limit][d_model] each), or NULL
- * for rows 0..n_rows-1.  All pointers are device pointers, 16-byte aligned;
+ * int32 row indices into w_gate/w_up/w_down ([row_limit][d_model] each, all
+ * three of that size), or NULL for rows 0..n_rows-1; n_rows = 0 gives y = 0.
+ * All pointers are device pointers, 16-byte aligned (rows_dev: 4-byte);
  * dtype NP_F32/NP_F16/NP_BF16; d_model in [8, 8192], rows a multiple of 16
- * bytes.  Enqueued on `stream` (cudaStream_t); the call allocates nothing:
- * y_dev is cleared on the stream and then accumulated into, and the
- * kernel's error word lives in a file-scope device array (256 bytes) whose
- * address the first call on each device looks up, so make that first call
- * before any stream capture.  All calls share the array: calls that overlap
- * on the GPU race.  Errors: NP_ERR_ARG for sizes or pointers out of range,
- * NP_ERR_CUDA if a launch fails. */
+ * bytes.  y_dev may share no byte with h_dev, the weights or the row list
+ * (it is cleared on the stream before the kernel runs).  Enqueued on
+ * `stream` (cudaStream_t); the call allocates nothing: y_dev is cleared on
+ * the stream and then accumulated into, and the kernel's error word lives
+ * in a file-scope device array (256 bytes) whose address the first call on
+ * each device looks up, so make that first call before any stream capture.
+ * All calls share the array: calls that overlap on the GPU race.
+ * Errors returned: NP_ERR_ARG for sizes, pointers or overlaps out of range,
+ * NP_ERR_CUDA if a launch fails.  Errors found by the kernel (a row index
+ * >= row_limit, for which it reads row 0 instead and so returns a wrong y;
+ * a bounded wait that expired, leaving y partial) are recorded in the shared
+ * error word and reported by np_ffn_rows_noalloc_check. */
 np_status np_ffn_rows_noalloc(const float* h_dev, const void* w_gate, const void* w_up, const void* w_down,
                               const int32_t* rows_dev, int32_t n_rows, int32_t row_limit, int32_t d_model,
                               int32_t dtype, int32_t has_gate, float* y_dev, void* stream);
+
+/* Synchronise `stream`, then read and clear the current device's error word
+ * of np_ffn_rows_noalloc: NP_ERR_STATE if a row index was out of range,
+ * NP_ERR_TIMEOUT if a device wait expired, in any call since the previous
+ * check (the last such error wins); NP_OK if none; NP_ERR_CUDA if the stream
+ * holds an asynchronous CUDA error.  Allocates nothing. */
+np_status np_ffn_rows_noalloc_check(void* stream);
 
 /* Number of kernel launches the model has issued since creation. */
 int64_t np_launch_count(np_model* m);

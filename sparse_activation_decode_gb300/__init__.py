@@ -4,6 +4,6 @@ The compute runs in the CUDA library built from csrc/ (see build.py); this
 package only marshals arguments to its C ABI (include/np.h).
 """
 from ._lib import NpError, load  # noqa: F401
-from .decoder import SparseDecoder, decoder_for, ffn_rows_noalloc  # noqa: F401
+from .decoder import SparseDecoder, decoder_for, ffn_rows_noalloc, ffn_rows_noalloc_check  # noqa: F401
 
-__all__ = ["SparseDecoder", "decoder_for", "ffn_rows_noalloc", "NpError", "load"]
+__all__ = ["SparseDecoder", "decoder_for", "ffn_rows_noalloc", "ffn_rows_noalloc_check", "NpError", "load"]

@@ -75,6 +75,7 @@ SIGNATURES = {
     "np_host_register": (_I32, [_P, _SZ]),
     "np_host_unregister": (_I32, [_P]),
     "np_ffn_rows_noalloc": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
+    "np_ffn_rows_noalloc_check": (_I32, [_P]),
     "np_launch_count": (_I64, [_P]),
     "np_status_str": (ctypes.c_char_p, [_I32]),
     "np_last_error": (ctypes.c_char_p, []),

@@ -46,6 +46,8 @@ np_status arg_fail(const char* what) {
 }
 }  // namespace
 
+void np::set_last_error(const char* what) { g_last_err = what; }
+
 #define CUDA_TRY(expr)                                      \
   do {                                                      \
     cudaError_t _e = (expr);                                \

@@ -45,6 +45,7 @@ size_t ffn_smem_bytes(int D, int dtype_bytes, int nproj, int n_stages);
 cudaError_t ffn_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_per_sm, int n_sms, int* n_stages,
                      int* grid);
 int ffn_max_chunks();        // 16-byte chunks per row the FFN supports
+void set_last_error(const char* what);  // text returned by np_last_error() on this thread
 // Persistent FFN over consecutive layers first..first+count-1 (batch 1),
 // launched cooperatively: one CTA per SM, two arrival counters per layer
 // (partials stored; y slices summed).  The split-K order is fixed.

@@ -1,4 +1,5 @@
-// Allocation-free FFN entry point (np_ffn_rows_noalloc).
+// Allocation-free FFN entry point (np_ffn_rows_noalloc) and its error check
+// (np_ffn_rows_noalloc_check).
 //
 // Some callers cannot call cudaMalloc: a serving loop that runs under a
 // fixed, pre-planned memory budget owned by its own allocator, or code on a
@@ -13,10 +14,12 @@
 // looked up once per device with cudaGetSymbolAddress while that device is
 // current (the first call on a device does this, so that first call should
 // come before any stream capture), and only that address is passed to the
-// kernel.  Every call on a device shares the array and it keeps the last
-// call's contents; the error word and the output are cleared on the
-// caller's stream before each launch.  Calls whose kernels overlap on the
-// GPU race on the array: serialize them (one stream, or events).
+// kernel.  Every call on a device shares the array and it keeps its
+// contents between calls: a bounds or wait error recorded by any call stays
+// in the error word until np_ffn_rows_noalloc_check reads and clears it (the
+// word starts at zero when the library is loaded).  The output is cleared
+// on the caller's stream before each launch.  Calls whose kernels overlap on
+// the GPU race on the array: serialize them (one stream, or events).
 #include <mutex>
 
 #include "np.h"
@@ -54,35 +57,62 @@ static cudaError_t noalloc_scratch_for_current_device(NoallocScratch** out) {
 
 }  // namespace np
 
+namespace {
+
+// [a, a + na) and [b, b + nb) share a byte
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+np_status noalloc_fail(np_status s, const char* what) {
+  np::set_last_error(what);
+  return s;
+}
+
+}  // namespace
+
 extern "C" np_status np_ffn_rows_noalloc(const float* h_dev, const void* w_gate, const void* w_up,
                                          const void* w_down, const int32_t* rows_dev, int32_t n_rows,
                                          int32_t row_limit, int32_t d_model, int32_t dtype, int32_t has_gate,
                                          float* y_dev, void* stream) {
   using namespace np;
-  if (!h_dev || !w_up || !w_down || !y_dev || (has_gate && !w_gate)) return NP_ERR_ARG;
-  if (dtype < NP_F32 || dtype > NP_BF16 || (has_gate != 0 && has_gate != 1)) return NP_ERR_ARG;
+  if (!h_dev || !w_up || !w_down || !y_dev || (has_gate && !w_gate))
+    return noalloc_fail(NP_ERR_ARG, "np_ffn_rows_noalloc: null pointer");
+  if (dtype < NP_F32 || dtype > NP_BF16 || (has_gate != 0 && has_gate != 1))
+    return noalloc_fail(NP_ERR_ARG, "np_ffn_rows_noalloc: bad dtype or has_gate");
   const int esz = dtype == NP_F32 ? 4 : 2;
   if (d_model < 8 || d_model > 8192 || (d_model * esz) % 16 != 0 || d_model / (16 / esz) > ffn_max_chunks())
-    return NP_ERR_ARG;
-  if (n_rows < 0 || row_limit < 1 || (!rows_dev && n_rows > row_limit)) return NP_ERR_ARG;
+    return noalloc_fail(NP_ERR_ARG, "np_ffn_rows_noalloc: d_model out of range");
+  if (n_rows < 0 || row_limit < 1 || (!rows_dev && n_rows > row_limit))
+    return noalloc_fail(NP_ERR_ARG, "np_ffn_rows_noalloc: n_rows or row_limit out of range");
   const uintptr_t align_or = reinterpret_cast<uintptr_t>(h_dev) | reinterpret_cast<uintptr_t>(y_dev) |
                              reinterpret_cast<uintptr_t>(w_gate) | reinterpret_cast<uintptr_t>(w_up) |
                              reinterpret_cast<uintptr_t>(w_down);
-  if (align_or & 15u) return NP_ERR_ARG;
+  if (align_or & 15u) return noalloc_fail(NP_ERR_ARG, "np_ffn_rows_noalloc: pointer not 16-byte aligned");
+  // y is cleared on the stream before the kernel reads its inputs, so it may
+  // share no byte with any of them
+  const size_t vec_bytes = sizeof(float) * (size_t)d_model;
+  const size_t w_bytes = (size_t)row_limit * (size_t)d_model * (size_t)esz;
+  if (overlaps(y_dev, vec_bytes, h_dev, vec_bytes) || overlaps(y_dev, vec_bytes, w_up, w_bytes) ||
+      overlaps(y_dev, vec_bytes, w_down, w_bytes) || (has_gate && overlaps(y_dev, vec_bytes, w_gate, w_bytes)) ||
+      overlaps(y_dev, vec_bytes, rows_dev, sizeof(int32_t) * (size_t)n_rows))
+    return noalloc_fail(NP_ERR_ARG, "np_ffn_rows_noalloc: y_dev overlaps an input");
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   NoallocScratch* scratch = nullptr;
-  if (noalloc_scratch_for_current_device(&scratch) != cudaSuccess) return NP_ERR_CUDA;
+  if (noalloc_scratch_for_current_device(&scratch) != cudaSuccess)
+    return noalloc_fail(NP_ERR_CUDA, "np_ffn_rows_noalloc: cudaGetSymbolAddress");
   int dev = 0, sms = 0, smem_sm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return NP_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) return noalloc_fail(NP_ERR_CUDA, "np_ffn_rows_noalloc: cudaGetDevice");
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   int n_stages = 0, grid = 0;
   if (ffn_plan(dtype, has_gate, d_model, esz, (size_t)smem_sm, sms, &n_stages, &grid) != cudaSuccess)
-    return NP_ERR_CUDA;
-  int* err_word = scratch->words;
-  if (cudaMemsetAsync(scratch->words, 0, sizeof(scratch->words), st) != cudaSuccess) return NP_ERR_CUDA;
-  if (cudaMemsetAsync(y_dev, 0, sizeof(float) * (size_t)d_model, st) != cudaSuccess) return NP_ERR_CUDA;
+    return noalloc_fail(NP_ERR_CUDA, "np_ffn_rows_noalloc: ffn_plan");
+  if (cudaMemsetAsync(y_dev, 0, vec_bytes, st) != cudaSuccess)
+    return noalloc_fail(NP_ERR_CUDA, "np_ffn_rows_noalloc: clearing y");
 
   FfnLaunch a{};
   a.h_in = h_dev;
@@ -101,6 +131,26 @@ extern "C" np_status np_ffn_rows_noalloc(const float* h_dev, const void* w_gate,
   a.gated = has_gate;
   a.n_stages = n_stages;
   a.grid = grid;
-  a.err = err_word;
-  return launch_ffn_rows(a, st) == cudaSuccess ? NP_OK : NP_ERR_CUDA;
+  a.err = scratch->words;
+  return launch_ffn_rows(a, st) == cudaSuccess ? NP_OK
+                                               : noalloc_fail(NP_ERR_CUDA, "np_ffn_rows_noalloc: kernel launch");
+}
+
+extern "C" np_status np_ffn_rows_noalloc_check(void* stream) {
+  using namespace np;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  NoallocScratch* scratch = nullptr;
+  if (noalloc_scratch_for_current_device(&scratch) != cudaSuccess)
+    return noalloc_fail(NP_ERR_CUDA, "np_ffn_rows_noalloc_check: cudaGetSymbolAddress");
+  if (cudaStreamSynchronize(st) != cudaSuccess)
+    return noalloc_fail(NP_ERR_CUDA, "np_ffn_rows_noalloc_check: stream synchronize");
+  int word = 0;
+  if (cudaMemcpyAsync(&word, scratch->words, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return noalloc_fail(NP_ERR_CUDA, "np_ffn_rows_noalloc_check: reading the error word");
+  if (word == 0) return NP_OK;
+  if (cudaMemsetAsync(scratch->words, 0, sizeof(int), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return noalloc_fail(NP_ERR_CUDA, "np_ffn_rows_noalloc_check: clearing the error word");
+  if (word == kDevErrTimeout) return noalloc_fail(NP_ERR_TIMEOUT, "np_ffn_rows_noalloc: a device wait timed out");
+  return noalloc_fail(NP_ERR_STATE, "np_ffn_rows_noalloc: a row index was out of range");
 }

@@ -286,17 +286,55 @@ def decoder_for(wl, *, h2d_mode: str = "fused", staging_rows: int | None = None,
         read_hook=read_hook, **kw)
 
 
+def _shares_storage(a: torch.Tensor, b: torch.Tensor) -> bool:
+    """Two device tensors' byte ranges overlap."""
+    a0, b0 = a.data_ptr(), b.data_ptr()
+    return a0 < b0 + b.numel() * b.element_size() and b0 < a0 + a.numel() * a.element_size()
+
+
 def ffn_rows_noalloc(h: torch.Tensor, w_gate: torch.Tensor | None, w_up: torch.Tensor, w_down: torch.Tensor,
                      rows: torch.Tensor | None, n_rows: int, y: torch.Tensor | None = None) -> torch.Tensor:
     """np_ffn_rows_noalloc: the FFN over listed rows without any device
     allocation by the library (its scratch is a fixed device array); for
-    callers that cannot allocate.  Enqueued on torch's current stream."""
+    callers that cannot allocate.  Enqueued on torch's current stream.
+    h: float32 [d_model]; weights [row_limit][d_model], one dtype, all the
+    same shape; rows: int32 row indices or None for rows 0..n_rows-1.
+    Raises ValueError for inputs the C entry point would misread."""
     lib = L.load()
+    ws = [w for w in (w_gate, w_up, w_down) if w is not None]
+    for w in ws:
+        if not w.is_cuda or not w.is_contiguous() or w.dim() != 2:
+            raise ValueError("weights must be contiguous 2-D CUDA tensors")
+        if w.shape != w_up.shape or w.dtype != w_up.dtype:
+            raise ValueError("gate, up and down weights must share one shape and dtype")
+    if w_up.dtype not in _DTYPES:
+        raise ValueError(f"unsupported weight dtype {w_up.dtype}")
+    d_model = int(w_up.shape[1])
+    if h.dtype != torch.float32 or not h.is_cuda or not h.is_contiguous() or h.numel() != d_model:
+        raise ValueError("h must be a contiguous float32 CUDA tensor of d_model elements")
+    if rows is not None:
+        if rows.dtype != torch.int32 or not rows.is_cuda or not rows.is_contiguous() or rows.numel() < n_rows:
+            raise ValueError("rows must be a contiguous int32 CUDA tensor holding at least n_rows indices")
+    elif n_rows > w_up.shape[0]:
+        raise ValueError("n_rows exceeds the weights' rows")
     if y is None:
         y = torch.empty_like(h)
+    elif y.dtype != torch.float32 or not y.is_cuda or not y.is_contiguous() or y.numel() != d_model:
+        raise ValueError("y must be a contiguous float32 CUDA tensor of d_model elements")
+    for t in ws + [h] + ([rows] if rows is not None else []):
+        if _shares_storage(y, t):
+            raise ValueError("y may not share memory with h, the weights or the row list")
     L.check(lib.np_ffn_rows_noalloc(h.data_ptr(), None if w_gate is None else w_gate.data_ptr(), w_up.data_ptr(),
                                     w_down.data_ptr(), None if rows is None else rows.data_ptr(), int(n_rows),
-                                    int(w_up.shape[0]), int(h.numel()), _DTYPES[w_up.dtype],
+                                    int(w_up.shape[0]), d_model, _DTYPES[w_up.dtype],
                                     int(w_gate is not None), y.data_ptr(), torch.cuda.current_stream().cuda_stream),
             "np_ffn_rows_noalloc")
     return y
+
+
+def ffn_rows_noalloc_check() -> None:
+    """np_ffn_rows_noalloc_check on torch's current stream: synchronise it,
+    then raise NpError if any np_ffn_rows_noalloc call since the last check
+    recorded a row index out of range (status -6) or an expired wait (-5)."""
+    lib = L.load()
+    L.check(lib.np_ffn_rows_noalloc_check(torch.cuda.current_stream().cuda_stream), "np_ffn_rows_noalloc_check")

@@ -114,5 +114,37 @@ def test_every_entry_point_rejects_null_arguments(lib, name):
     # crash; freeing a null model is a no-op
     res, args = L.SIGNATURES[name]
     vals = [0 if a in _INTS else None for a in args]
+    if name == "np_ffn_rows_noalloc_check":
+        # its only argument is a stream, and NULL (the default stream) is a
+        # valid one: without a GPU the call fails in CUDA, cleanly
+        assert getattr(lib, name)(*vals) in (L.NP_OK, L.NP_ERR_CUDA)
+        return
     expected = L.NP_OK if name == "np_free_model" else L.NP_ERR_ARG
     assert getattr(lib, name)(*vals) == expected
+
+
+@pytest.mark.parametrize("case", ["y is h", "y inside h", "y inside down", "y over the row list",
+                                  "unaligned y", "row_limit 0", "d_model 4"])
+def test_noalloc_rejects_bad_arguments_before_cuda(lib, case):
+    # np_ffn_rows_noalloc: y may share no byte with its inputs (it is cleared
+    # on the stream before they are read), pointers are 16-byte aligned and
+    # sizes in range; all checked on the host before any CUDA call.
+    D = 256
+    h, g, u, d, rows, y = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000
+    n_rows, limit, dm = 10, 100, D
+    if case == "y is h":
+        y = h
+    elif case == "y inside h":
+        y = h + 512
+    elif case == "y inside down":
+        y = d + 100 * D * 2 - 16          # the last 16 bytes of a 100-row f16 block
+    elif case == "y over the row list":
+        y = rows - 16
+    elif case == "unaligned y":
+        y = 0x600008
+    elif case == "row_limit 0":
+        limit = 0
+    elif case == "d_model 4":
+        dm = 4
+    st = lib.np_ffn_rows_noalloc(h, g, u, d, rows, n_rows, limit, dm, L.NP_F16, 1, y, None)
+    assert st == L.NP_ERR_ARG
