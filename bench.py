@@ -48,7 +48,7 @@ NCU_TRAFFIC = {
 SRC_DIR = os.path.join(ROOT, "sparse_activation_decode_gb300", "csrc")
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=256)
@@ -73,7 +73,11 @@ def parse():
                         "then standalone calls) and exit")
     p.add_argument("--layers", type=int, default=None,
                    help="with --profile-case: keep only this many layers (same shapes per layer)")
-    return p.parse_args()
+    return p.parse_args(argv)
+
+
+def parse_args(argv):
+    return parse(argv)
 
 
 def replica_seed(seed: int, rank: int) -> int:
@@ -188,13 +192,14 @@ def kernel_table(prof, peaks, h2d_peak):
             continue
         ms = d["ms"]
         gbs = d["bytes"] / (ms * 1e-3) / 1e9 if ms > 0 and d["bytes"] > 0 else None
-        bound = "host_link" if kind == "gather" else "hbm"
-        peak = h2d_peak if bound == "host_link" else peaks["hbm_gbs"]
+        # the set kernel moves ~100 KB per launch: latency-bound, no roofline
+        bound = {"gather": "host_link", "set": "latency"}.get(kind, "hbm")
+        peak = {"host_link": h2d_peak, "hbm": peaks["hbm_gbs"]}.get(bound)
         out[kind] = {"launches": d["launches"], "ms_total": round(ms, 4),
                      "us_per_launch": round(1e3 * ms / d["launches"], 3),
                      "bytes_per_launch": d["bytes"] // d["launches"] if d["bytes"] else 0,
                      "gbs": round(gbs, 1) if gbs else None, "bound": bound,
-                     "frac": round(gbs / peak, 4) if gbs else None}
+                     "frac": round(gbs / peak, 4) if gbs and peak else None}
     return out
 
 
@@ -219,6 +224,54 @@ def link_busy_ms(timeline):
     if cs is not None:
         busy += ce - cs
     return busy
+
+
+COMPUTE_KINDS = ("dense", "predictor", "set", "ffn", "finish")
+
+
+def _union(iv):
+    """Sorted disjoint union of intervals [(a, b)]."""
+    out = []
+    for a, b in sorted(iv):
+        if out and a <= out[-1][1]:
+            out[-1][1] = max(out[-1][1], b)
+        else:
+            out.append([a, b])
+    return out
+
+
+def _measure(iv):
+    return sum(b - a for a, b in iv)
+
+
+def _intersect(u, v):
+    """Total length of the intersection of two disjoint unions."""
+    i = j = 0
+    tot = 0.0
+    while i < len(u) and j < len(v):
+        a, b = max(u[i][0], v[j][0]), min(u[i][1], v[j][1])
+        if b > a:
+            tot += b - a
+        if u[i][1] < v[j][1]:
+            i += 1
+        else:
+            j += 1
+    return tot
+
+
+def link_overlap(timeline):
+    """Host-link time against compute time over a profiled run (ms, totals):
+    busy = union of the gather launches; exposed = link busy while no
+    compute kernel (dense, predictor, set, FFN, final add) runs; idle =
+    compute running while the link is idle (the windows a per-token pipeline
+    cannot fill with reads); span = first start to last end."""
+    link = _union([(a, b) for k, a, b in timeline if k == "gather"])
+    comp = _union([(a, b) for k, a, b in timeline if k in COMPUTE_KINDS])
+    both = _intersect(link, comp)
+    busy, cbusy = _measure(link), _measure(comp)
+    span = (max(b for _, _, b in timeline) - min(a for _, a, _ in timeline)) if timeline else 0.0
+    return {"busy": busy, "exposed": busy - both, "overlapped": both, "idle_while_compute": cbusy - both,
+            "span": span}
 
 
 def isolated_kernels(dec, torch, cfg, reps=5):
@@ -349,6 +402,33 @@ def profile_case(args):
     print("profile case done")
 
 
+def config_dict(cfg, args, world):
+    """The workload the line is quoted on (shared by both arms)."""
+    return {"workload": cfg.name, "layers": cfg.n_layers, "dense_prefix": cfg.n_dense,
+            "d_model": cfg.d_model, "d_ff": cfg.d_ff, "k_max": cfg.k_max, "centroids": cfg.n_centroids,
+            "combine": cfg.combine, "persistence": cfg.persistence, "batch": cfg.batch,
+            "density": cfg.density, "warm_fill_tokens": cfg.n_warm,
+            "ffn": "tcgen05 tensor cores" if cfg.batch > 1 else "CUDA cores",
+            "h2d_mode": args.h2d_mode, "slots": cfg.slots, "residency": cfg.residency,
+            "lookahead": cfg.lookahead, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (per-token weights ~2 GB > 129 MB)"}
+
+
+def workload_config(args):
+    """CONFIGS[--config] with the command line's overrides."""
+    from workloads import CONFIGS
+    base = CONFIGS[args.config]
+    if args.persistence is not None:
+        base = base.replace(persistence=args.persistence)
+    if args.slots is not None:
+        base = base.replace(slots=args.slots)
+    if args.residency is not None:
+        base = base.replace(residency=args.residency)
+    if args.lookahead is not None:
+        base = base.replace(lookahead=args.lookahead)
+    return base
+
+
 def run_cuda(args):
     import torch
     import torch.distributed as dist
@@ -369,17 +449,14 @@ def run_cuda(args):
     build()
     peaks = load_peaks()
     W, K = args.warmup, args.steps
-    base = CONFIGS[args.config]
-    if args.persistence is not None:
-        base = base.replace(persistence=args.persistence)
-    if args.slots is not None:
-        base = base.replace(slots=args.slots)
-    if args.residency is not None:
-        base = base.replace(residency=args.residency)
-    if args.lookahead is not None:
-        base = base.replace(lookahead=args.lookahead)
+    base = workload_config(args)
+    # token positions: the workload's prompt warm fill, W warm-up steps, K
+    # timed steps, then the profiled, statistics and end-to-end passes, each
+    # continuing the sequence
+    n_fill = base.n_warm
+    KP, NST = min(K, 64), 16
     span = (base.batch - 1) * base.phase_step + 24
-    T = min(W + 3 * K, base.n_centroids - span if base.n_centroids else 10 ** 9)
+    T = min(n_fill + W + 2 * K + KP + NST, base.n_centroids - span if base.n_centroids else 10 ** 9)
     cfg = base.replace(n_warm=0, n_decode=T, seed=replica_seed(base.seed, rank))
     B = cfg.batch
     t0 = time.time()
@@ -394,11 +471,14 @@ def run_cuda(args):
         return xs[i % T].clone()
 
     h2d_peak = h2d_peak_gbs(torch) if rank == 0 else None
-    # warm-up (includes the cold start)
-    for i in range(W):
-        dec.decode_token(tok(i))
+    # the prompt warm fill (the cold start is its first token), then warm-up
+    pos = 0
+    for i in range(n_fill + W):
+        dec.decode_token(tok(pos))
+        pos += 1
     torch.cuda.synchronize()
-    hs = [tok(W + k) for k in range(K)]
+    hs = [tok(pos + k) for k in range(K)]
+    pos += K
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -420,10 +500,10 @@ def run_cuda(args):
 
     # live per-kernel durations (events on each kernel's own stream); few
     # enough tokens that the library keeps every launch in its timeline
-    KP = min(K, 64)
     dec.profile()
     dec.set_profiling(True)
-    hs2 = [tok(W + K + k) for k in range(KP)]
+    hs2 = [tok(pos + k) for k in range(KP)]
+    pos += KP
     for k in range(KP):
         dec.decode_token(hs2[k])
     timeline = dec.timeline()
@@ -436,9 +516,10 @@ def run_cuda(args):
     iso = isolated_kernels(dec, torch, cfg)
     # rows read over the host link and rows moved inside HBM per token
     # (synchronising stats calls, after every timed region of the decode)
-    n_st, din_rows, moved_rows, act_rows = 16, 0, 0, 0
+    n_st, din_rows, moved_rows, act_rows = NST, 0, 0, 0
     for k in range(n_st):
-        st = dec.decode_token(tok(W + K + KP + k), stats=True)
+        st = dec.decode_token(tok(pos), stats=True)
+        pos += 1
         din_rows += st["din_rows"]
         moved_rows += st["moved_rows"]
         act_rows += st["active_rows"]
@@ -454,7 +535,8 @@ def run_cuda(args):
     e2e = None
     if not args.no_e2e:
         D, B = cfg.d_model, cfg.batch
-        hin = torch.stack([xs[(W + 2 * K + k) % T] for k in range(K)]).cpu().pin_memory()
+        hin = torch.stack([xs[(pos + k) % T] for k in range(K)]).cpu().pin_memory()
+        pos += K
         hout = torch.empty_like(hin).pin_memory()
         hdev = torch.empty((B, D), dtype=torch.float32, device="cuda")
         torch.cuda.synchronize()
@@ -475,7 +557,7 @@ def run_cuda(args):
         return None
     dom = max(((k, v) for k, v in table.items() if k != "finish"), key=lambda kv: kv[1]["ms_total"])
     dk, dv = dom
-    KP = min(K, 64)
+    ov = link_overlap(timeline)
     if dv["bound"] == "host_link":
         # concurrent gather launches share the link: rate over the union of
         # their intervals, per launch = bytes per launch / (busy / launches)
@@ -525,15 +607,18 @@ def run_cuda(args):
         "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"{cfg.dtype} weights, f32 accumulate", "data": "synthetic (seeded; shapes of the pages' workloads)",
-        "config": {"workload": cfg.name, "layers": cfg.n_layers, "dense_prefix": cfg.n_dense,
-                   "d_model": cfg.d_model, "d_ff": cfg.d_ff, "k_max": cfg.k_max, "centroids": cfg.n_centroids,
-                   "combine": cfg.combine, "persistence": cfg.persistence, "batch": cfg.batch,
-                   "density": cfg.density, "ffn": "tcgen05 tensor cores" if cfg.batch > 1 else "CUDA cores",
-                   "h2d_mode": args.h2d_mode, "slots": cfg.slots, "residency": cfg.residency,
-                   "lookahead": cfg.lookahead, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (per-token weights ~2 GB > 129 MB)"},
+        "config": config_dict(base, args, world),
         "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": table,
-        "h2d_peak_gbs": round(h2d_peak, 1), "h2d_peak_after_gbs": round(h2d_after, 1), "host_link_busy_ms_per_token": round(link_ms / KP, 4),
+        "h2d_peak_gbs": round(h2d_peak, 1), "h2d_peak_after_gbs": round(h2d_after, 1),
+        "host_link_busy_ms_per_token": round(link_ms / KP, 4),
+        # Budgeting Bytes' exposed-I/O view of the profiled tokens: link time
+        # no compute kernel overlaps, and compute time with the link idle
+        "host_link_per_token_ms": {"busy": round(ov["busy"] / KP, 4), "exposed": round(ov["exposed"] / KP, 4),
+                                   "overlapped_by_compute": round(ov["overlapped"] / KP, 4),
+                                   "idle_while_compute": round(ov["idle_while_compute"] / KP, 4),
+                                   "profiled_span": round(ov["span"] / KP, 4),
+                                   "note": "profiled pass (events per launch on its stream; upper bounds for "
+                                           "launches that wait on another stream)"},
         "profiled_tokens": KP, "movement": movement,
         "gpu_launches": launches, "active_density_last_step": round(union_density, 4) if union_density else None,
         "clocks": clk.summary(), "e2e": e2e, "workload_gen_s": round(gen_s, 1),
@@ -586,30 +671,40 @@ def main():
 
 
 def run_reference(args):
-    """The reference arm is the fp64 oracle on the host cores, same config and
-    metric, on a bounded sample of tokens."""
+    """The reference arm is the fp64 oracle on the host cores, on the same
+    workload, metric and config as the CUDA arm: W untimed warm-up tokens
+    (the first is the cold start), then K timed tokens.  The oracle's work
+    per token does not depend on the warm fill, which it skips."""
     import torch  # noqa: F401
-    from workloads import CONFIGS, make_workload
+    from workloads import make_workload
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    base = CONFIGS[args.config]
-    if args.persistence is not None:
-        base = base.replace(persistence=args.persistence)
-    n_tok = max(1, min(args.steps, 16))
-    cfg = base.replace(n_warm=0, n_decode=n_tok + 1)
+    base = workload_config(args)
+    W, K = max(args.warmup, 0), max(args.steps, 1)
+    cfg = base.replace(n_warm=0, n_decode=W + K)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     wl = make_workload(cfg, device=dev)
     wl.dense_w = wl.dense_w.cpu() if wl.dense_w is not None else None
     wl.pred_w1, wl.pred_w2 = wl.pred_w1.cpu(), wl.pred_w2.cpu()
-    n, sec = run_oracle_tokens(wl, n_tok, budget_s=120)
-    v = n * cfg.batch / sec
+    wl.pred_b2 = wl.pred_b2.cpu() if wl.pred_b2 is not None else None
+    wl.x = wl.x.cpu()
+    from oracle import OracleDecoder
+    orc = OracleDecoder(wl, materialize_buffers=False)
+    for t in range(W):
+        orc.step(wl.x[t].numpy())
+    t0 = time.time()
+    for t in range(W, W + K):
+        orc.step(wl.x[t].numpy())
+    sec = time.time() - t0
+    v = K * cfg.batch / sec
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tok/s", "n_gpus": args.gpus,
-            "steps": n, "warmup": 1, "ms_per_step": round(1e3 * sec / n, 2), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name},
+            "steps": K, "warmup": W, "ms_per_step": round(1e3 * sec / K, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; shapes of the "
+            "pages' workloads)", "config": config_dict(base, args, args.gpus),
             "cpu_baseline": {"value": round(v, 4), "unit": "tok/s", "cores": cores_used(), "kind": "oracle",
-                             "sample": f"{n} steps x {cfg.batch} sequences of {cfg.name} after a cold-start step"},
+                             "sample": f"{K} steps x {cfg.batch} sequences of {cfg.name} after {W} warm-up "
+                                       "steps (the first a cold start); fp64 numpy"},
             "e2e": {"value": round(v, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

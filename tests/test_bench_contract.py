@@ -18,7 +18,7 @@ def _bench(*args, timeout=300):
 
 
 def test_reference_arm_prints_one_contract_line():
-    r = _bench("--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "0")
+    r = _bench("--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "3")
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
     assert len(lines) == 1
@@ -28,8 +28,13 @@ def test_reference_arm_prints_one_contract_line():
         assert key in d, key
     assert d["impl"] == "reference"
     assert d["unit"] == "tok/s" and d["higher_is_better"] is True
-    assert d["value"] > 0 and d["steps"] == 2
+    assert d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 3
     assert d["config"]["workload"] == "tiny"
+    # the same config object as the CUDA arm's line for these arguments
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.parse_args(["--config", "tiny", "--steps", "2", "--warmup", "3"])
+    assert d["config"] == bench.config_dict(bench.workload_config(args), args, 1)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

@@ -73,3 +73,27 @@ def test_clock_summary_parses_nvidia_smi_lines():
     assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
     empty = bench.ClockSampler(0).summary()
     assert empty == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_link_overlap_against_brute_force():
+    # exposed link time = link busy with no compute kernel running; idle =
+    # compute with the link idle; checked on a fine time grid
+    import random
+    import bench
+    rnd = random.Random(7)
+    for _ in range(20):
+        tl = []
+        for _ in range(rnd.randint(1, 12)):
+            k = rnd.choice(["gather", "gather", "ffn", "dense", "predictor", "set", "finish", "scatter"])
+            a = rnd.randint(0, 200) / 10
+            tl.append((k, a, a + rnd.randint(1, 60) / 10))
+        ov = bench.link_overlap(tl)
+        step = 0.01
+        grid = [i * step + step / 2 for i in range(int(30 / step))]
+        on = lambda kinds, t: any(a <= t < b for k, a, b in tl if k in kinds)
+        link = sum(step for t in grid if on(("gather",), t))
+        comp = sum(step for t in grid if on(bench.COMPUTE_KINDS, t))
+        both = sum(step for t in grid if on(("gather",), t) and on(bench.COMPUTE_KINDS, t))
+        assert abs(ov["busy"] - link) < 0.05
+        assert abs(ov["exposed"] - (link - both)) < 0.05
+        assert abs(ov["idle_while_compute"] - (comp - both)) < 0.05

@@ -255,6 +255,41 @@ def test_full_size_sampled(cfg, tokens):
     assert summ["max_h_rel"] < FFN_TOL
 
 
+@pytest.mark.parametrize("cfg,tokens", [(LLAMA7B, 3), (OPT67B.replace(lookahead=2), 3), (BATCHED7B, 2)],
+                         ids=["llama2-7b", "opt-6.7b-lookahead2", "llama2-7b-batch8"])
+def test_full_size_fused(cfg, tokens):
+    # the host-link mode the benchmark times: records read from host memory
+    # straight into their slots, at the full shapes
+    wl = make_workload(cfg.replace(n_warm=0, n_decode=tokens), device="cuda")
+    summ = run_and_compare(wl, tokens, h2d_mode="fused", check_buffers=False, sample_slots=64,
+                           check_layer_y=True)
+    assert summ["tokens"] == tokens
+    assert summ["max_h_rel"] < FFN_TOL
+
+
+def test_llama7b_warm_state_fused_every_buffer_byte():
+    # the state the benchmark decodes from: 26 tokens of slot churn after the
+    # cold start (freed slots reused all over the K_max range), fused host-link
+    # mode, every token's integer state compared in full; then every byte of
+    # all 31 layers' three resident buffers against the oracle's buffers, and
+    # each layer's FFN output on the last token
+    T = 26
+    cfg = LLAMA7B.replace(n_warm=0, n_decode=T)
+    wl = make_workload(cfg, device="cuda")
+    dec = build_decoder(wl, h2d_mode="fused")
+    orc = OracleDecoder(wl, materialize_buffers=True)
+    try:
+        summ = run_and_compare(wl, T - 1, dec=dec, orc=orc, check_buffers=False, check_layer_y=False)
+        assert summ["near_ties"] == 0
+        # the slots in use are spread over the whole buffer by now
+        inv = orc.inv
+        assert (inv >= 0).sum(axis=1).min() > 0.9 * cfg.k_max
+        last = run_and_compare(wl, 1, dec=dec, orc=orc, start=T - 1, check_buffers=True, check_layer_y=True)
+        assert last["max_h_rel"] < FFN_TOL and last["max_y_rel"] < FFN_TOL
+    finally:
+        dec.close()
+
+
 @pytest.mark.parametrize("cfg,tokens,kw", [(SMALL_BATCHED.replace(slots="compact"), 6, {}),
                                            (SMALL_OPT.replace(lookahead=2), 6, {"h2d_mode": "fused"}),
                                            (BATCHED7B.replace(slots="compact"), 3,
