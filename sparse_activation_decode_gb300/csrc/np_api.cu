@@ -21,6 +21,7 @@
 // the rows already overwritten are copied back from the store.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -116,6 +117,8 @@ struct np_model {
   cudaStream_t ours[8] = {};
   int n_ours = 0;
   unsigned* arrive = nullptr;            // [2L] arrival counters of the chain
+  unsigned* gdone = nullptr;             // [L] per-layer read counters of the per-token pipeline
+  bool token_chain = false;              // one persistent launch reads and runs every layer after layer 0
   float* chain_part = nullptr;           // [chain_grid][D] partial y of the chain
   int gather_grid = 0, scatter_grid = 0, pred_grid = 0;
   int rps1 = 1, rps2 = 1, ns1 = 2, ns2 = 2;
@@ -154,11 +157,15 @@ struct np_model {
 
 namespace {
 
+// An integer tuning switch from the environment: its value when set to a
+// decimal integer (0 included), else `dflt`.
 int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   if (!v || !*v) return dflt;
-  const int x = std::atoi(v);
-  return x > 0 ? x : dflt;
+  char* end = nullptr;
+  const long x = std::strtol(v, &end, 10);
+  if (end == v || *end != '\0' || x < INT_MIN || x > INT_MAX) return dflt;
+  return (int)x;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -916,9 +923,20 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   // their grids small leaves the SMs to the FFN running beside them.
   // NP_TUNE_GATHER_CTAS / NP_TUNE_SCATTER_CTAS override the defaults.
   m->graph_off = env_int("NP_TUNE_GRAPH", 1) == 0;
+  // Per-token pipeline: by default where a dense prefix of two or more
+  // layers sits on the stream pipeline's FFN stream ahead of the sparse
+  // layers (measured: Llama-2-13B shape 516 -> 540 tok/s; the 7B shape, one
+  // dense layer, is faster on the stream pipeline, 756 vs 702, because its
+  // reads start after the first predictor group instead of after all of
+  // them).  NP_TUNE_TOKEN_CHAIN=0/1 forces it off/on.
+  const int tc_env = env_int("NP_TUNE_TOKEN_CHAIN", -1);
+  m->token_chain = (tc_env == 1 || (tc_env == -1 && m->dn >= 2)) && m->B == 1 && m->S > 0 &&
+                   m->d.pred_kind == NP_PRED_SHARED_ARGMAX && !m->compact && m->d.h2d_mode == NP_H2D_FUSED;
   m->pdl_mask = env_int("NP_TUNE_PDL", 5);
   m->gather_grid = env_int("NP_TUNE_GATHER_CTAS", 32);
   m->scatter_grid = env_int("NP_TUNE_SCATTER_CTAS", 4 * m->sms);
+  if (m->gather_grid < 1) m->gather_grid = 32;
+  if (m->scatter_grid < 1) m->scatter_grid = 4 * m->sms;
   m->pred_grid = 2 * m->sms;
   if (env_int("NP_TUNE_VERBOSE", 0) == 1)
     std::fprintf(stderr, "np: ffn grid %d, ring %d slots; gather %d scatter %d CTAs\n", m->ffn_grid, m->ffn_stages,
@@ -967,6 +985,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if ((st = dev_alloc(m, &m->fire, (size_t)m->W)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->logits, F)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->arrive, 2 * (size_t)m->L)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->gdone, (size_t)m->L)) != NP_OK) return fail(st);
   if (m->B == 1 && (st = dev_alloc(m, &m->chain_part, (size_t)m->chain_grid * m->D)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->hbase, 2 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->yacc, 3 * (size_t)m->B * m->D)) != NP_OK) return fail(st);
@@ -976,8 +995,10 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     m->tc = true;
     const int dt = m->d.dtype;
     const size_t optin = m->smem_optin - 1024;
-    const int want = env_int("NP_TUNE_MMA_CLUSTERS", 0);
-    const int max_st = env_int("NP_TUNE_MMA_STAGES", 0);
+    int want = env_int("NP_TUNE_MMA_CLUSTERS", 0);
+    int max_st = env_int("NP_TUNE_MMA_STAGES", 0);
+    if (want < 0) want = 0;
+    if (max_st < 0) max_st = 0;
     const int ffn_mode = m->d.has_gate ? kMmaFfnGated : kMmaFfnUp;
     if ((e = mma_plan(ffn_mode, dt == NP_BF16, m->D, optin, m->sms, want, max_st, &m->plan_ffn)) != cudaSuccess ||
         (e = mma_plan(kMmaHidden, dt == NP_BF16, m->D, optin, m->sms, want, max_st, &m->plan_hid)) != cudaSuccess ||
@@ -1018,7 +1039,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     cudaDeviceGetStreamPriorityRange(&lo, &hi);
     // NP_TUNE_SIDE_PRIORITY=0 puts the internal gather/scatter streams at the
     // default priority instead of the highest
-    const int pr = env_int("NP_TUNE_SIDE_PRIORITY", 1) == 1 ? hi : lo;
+    const int pr = env_int("NP_TUNE_SIDE_PRIORITY", 1) != 0 ? hi : lo;
     e = cudaStreamCreateWithPriority(&m->g1, cudaStreamNonBlocking, pr);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&m->xs, cudaStreamNonBlocking, pr);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->fs, cudaStreamNonBlocking);
@@ -1215,6 +1236,37 @@ np_status np_dense_mlp(np_model* m, int32_t layer, const float* h_dev, float* y_
   return enqueue_layer_ffn(m, m->main, layer, h_dev, nullptr, nullptr, y_dev, nullptr);
 }
 
+// The persistent chain over layers first .. first+count-1 (batch 1) on the
+// residual stream h_dev; the arrival counters must be zero.
+FfnChainLaunch chain_args(np_model* m, int first, int count, float* h_dev) {
+  FfnChainLaunch a{};
+  a.dense_w = m->d.dense_w;
+  a.bufs = m->bufs;
+  a.active_slot = m->active_slot;
+  a.counts = m->counts;
+  a.n_rows = m->slot_hw;
+  a.compact = m->compact;
+  a.n_dense = m->dn;
+  a.F = m->F;
+  a.K = m->K;
+  a.first = first;
+  a.count = count;
+  a.h = h_dev;
+  a.hbase = m->hbase;
+  a.yacc = m->yacc;
+  a.part = m->chain_part;
+  a.arrive = m->arrive;
+  a.D = m->D;
+  a.dtype = m->d.dtype;
+  a.dtype_bytes = m->esz;
+  a.gated = m->d.has_gate;
+  a.swiglu = m->d.activation == NP_ACT_SWIGLU;
+  a.n_stages = m->chain_stages;
+  a.grid = m->chain_grid;
+  a.err = m->err;
+  return a;
+}
+
 np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev) {
   if (!m || !h_dev) return arg_fail("null argument");
   begin_call(m);
@@ -1233,31 +1285,7 @@ np_status np_ffn_layers(np_model* m, int32_t first, int32_t count, float* h_dev)
     // batch 1: one persistent kernel streams the whole range
     CUDA_TRY(cudaMemsetAsync(m->arrive, 0, sizeof(unsigned) * 2 * (size_t)count, st));
     forget(m, st);
-    FfnChainLaunch a{};
-    a.dense_w = m->d.dense_w;
-    a.bufs = m->bufs;
-    a.active_slot = m->active_slot;
-    a.counts = m->counts;
-    a.n_rows = m->slot_hw;
-    a.compact = m->compact;
-    a.n_dense = m->dn;
-    a.F = m->F;
-    a.K = m->K;
-    a.first = first;
-    a.count = count;
-    a.h = h_dev;
-    a.hbase = m->hbase;
-    a.yacc = m->yacc;
-    a.part = m->chain_part;
-    a.arrive = m->arrive;
-    a.D = m->D;
-    a.dtype = m->d.dtype;
-    a.dtype_bytes = m->esz;
-    a.gated = m->d.has_gate;
-    a.swiglu = m->d.activation == NP_ACT_SWIGLU;
-    a.n_stages = m->chain_stages;
-    a.grid = m->chain_grid;
-    a.err = m->err;
+    const FfnChainLaunch a = chain_args(m, first, count, h_dev);
     return launch(m, NP_KIND_FFN, st, 0, [&] { return launch_ffn_chain(a, st); });
   }
   for (int i = 0; i < count; ++i) {
@@ -1286,6 +1314,39 @@ np_status enqueue_token(np_model* m, float* h_dev) {
   CUDA_TRY(cudaMemsetAsync(chain_y(m, 0), 0, sizeof(float) * m->B * m->D, m->main));
   forget(m, m->main);
   cudaStream_t fin = m->main;
+  if (shared && m->S > 0 && m->token_chain && !m->d.read_hook) {
+    // Per-token pipeline (one persistent launch for layers 1..L-1): dense
+    // layer 0, the predictor, one set kernel for every sparse layer, then a
+    // cooperative kernel whose reader warps bring each sparse layer's
+    // incoming records from the host store into their slots while its FFN
+    // producers wait, per layer, until every CTA's readers are done.
+    // Layer 0 also runs on the chain kernel (fixed-order split-K), so the
+    // whole token is reproducible bit for bit.
+    cudaStream_t st = m->main;
+    CUDA_TRY(cudaMemsetAsync(m->arrive, 0, sizeof(unsigned) * 2, st));
+    forget(m, st);
+    const FfnChainLaunch a0 = chain_args(m, 0, 1, h_dev);
+    NP_TRY(launch(m, NP_KIND_DENSE, st, (int64_t)m->nproj * m->F * m->row_bytes,
+                  [&] { return launch_ffn_chain(a0, st); }));
+    NP_TRY(enqueue_pred_hidden(m, h_dev, nullptr));
+    NP_TRY(enqueue_pred_heads(m, 0, m->NH));
+    m->pending_bits = all_layers(m);
+    SetLaunch sa = set_args(m, 0, m->S);
+    sa.keys = m->keys;
+    sa.ids_out = m->ids;
+    sa.pdl = pdl_for(m, st, 2);
+    NP_TRY(launch(m, NP_KIND_SET, st, (int64_t)m->S * m->W * 8, [&] { return launch_set(sa, st); }));
+    CUDA_TRY(cudaMemsetAsync(m->arrive, 0, sizeof(unsigned) * 2 * (size_t)(m->L - 1), st));
+    CUDA_TRY(cudaMemsetAsync(m->gdone, 0, sizeof(unsigned) * (size_t)(m->L - 1), st));
+    forget(m, st);
+    FfnChainLaunch a = chain_args(m, 1, m->L - 1, h_dev);
+    a.g_store = m->store_dev;
+    a.din_n = m->din_n;
+    a.din_s = m->din_s;
+    a.gdone = m->gdone;
+    NP_TRY(launch(m, NP_KIND_FFN, st, 0, [&] { return launch_ffn_chain(a, st); }));
+    return bump_token(m);
+  }
   if (shared && m->S > 0) {
     // main: dense layer 0, the predictor's hidden layer, then per layer
     // group the group's predictor heads, its set kernel and its reads on the

@@ -43,7 +43,8 @@ constexpr int kFfnThreads = 256;                 // consumer threads of the per-
 constexpr int kFfnWarps = kFfnThreads / 32;      // consumer warps
 constexpr int kFfnBlock = kFfnThreads + 32;      // plus one producer warp
 constexpr int kChainThreads = 512;               // consumer threads of the persistent chain
-constexpr int kChainBlock = kChainThreads + 32;
+constexpr int kChainReaders = 64;                // host-store reader threads of the persistent chain
+constexpr int kChainBlock = kChainThreads + 32 + kChainReaders;
 constexpr int kChainGroup = 4;                   // rows per block barrier in the chain (2 for wide rows)
 constexpr int kRowCache = 64;                    // row indices cached per CTA
 
@@ -639,6 +640,20 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
       const int* list;
       int limit;
       const int my_n = layer_rows(i, &wg, &wu, &wd, &list, &limit);
+      if (a.g_store && a.first + i >= a.n_dense) {
+        // every CTA has written this layer's incoming rows: the async-proxy
+        // reads below must see those generic-proxy writes
+        int fail = 0;
+        if (lane == 0) {
+          fail = wait_count(a.gdone + i, (unsigned)G, a.err) ? 0 : 1;
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        if (__shfl_sync(0xffffffffu, fail, 0)) {
+          if (lane == 0) s_abort = 1;
+          stop = true;
+          break;
+        }
+      }
       for (int b0 = 0; b0 < my_n && !stop; b0 += 32) {
         int mine = 0;
         if (b0 + lane < my_n) {
@@ -675,6 +690,60 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
             stop = true;
             break;
           }
+        }
+      }
+    }
+  } else if (warp > kChainThreads / 32) {
+    // ------------------------------------------------------------ readers
+    // Incoming records of each sparse layer, straight from the host store
+    // into their slots (CTA c takes records c, c + G, ...); the rows of a
+    // record are copied by the reader threads with eight 16-byte loads in
+    // flight each.  Once a CTA's readers are done with a layer, one release
+    // per CTA counts it in gdone.  They run ahead of the FFNs, bounded only
+    // by the host link.
+    if (a.g_store) {
+      constexpr int kIlpR = 8;
+      const int rt = tid - (kChainThreads + 32);
+      const int row_vec = (int)(row_bytes / 16u);
+      const int rec_vec = NPROJ * row_vec;
+      for (int i = 0; i < a.count; ++i) {
+        const int l = a.first + i;
+        if (l < a.n_dense) continue;
+        const int s = l - a.n_dense;
+        int n_in = a.counts[(size_t)s * 4 + 1];
+        n_in = n_in < 0 ? 0 : (n_in > a.K ? a.K : n_in);
+        const uint4* store = static_cast<const uint4*>(a.g_store) + (size_t)s * a.F * rec_vec;
+        uint4* bufs = reinterpret_cast<uint4*>(const_cast<void*>(a.bufs)) + (size_t)s * NPROJ * a.K * row_vec;
+        for (int r = (int)blockIdx.x; r < n_in; r += G) {
+          const int n = a.din_n[(size_t)s * a.K + r], slot = a.din_s[(size_t)s * a.K + r];
+          if ((unsigned)n >= (unsigned)a.F || (unsigned)slot >= (unsigned)a.K) {
+            if (rt == 0) atomicExch(a.err, kDevErrBounds);
+            continue;
+          }
+          const uint4* src = store + (size_t)n * rec_vec;
+          for (int p = 0; p < NPROJ; ++p) {
+            uint4* dst = bufs + ((size_t)p * a.K + slot) * row_vec;
+            for (int b = rt; b < row_vec; b += kChainReaders * kIlpR) {
+              uint4 v[kIlpR];
+#pragma unroll
+              for (int u = 0; u < kIlpR; ++u) {
+                const int j = b + u * kChainReaders;
+                if (j < row_vec) v[u] = src[(size_t)p * row_vec + j];
+              }
+#pragma unroll
+              for (int u = 0; u < kIlpR; ++u) {
+                const int j = b + u * kChainReaders;
+                if (j < row_vec) dst[j] = v[u];
+              }
+            }
+          }
+        }
+        // the rows written by every reader of this CTA, then one arrival
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        asm volatile("bar.sync 2, %0;" ::"n"(kChainReaders) : "memory");
+        if (rt == 0) {
+          __threadfence();
+          atomicAdd(a.gdone + i, 1u);
         }
       }
     }

@@ -65,6 +65,12 @@ struct FfnChainLaunch {
   unsigned* arrive;          // [2 count] arrival counters, zero beforehand
   int D, dtype, dtype_bytes, gated, swiglu, n_stages, grid;
   int* err;
+  // Optional reads of each sparse layer's incoming records inside the same
+  // launch (per-token pipeline); g_store = null: the rows are resident.
+  const void* g_store;       // device-visible host store [S][F][n_proj][D]
+  const int* din_n;          // [S][K] incoming neurons
+  const int* din_s;          // [S][K] their slots
+  unsigned* gdone;           // [count] CTAs done reading layer first+i, zero beforehand
 };
 cudaError_t ffn_chain_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_optin, int n_sms,
                            int* n_stages, int* grid);

@@ -379,3 +379,51 @@ def test_max_sizes():
     wl = make_workload(cfg, device="cuda")
     summ = run_and_compare(wl, 3, check_buffers=False, sample_slots=64, check_layer_y=True)
     assert summ["max_h_rel"] < FFN_TOL
+
+
+# ---------------------------------------------------------------------------
+# Per-token pipeline (NP_TUNE_TOKEN_CHAIN=1): after layer 0, the predictor and
+# one set kernel, a single persistent launch reads every sparse layer's
+# incoming records into their slots and runs layers 1..L-1, each layer's FFN
+# waiting inside the kernel for its rows.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg,tokens,kw", [
+    (TINY, 6, {}),
+    (SMALL_F16, 8, {}),
+    (SMALL_BF16, 6, {}),
+    (SMALL_F16.replace(activation="swiglu"), 5, {}),
+    (LLAMA7B.replace(n_warm=0, n_decode=3), 3, {"check_buffers": False, "sample_slots": 64}),
+    (LLAMA13B.replace(n_warm=0, n_decode=2), 2, {"check_buffers": False, "sample_slots": 64}),
+], ids=["tiny", "small-f16", "small-bf16", "small-f16-swiglu", "llama2-7b", "llama2-13b"])
+def test_token_pipeline_matches_oracle(cfg, tokens, kw, monkeypatch):
+    monkeypatch.setenv("NP_TUNE_TOKEN_CHAIN", "1")
+    wl = make_workload(cfg, device="cuda")
+    summ = run_and_compare(wl, tokens, h2d_mode="fused", **kw)
+    assert summ["tokens"] == tokens
+    assert summ["max_h_rel"] < FFN_TOL
+
+
+def test_token_pipeline_replay_matches_eager(monkeypatch):
+    # the captured token (cooperative launches inside the graph) against the
+    # launches issued one by one: every FFN of this pipeline adds its split-K
+    # partials in a fixed order, so integer state and h agree bit for bit
+    monkeypatch.setenv("NP_TUNE_TOKEN_CHAIN", "1")
+    cfg = SMALL_F16
+    wl = make_workload(cfg)
+    outs = []
+    for graph in ("1", "0"):
+        monkeypatch.setenv("NP_TUNE_GRAPH", graph)
+        dec = build_decoder(wl, h2d_mode="fused")
+        hs, states = [], []
+        for t in range(6):
+            h = wl.x[t].cuda().clone()
+            dec.decode_token(h)
+            hs.append(h.cpu())
+            states.append([dec.get_state(cfg.n_dense + s) for s in range(cfg.n_sparse)])
+        dec.check_error()
+        outs.append((hs, states))
+        dec.close()
+    (h1, s1), (h0, s0) = outs
+    assert s1 == s0
+    for a, b in zip(h1, h0):
+        assert torch.equal(a, b)
