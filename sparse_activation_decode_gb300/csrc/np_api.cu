@@ -119,6 +119,7 @@ struct np_model {
   unsigned* arrive = nullptr;            // [2L] arrival counters of the chain
   unsigned* gdone = nullptr;             // [L] per-layer read counters of the per-token pipeline
   bool token_chain = false;              // one persistent launch reads and runs every layer after layer 0
+  int withhold_layer = -1;               // failure test hook, see NP_TEST_WITHHOLD_ARRIVAL
   float* chain_part = nullptr;           // [chain_grid][D] partial y of the chain
   int gather_grid = 0, scatter_grid = 0, pred_grid = 0;
   int rps1 = 1, rps2 = 1, ns1 = 2, ns2 = 2;
@@ -932,6 +933,10 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   const int tc_env = env_int("NP_TUNE_TOKEN_CHAIN", -1);
   m->token_chain = (tc_env == 1 || (tc_env == -1 && m->dn >= 2)) && m->B == 1 && m->S > 0 &&
                    m->d.pred_kind == NP_PRED_SHARED_ARGMAX && !m->compact && m->d.h2d_mode == NP_H2D_FUSED;
+  // Failure test hook (never set in normal use): NP_TEST_WITHHOLD_ARRIVAL=l
+  // withholds one reader arrival for layer l in the per-token pipeline, so
+  // that token ends with NP_ERR_TIMEOUT after the kernel's bounded waits.
+  m->withhold_layer = env_int("NP_TEST_WITHHOLD_ARRIVAL", -1);
   m->pdl_mask = env_int("NP_TUNE_PDL", 5);
   m->gather_grid = env_int("NP_TUNE_GATHER_CTAS", 32);
   m->scatter_grid = env_int("NP_TUNE_SCATTER_CTAS", 4 * m->sms);
@@ -1264,6 +1269,7 @@ FfnChainLaunch chain_args(np_model* m, int first, int count, float* h_dev) {
   a.n_stages = m->chain_stages;
   a.grid = m->chain_grid;
   a.err = m->err;
+  a.withhold = -1;
   return a;
 }
 
@@ -1344,6 +1350,7 @@ np_status enqueue_token(np_model* m, float* h_dev) {
     a.din_n = m->din_n;
     a.din_s = m->din_s;
     a.gdone = m->gdone;
+    a.withhold = m->withhold_layer >= 1 ? m->withhold_layer - 1 : -1;
     NP_TRY(launch(m, NP_KIND_FFN, st, 0, [&] { return launch_ffn_chain(a, st); }));
     return bump_token(m);
   }

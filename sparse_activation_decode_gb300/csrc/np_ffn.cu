@@ -741,7 +741,7 @@ __global__ void __launch_bounds__(kChainBlock, 1) ffn_chain_kernel(FfnChainLaunc
         // the rows written by every reader of this CTA, then one arrival
         asm volatile("fence.proxy.async.global;" ::: "memory");
         asm volatile("bar.sync 2, %0;" ::"n"(kChainReaders) : "memory");
-        if (rt == 0) {
+        if (rt == 0 && !(i == a.withhold && blockIdx.x == 0)) {
           __threadfence();
           atomicAdd(a.gdone + i, 1u);
         }

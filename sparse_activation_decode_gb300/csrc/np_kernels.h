@@ -71,6 +71,10 @@ struct FfnChainLaunch {
   const int* din_n;          // [S][K] incoming neurons
   const int* din_s;          // [S][K] their slots
   unsigned* gdone;           // [count] CTAs done reading layer first+i, zero beforehand
+  // Failure test hook: CTA 0's readers skip their arrival for chain layer
+  // `withhold` (-1: none), so that layer's count never completes and the
+  // bounded waits behind it run out (the kernel reports a timeout and exits).
+  int withhold;
 };
 cudaError_t ffn_chain_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_optin, int n_sms,
                            int* n_stages, int* grid);
