@@ -146,6 +146,16 @@ struct np_model {
   cudaStream_t ps = nullptr;
   cudaEvent_t ev_pin = nullptr, ev_psrc = nullptr;
   bool graph_off = false;       // disabled, or the capture failed
+  // token capture: the per-layer FFN kernel nodes in issue order, and the
+  // edges between consecutive ones made programmatic (relax_ffn_edges)
+  struct CapNode {
+    cudaStream_t st;
+    cudaGraphNode_t node;
+  };
+  bool capturing = false;
+  bool graph_pdl = true;
+  std::vector<CapNode> cap_ffn;
+  std::vector<std::pair<cudaGraphNode_t, cudaGraphNode_t>> relaxed;
   int64_t graph_launches = 0;   // kernels in one replay
   int64_t eager_tokens = 0;     // tokens issued launch by launch (the first one sets kernel attributes)
   std::vector<EventPair> prof_free;
@@ -344,8 +354,32 @@ np_status enqueue_tc_ffn(np_model* m, cudaStream_t st, int l, const float* hb, c
 
 // FFN of layer l (dense or sparse) for every sequence, on the kernel that
 // fits the batch: x = rmsnorm(hb + yprev), y added into y_acc.
+// During the token capture, remember the kernel node just added to `st`.
+void note_ffn_node(np_model* m, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaGraphNode_t* deps = nullptr;
+  size_t nd = 0;
+  if (cudaStreamGetCaptureInfo(st, &cs, nullptr, nullptr, &deps, nullptr, &nd) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  if (cs == cudaStreamCaptureStatusActive && nd == 1) m->cap_ffn.push_back({st, deps[0]});
+}
+
+np_status enqueue_layer_ffn_kernel(np_model* m, cudaStream_t st, int l, const float* hb, const float* yprev,
+                                   float* hb_out, float* y_acc, float* y_zero);
+
+// One layer's FFN kernel; under the token capture its node is recorded when
+// the kernel may take a programmatic edge from the previous layer's FFN.
 np_status enqueue_layer_ffn(np_model* m, cudaStream_t st, int l, const float* hb, const float* yprev,
                             float* hb_out, float* y_acc, float* y_zero) {
+  NP_TRY(enqueue_layer_ffn_kernel(m, st, l, hb, yprev, hb_out, y_acc, y_zero));
+  if (m->capturing && (!m->tc || (m->pdl_mask & 4) != 0)) note_ffn_node(m, st);
+  return NP_OK;
+}
+
+np_status enqueue_layer_ffn_kernel(np_model* m, cudaStream_t st, int l, const float* hb, const float* yprev,
+                                   float* hb_out, float* y_acc, float* y_zero) {
   if (m->tc) return enqueue_tc_ffn(m, st, l, hb, yprev, hb_out, y_acc, y_zero);
   if (l < m->dn) {
     const size_t proj_stride = (size_t)m->F * m->row_bytes;
@@ -924,6 +958,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   // their grids small leaves the SMs to the FFN running beside them.
   // NP_TUNE_GATHER_CTAS / NP_TUNE_SCATTER_CTAS override the defaults.
   m->graph_off = env_int("NP_TUNE_GRAPH", 1) == 0;
+  m->graph_pdl = env_int("NP_TUNE_GRAPH_PDL", 1) != 0;
   // Per-token pipeline: by default where a dense prefix of two or more
   // layers sits on the stream pipeline's FFN stream ahead of the sparse
   // layers (measured: Llama-2-13B shape 516 -> 540 tok/s; the 7B shape, one
@@ -1467,6 +1502,74 @@ np_status enqueue_token(np_model* m, float* h_dev) {
   return NP_OK;
 }
 
+// Put back the full edges that relax_ffn_edges made programmatic.
+bool restore_ffn_edges(np_model* m, cudaGraph_t g) {
+  cudaGraphEdgeData prog{};
+  prog.from_port = cudaGraphKernelNodePortProgrammatic;
+  prog.type = cudaGraphDependencyTypeProgrammatic;
+  const cudaGraphEdgeData full{};
+  bool ok = true;
+  for (auto& e : m->relaxed) {
+    if (cudaGraphRemoveDependencies(g, &e.first, &e.second, &prog, 1) != cudaSuccess ||
+        cudaGraphAddDependencies(g, &e.first, &e.second, &full, 1) != cudaSuccess)
+      ok = false;
+  }
+  m->relaxed.clear();
+  cudaGetLastError();
+  return ok;
+}
+
+// In the captured token, a layer's FFN that follows the previous layer's FFN
+// on its stream after event waits (its rows' reads, the predictions that
+// read its input buffers) has full edges from all of them: capture keeps a
+// programmatic edge only for a launch with one dependency, and one from
+// another stream would be unsound (that stream's kernel writes the rows).
+// Here the edge from the previous FFN alone becomes programmatic.  Both FFN
+// kernels trigger their dependents as they start; before griddepcontrol.wait
+// they read only weights, row counts, row lists and slot maps, which come
+// from the set kernel and the layer's reads through the full edges that
+// stay; every CTA waits before it reads h or y or writes anything.  So
+// layer l's rows stream while layer l-1 finishes, as between back-to-back
+// launches on one stream.  Returns false on an API error (edges changed so
+// far are put back).
+bool relax_ffn_edges(np_model* m, cudaGraph_t g) {
+  cudaGraphEdgeData prog{};
+  prog.from_port = cudaGraphKernelNodePortProgrammatic;
+  prog.type = cudaGraphDependencyTypeProgrammatic;
+  m->relaxed.clear();
+  auto fail = [&] {
+    restore_ffn_edges(m, g);
+    return false;
+  };
+  for (size_t i = 1; i < m->cap_ffn.size(); ++i) {
+    cudaGraphNode_t prev = nullptr;  // the previous FFN node on the same stream
+    for (size_t j = i; j-- > 0;)
+      if (m->cap_ffn[j].st == m->cap_ffn[i].st) {
+        prev = m->cap_ffn[j].node;
+        break;
+      }
+    if (!prev) continue;
+    cudaGraphNode_t node = m->cap_ffn[i].node;
+    size_t nd = 0;
+    if (cudaGraphNodeGetDependencies(node, nullptr, nullptr, &nd) != cudaSuccess) return fail();
+    std::vector<cudaGraphNode_t> deps(nd);
+    std::vector<cudaGraphEdgeData> ed(nd);
+    if (nd > 0 && cudaGraphNodeGetDependencies(node, deps.data(), ed.data(), &nd) != cudaSuccess) return fail();
+    for (size_t k = 0; k < nd; ++k) {
+      // only a full edge straight from the previous FFN (another operation
+      // between the two on the stream would be the dependency instead)
+      if (deps[k] != prev || ed[k].type != cudaGraphDependencyTypeDefault || ed[k].from_port != 0) continue;
+      if (cudaGraphRemoveDependencies(g, &prev, &node, &ed[k], 1) != cudaSuccess) return fail();
+      if (cudaGraphAddDependencies(g, &prev, &node, &prog, 1) != cudaSuccess) {
+        cudaGraphAddDependencies(g, &prev, &node, &ed[k], 1);
+        return fail();
+      }
+      m->relaxed.push_back({prev, node});
+    }
+  }
+  return true;
+}
+
 // Capture one token's launches (every stream, forked from and joined back to
 // the main stream) as a graph over h_io.  A failed capture leaves the model
 // on eager launches.
@@ -1483,15 +1586,29 @@ np_status capture_token(np_model* m) {
     m->graph_off = true;
     return NP_OK;
   }
+  m->capturing = true;
+  m->cap_ffn.clear();
   const np_status st = enqueue_token(m, m->h_io);
+  m->capturing = false;
   cudaGraph_t g = nullptr;
   e = cudaStreamEndCapture(m->main, &g);
   begin_call(m);
   m->main = user_main;
   m->pending_bits = 0;  // the capture only recorded the work
   m->committed_since_token = 0;
-  if (st == NP_OK && e == cudaSuccess && g) e = cudaGraphInstantiate(&m->graph, g, 0);
+  if (st == NP_OK && e == cudaSuccess && g) {
+    if (m->graph_pdl && !relax_ffn_edges(m, g) && env_int("NP_TUNE_VERBOSE", 0) == 1)
+      std::fprintf(stderr, "np: FFN edges left full (%s)\n", cudaGetErrorString(cudaGetLastError()));
+    e = cudaGraphInstantiate(&m->graph, g, 0);
+    if (e != cudaSuccess && !m->relaxed.empty()) {
+      // instantiate the token with full edges instead
+      cudaGetLastError();
+      m->graph = nullptr;
+      e = restore_ffn_edges(m, g) ? cudaGraphInstantiate(&m->graph, g, 0) : cudaErrorUnknown;
+    }
+  }
   if (g) cudaGraphDestroy(g);
+  m->cap_ffn.clear();
   if (st != NP_OK || e != cudaSuccess || !m->graph) {
     if (env_int("NP_TUNE_VERBOSE", 0) == 1)
       std::fprintf(stderr, "np: token capture failed (status %d, %s; %s)\n", (int)st, cudaGetErrorString(e),
@@ -1503,7 +1620,8 @@ np_status capture_token(np_model* m) {
   m->graph_launches = m->launches - l0;
   m->launches = l0;
   if (m->graph && env_int("NP_TUNE_VERBOSE", 0) == 1)
-    std::fprintf(stderr, "np: token captured (%lld kernels)\n", (long long)m->graph_launches);
+    std::fprintf(stderr, "np: token captured (%lld kernels, %zu programmatic FFN edges)\n",
+                 (long long)m->graph_launches, m->relaxed.size());
   return NP_OK;
 }
 

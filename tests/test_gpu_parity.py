@@ -1,5 +1,6 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle."""
 import ctypes
+import re
 
 import numpy as np
 import pytest
@@ -374,6 +375,29 @@ def test_graph_replay_matches_eager(cfg, monkeypatch):
     assert s1 == s0
     for a, b in zip(h1, h0):
         assert oracle.rel_l2(a.numpy().ravel(), b.numpy().ravel()) < 1e-5
+
+
+@pytest.mark.parametrize("cfg,tokens,kw", [
+    (SMALL_F16, 6, {"h2d_mode": "fused"}),
+    (SMALL_BF16, 6, {}),                      # dense layer 1 -> the first sparse layer as well
+    (SMALL_BATCHED, 6, {}),
+    (SMALL_OPT.replace(lookahead=2), 6, {"h2d_mode": "fused"}),
+    (BATCHED7B, 4, {"check_buffers": False, "sample_slots": 64}),
+], ids=["small-f16-fused", "small-bf16", "small-batched", "small-opt-lookahead2-fused", "llama2-7b-batch8"])
+def test_graph_programmatic_ffn_edges(cfg, tokens, kw, monkeypatch, capfd):
+    # in the captured token each layer's FFN takes a programmatic edge from
+    # the previous layer's FFN, while the edges from its rows' reads (and
+    # from predictions that read its input buffers) stay full; the replayed
+    # tokens must agree with the oracle as the eager first token does
+    monkeypatch.setenv("NP_TUNE_VERBOSE", "1")
+    wl = make_workload(cfg.replace(n_warm=0, n_decode=tokens), device="cuda")
+    summ = run_and_compare(wl, tokens, **kw)
+    err = capfd.readouterr().err
+    cap = re.search(r"token captured \((\d+) kernels, (\d+) programmatic FFN edges\)", err)
+    assert cap, err[-2000:]
+    assert int(cap.group(2)) >= 1
+    assert summ["tokens"] == tokens
+    assert summ["max_h_rel"] < FFN_TOL
 
 
 def test_max_sizes():
