@@ -123,6 +123,7 @@ struct np_model {
   float* chain_part = nullptr;           // [chain_grid][D] partial y of the chain
   int gather_grid = 0, scatter_grid = 0, pred_grid = 0;
   int rps1 = 1, rps2 = 1, ns1 = 2, ns2 = 2;
+  int ns1_side = 2, ns2_side = 2;  // predictor rings beside an FFN (lookahead stream)
   // state
   uint64_t pending_bits = 0, committed_since_token = 0;
   int64_t token = 0;
@@ -548,10 +549,11 @@ np_status enqueue_predict(np_model* m, int layer, const float* h, bool want_ids 
   const unsigned char* w2 =
       static_cast<const unsigned char*>(m->d.pred_w2) + (size_t)layer * m->F * m->H * m->esz;
   const unsigned char* b2 = static_cast<const unsigned char*>(m->d.pred_b2) + (size_t)layer * m->F * m->esz;
+  const bool side = m->ps && m->main == m->ps;  // beside the FFN stream
   NP_TRY(enqueue_rowdot(m, w1, m->H, m->D, h, 1, 0, nullptr, m->z, nullptr, 0, nullptr, m->fire, m->W, m->rps1,
-                        m->ns1, h2));
+                        side ? m->ns1_side : m->ns1, h2));
   return enqueue_rowdot(m, w2, m->F, m->H, m->z, 0, 2, b2, m->logits, nullptr, 0, m->fire, nullptr, 0, m->rps2,
-                        m->ns2);
+                        side ? m->ns2_side : m->ns2);
 }
 
 SetLaunch set_args(np_model* m, int first_sparse, int n_layers);
@@ -978,6 +980,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if (m->gather_grid < 1) m->gather_grid = 32;
   if (m->scatter_grid < 1) m->scatter_grid = 4 * m->sms;
   m->pred_grid = 2 * m->sms;
+  if (env_int("NP_TUNE_PRED_CTAS", 0) > 0) m->pred_grid = env_int("NP_TUNE_PRED_CTAS", 0);
   if (env_int("NP_TUNE_VERBOSE", 0) == 1)
     std::fprintf(stderr, "np: ffn grid %d, ring %d slots; gather %d scatter %d CTAs\n", m->ffn_grid, m->ffn_stages,
                  m->gather_grid, m->scatter_grid);
@@ -986,6 +989,32 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   m->ns1 = pick_stages(m->rps1 * m->row_bytes, rowdot_smem_bytes(m->D, m->esz, m->rps1, 0), per_cta);
   m->ns2 = pick_stages(m->rps2 * (size_t)m->H * m->esz, rowdot_smem_bytes(m->H, m->esz, m->rps2, 0), per_cta);
   if (m->ns1 < 2 || m->ns2 < 2) return fail(arg_fail("predictor rows too large for the shared-memory ring"));
+  {
+    // The per-layer predictor with a lookahead runs on its own stream beside
+    // the FFN.  Its CTAs (two per SM) then share each SM with one FFN CTA, so
+    // their rings are cut to what fits beside it; otherwise a second
+    // predictor CTA finds no room on SMs that hold an FFN CTA and the
+    // predictor runs in two waves.  Measured on the OPT window workload
+    // (lookahead 2): 666-686 tok/s with the full rings, 730-754 with rings
+    // that fit; alone, the full rings stream faster (0.59 vs 0.47 of HBM).
+    int smem_sm = 0;
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    const size_t ffn_cta = ffn_smem_bytes(m->D, m->esz, m->nproj, m->ffn_stages) + 1024;
+    const size_t pair = (size_t)smem_sm > ffn_cta ? ((size_t)smem_sm - ffn_cta) / 2 : 0;
+    const size_t side = pair > 1024 ? pair - 1024 : 0;
+    const int s1 = pick_stages(m->rps1 * m->row_bytes, rowdot_smem_bytes(m->D, m->esz, m->rps1, 0), side);
+    const int s2 = pick_stages(m->rps2 * (size_t)m->H * m->esz, rowdot_smem_bytes(m->H, m->esz, m->rps2, 0), side);
+    m->ns1_side = s1 >= 2 ? std::min(s1, m->ns1) : m->ns1;
+    m->ns2_side = s2 >= 2 ? std::min(s2, m->ns2) : m->ns2;
+    // NP_TUNE_PRED_STAGES caps every predictor ring (for sweeps)
+    const int cap = env_int("NP_TUNE_PRED_STAGES", 0);
+    if (cap >= 2) {
+      m->ns1 = std::min(m->ns1, cap);
+      m->ns2 = std::min(m->ns2, cap);
+      m->ns1_side = std::min(m->ns1_side, cap);
+      m->ns2_side = std::min(m->ns2_side, cap);
+    }
+  }
 
   // allocations
   const size_t S = (size_t)m->S, F = m->F, K = m->K;
