@@ -109,6 +109,7 @@ struct np_model {
   std::vector<void*> allocs;
   // launch shapes
   int ffn_grid = 0, ffn_stages = 0;
+  int ffn_stages_dense = 0;              // ring of the dense layers' FFN launches
   int chain_grid = 0, chain_stages = 0;  // persistent FFN chain (batch 1)
   int pdl_mask = 5;                      // programmatic dependent launch: 1 predictor, 2 set kernel, 4 tensor-core kernels
   // streams whose last operation is a kernel launched by the current API
@@ -343,7 +344,7 @@ np_status enqueue_ffn(np_model* m, cudaStream_t st, int kind, const unsigned cha
   a.dtype_bytes = m->esz;
   a.gated = m->d.has_gate;
   a.swiglu = m->d.activation == NP_ACT_SWIGLU;
-  a.n_stages = m->ffn_stages;
+  a.n_stages = kind == NP_KIND_DENSE ? m->ffn_stages_dense : m->ffn_stages;
   a.grid = m->ffn_grid;
   a.err = m->err;
   a.pdl = pdl_for(m, st, 0);
@@ -950,6 +951,21 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     }
     const int ctas = env_int("NP_TUNE_FFN_CTAS", 0);
     if (ctas > 0) m->ffn_grid = ctas;
+    // A dense layer streams every row of d_ff (72 per CTA at the 7B shape)
+    // and, as the token's first kernel, runs alone: a deeper ring with one
+    // CTA per SM keeps the rows ahead of the consumers (7B dense layer 0 in
+    // the decode: 54 -> 49 us).  The sparse layers keep the two-per-SM ring,
+    // so that the next layer's CTAs and the reads fit beside them.
+    // NP_TUNE_DENSE_SLOTS sets the dense ring (default 6).
+    m->ffn_stages_dense = m->ffn_stages;
+    int ds = env_int("NP_TUNE_DENSE_SLOTS", 6);
+    if (ds > 16) ds = 16;
+    while (ds > m->ffn_stages && ffn_smem_bytes(m->D, m->esz, m->nproj, ds) > m->smem_optin - 1024) --ds;
+    if (m->dn > 0 && ds > m->ffn_stages) {
+      if ((e = ffn_set_smem(m->d.dtype, m->d.has_gate, m->D, m->esz, ds)) != cudaSuccess)
+        return fail(cuda_fail(e, "ffn_set_smem"));
+      m->ffn_stages_dense = ds;
+    }
     if (m->B == 1) {
       e = ffn_chain_plan(m->d.dtype, m->d.has_gate, m->D, m->esz, m->smem_optin - 1024, m->sms, &m->chain_stages,
                          &m->chain_grid);

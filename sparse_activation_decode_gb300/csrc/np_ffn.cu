@@ -34,6 +34,10 @@
 //  * split-K over CTAs: each CTA adds its partial y to the layer's
 //    accumulator with vector atomics (fp32; the order of the CTAs' additions
 //    is not fixed).
+#include <mutex>
+#include <tuple>
+#include <vector>
+
 #include "np_common.cuh"
 #include "np_kernels.h"
 
@@ -949,6 +953,29 @@ static void* pick_chain_kernel(int dtype, bool gated, int D, int dtype_bytes) {
                     : dtype == 1 ? chain_kernel_for<__half, false>(mc) : chain_kernel_for<__nv_bfloat16, false>(mc);
 }
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` unless it is
+// already at least that on this device.  The limit is per kernel, not per
+// model, so it never goes down: a model planned later with smaller rings
+// leaves the launches of a model planned earlier valid.
+static cudaError_t raise_smem(const void* k, size_t bytes) {
+  static std::mutex mu;
+  static std::vector<std::tuple<const void*, int, size_t>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto& t : done)
+    if (std::get<0>(t) == k && std::get<1>(t) == dev) {
+      if (bytes <= std::get<2>(t)) return cudaSuccess;
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+      if (e == cudaSuccess) std::get<2>(t) = bytes;
+      return e;
+    }
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done.emplace_back(k, dev, bytes);
+  return e;
+}
+
 size_t ffn_smem_bytes(int D, int dtype_bytes, int nproj, int n_stages) {
   return 512 + (size_t)n_stages * nproj * D * dtype_bytes + 1024;  // barriers/rows, ring, partial sums
 }
@@ -971,7 +998,7 @@ cudaError_t ffn_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_p
   if (ffn_smem_bytes(D, dtype_bytes, nproj, ns) > per_cta) return cudaErrorInvalidValue;
   void* k = pick_kernel(dtype, gated != 0, D, dtype_bytes);
   const size_t smem = ffn_smem_bytes(D, dtype_bytes, nproj, ns);
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = raise_smem(k, smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kFfnBlock, smem);
@@ -986,8 +1013,7 @@ cudaError_t ffn_plan(int dtype, int gated, int D, int dtype_bytes, size_t smem_p
 
 cudaError_t ffn_set_smem(int dtype, int gated, int D, int dtype_bytes, int n_stages) {
   void* k = pick_kernel(dtype, gated != 0, D, dtype_bytes);
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)ffn_smem_bytes(D, dtype_bytes, gated ? 3 : 2, n_stages));
+  return raise_smem(k, ffn_smem_bytes(D, dtype_bytes, gated ? 3 : 2, n_stages));
 }
 
 cudaError_t launch_ffn_rows(const FfnLaunch& a, cudaStream_t st) {
@@ -1015,7 +1041,7 @@ cudaError_t ffn_chain_plan(int dtype, int gated, int D, int dtype_bytes, size_t 
   const size_t smem = chain_smem_bytes(D, dtype_bytes, nproj, ns);
   if (smem > smem_optin) return cudaErrorInvalidValue;
   void* k = pick_chain_kernel(dtype, gated != 0, D, dtype_bytes);
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = raise_smem(k, smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kChainBlock, smem);
