@@ -774,9 +774,11 @@ np_status sync_model(np_model* m) {
   return NP_OK;
 }
 
-int pick_rps(size_t row_bytes) {
+// Rows per predictor ring stage: powers of two up to 8 whose stage stays
+// within `stage_cap` bytes (NP_TUNE_PRED_STAGE_BYTES, default 24 KiB).
+int pick_rps(size_t row_bytes, size_t stage_cap) {
   int r = 1;
-  while (r < 8 && (size_t)(r * 2) * row_bytes <= 24576) r *= 2;
+  while (r < 8 && (size_t)(r * 2) * row_bytes <= stage_cap) r *= 2;
   return r;
 }
 
@@ -1000,8 +1002,17 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if (env_int("NP_TUNE_VERBOSE", 0) == 1)
     std::fprintf(stderr, "np: ffn grid %d, ring %d slots; gather %d scatter %d CTAs\n", m->ffn_grid, m->ffn_stages,
                  m->gather_grid, m->scatter_grid);
-  m->rps1 = pick_rps(m->row_bytes);
-  m->rps2 = pick_rps((size_t)m->H * m->esz);
+  {
+    // The shared predictor streams long runs of rows alone or beside the
+    // sparse FFNs: 48 KiB stages halve its block barriers per byte (7B heads
+    // alone 93.5 -> 90.6 us, 13B 117 -> 114 us).  The per-layer predictor
+    // keeps 24 KiB stages, so that its rings still fit beside an FFN CTA.
+    const int dflt = m->d.pred_kind == NP_PRED_SHARED_ARGMAX ? 49152 : 24576;
+    const int cap = env_int("NP_TUNE_PRED_STAGE_BYTES", dflt);
+    const size_t stage_cap = cap > 0 ? (size_t)cap : (size_t)dflt;
+    m->rps1 = pick_rps(m->row_bytes, stage_cap);
+    m->rps2 = pick_rps((size_t)m->H * m->esz, stage_cap);
+  }
   m->ns1 = pick_stages(m->rps1 * m->row_bytes, rowdot_smem_bytes(m->D, m->esz, m->rps1, 0), per_cta);
   m->ns2 = pick_stages(m->rps2 * (size_t)m->H * m->esz, rowdot_smem_bytes(m->H, m->esz, m->rps2, 0), per_cta);
   if (m->ns1 < 2 || m->ns2 < 2) return fail(arg_fail("predictor rows too large for the shared-memory ring"));

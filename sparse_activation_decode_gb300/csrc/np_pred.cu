@@ -33,6 +33,18 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
   return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
 }
 
+namespace {
+// d = a * b + c on a pair of floats (one packed FP32x2 FMA)
+__device__ __forceinline__ float2 fma_pair(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+}  // namespace
+
 template <typename T, int RPS>
 __global__ void __launch_bounds__(kThreads, 2) rowdot_kernel(RowdotLaunch a) {
   static_assert(RPS <= 32 && 32 % RPS == 0, "a group's rows must share one mask word");
@@ -88,12 +100,15 @@ __global__ void __launch_bounds__(kThreads, 2) rowdot_kernel(RowdotLaunch a) {
     for (int j = tid; j < len; j += kThreads) xs[j] = a.vec[j];
     __syncthreads();
   }
-  float xr[kMaxChunksPerThread][E];
+  // x in registers as float pairs: each row's dot product runs as two
+  // interleaved fp32 sums (even and odd elements), added at the end
+  float2 xr[kMaxChunksPerThread][E / 2];
 #pragma unroll
   for (int k = 0; k < kMaxChunksPerThread; ++k) {
     const int c = tid + k * kThreads;
 #pragma unroll
-    for (int e = 0; e < E; ++e) xr[k][e] = (c < NC) ? xs[c * E + e] : 0.f;
+    for (int e = 0; e < E / 2; ++e)
+      xr[k][e] = (c < NC) ? make_float2(xs[c * E + 2 * e], xs[c * E + 2 * e + 1]) : make_float2(0.f, 0.f);
   }
 
   int issued_upto = my_n < a.n_stages ? my_n : a.n_stages;
@@ -103,9 +118,9 @@ __global__ void __launch_bounds__(kThreads, 2) rowdot_kernel(RowdotLaunch a) {
     const bool ok = mbar_wait(&bars[s], (uint32_t)(j / a.n_stages) & 1u, a.err);
     const int nr = rows_in(j);
     const uint4* st = reinterpret_cast<const uint4*>(stages + (size_t)s * stage_bytes);
-    float p[RPS];
+    float2 p2[RPS];
 #pragma unroll
-    for (int r = 0; r < RPS; ++r) p[r] = 0.f;
+    for (int r = 0; r < RPS; ++r) p2[r] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < kMaxChunksPerThread; ++k) {
       const int c = tid + k * kThreads;
@@ -116,11 +131,14 @@ __global__ void __launch_bounds__(kThreads, 2) rowdot_kernel(RowdotLaunch a) {
             float f[E];
             Elem<T>::load(st[r * NC + c], f);
 #pragma unroll
-            for (int e = 0; e < E; ++e) p[r] = fmaf(f[e], xr[k][e], p[r]);
+            for (int e = 0; e < E / 2; ++e) p2[r] = fma_pair(make_float2(f[2 * e], f[2 * e + 1]), xr[k][e], p2[r]);
           }
         }
       }
     }
+    float p[RPS];
+#pragma unroll
+    for (int r = 0; r < RPS; ++r) p[r] = p2[r].x + p2[r].y;
     float* rb = red + (j & 1) * 8 * RPS;
 #pragma unroll
     for (int r = 0; r < RPS; ++r) {
@@ -131,8 +149,9 @@ __global__ void __launch_bounds__(kThreads, 2) rowdot_kernel(RowdotLaunch a) {
       aborted = true;
       break;
     }
-    if (tid == 0 && j >= 1 && j - 1 + a.n_stages < my_n) {
-      issue(j - 1 + a.n_stages);
+    // every thread has read stage j (the barrier above): refill it
+    if (tid == 0 && j + a.n_stages < my_n) {
+      issue(j + a.n_stages);
       ++issued_upto;
     }
     const int row0 = ((int)blockIdx.x + j * (int)gridDim.x) * RPS;
