@@ -36,14 +36,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # source file still has the recorded hash.
 NCU_TRAFFIC = {
     ("gather", "llama2-7b-relu"): {"src": "np_scatter.cu", "src_hash": "92078b0e6f793061", "bytes_per_launch": 113408},
-    ("ffn", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "1dee64556eebfcef", "bytes_per_launch": 50403000},
-    ("dense", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "1dee64556eebfcef", "bytes_per_launch": 273352000},
+    ("ffn", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "6f6a8b516ec3344b", "bytes_per_launch": 50404000},
+    ("dense", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "6f6a8b516ec3344b", "bytes_per_launch": 273740000},
     # one persistent launch over the 31 sparse layers, per layer
-    ("ffn_chain", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "1dee64556eebfcef",
-                                      "bytes_per_launch": 50485000},
+    ("ffn_chain", "llama2-7b-relu"): {"src": "np_ffn.cu", "src_hash": "6f6a8b516ec3344b",
+                                      "bytes_per_launch": 50480000},
     # the per-token pipeline's persistent launch (layers 1..39), scaled from a
     # 12-layer capture by the sparse layers it covers
-    ("token_pipeline", "llama2-13b-relu"): {"src": "np_ffn.cu", "src_hash": "1dee64556eebfcef",
+    ("token_pipeline", "llama2-13b-relu"): {"src": "np_ffn.cu", "src_hash": "6f6a8b516ec3344b",
                                            "bytes_per_launch": 3384000000},
     # mean of the two standalone sparse launches of the capture; dense layer 0
     ("ffn", "llama2-7b-batch8"): {"src": "np_mma.cu", "src_hash": "c5045b62f412d001", "bytes_per_launch": 84082560},
