@@ -150,7 +150,7 @@ OPT67B = Config(
 BATCHED7B = Config(
     name="llama2-7b-batch8", n_layers=32, n_dense=1, d_model=4096, d_ff=11008,
     k_max=4096, n_centroids=1024, dtype="bf16", density=0.055, persistence=0.83,
-    pred_hidden=2816, batch=8, n_warm=0, n_decode=256, seed=1004)
+    pred_hidden=2816, batch=8, n_warm=128, n_decode=256, seed=1004)
 # density 0.055 with sequences two chain links apart puts the union of the
 # eight sequences' gate|up sets near 30% of d_ff at persistence 0.83 (48-52%
 # at 0.5, 18% at 0.95; above K_max = 37% it is capped).
