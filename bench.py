@@ -317,7 +317,10 @@ def isolated_kernels(dec, torch, cfg, reps=5):
         out["dense"] = {"us_per_launch": round(1e3 * ms, 3), "bytes_per_launch": byt,
                         "gbs": round(byt / (ms * 1e-3) / 1e9, 1)}
     ms = timed(lambda: dec.predict(h), reps)
-    byt = (cfg.pred_hidden * cfg.d_model + cfg.n_heads * cfg.n_centroids * cfg.pred_hidden) * cfg.elem_bytes
+    if cfg.pred_kind == "shared_argmax":  # W1, then every head's centroid rows
+        byt = (cfg.pred_hidden * cfg.d_model + cfg.n_heads * cfg.n_centroids * cfg.pred_hidden) * cfg.elem_bytes
+    else:  # one layer's W1, W2 and output bias
+        byt = (cfg.pred_hidden * cfg.d_model + cfg.d_ff * cfg.pred_hidden + cfg.d_ff) * cfg.elem_bytes
     out["predictor"] = {"us_per_call": round(1e3 * ms, 3), "bytes_per_call": byt,
                         "gbs": round(byt / (ms * 1e-3) / 1e9, 1)}
     return out
