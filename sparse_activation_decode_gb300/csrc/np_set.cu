@@ -177,6 +177,11 @@ __device__ __forceinline__ void compact_assign(const SetLaunch& a, int s, int ti
   }
 }
 
+// HIST: window or frequency residency, which keeps a per-neuron history (the
+// last token a neuron was active, or its count).  Without it the kernel has
+// no history registers and needs half the register file, so its CTA fits
+// beside another kernel's CTAs on one SM.
+template <bool HIST>
 __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   __shared__ int wsum[32];
   __shared__ unsigned long long wsum64[32];
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   int* __restrict__ inv = a.inv + (size_t)s * K;
   int* __restrict__ ct = a.content + (size_t)s * K;
   uint32_t* __restrict__ res = a.resbits + (size_t)s * W;
-  int* __restrict__ ls = (a.window > 1 || a.frequency) ? a.last_seen + (size_t)s * F : nullptr;
+  int* __restrict__ ls = HIST ? a.last_seen + (size_t)s * F : nullptr;
   int* __restrict__ out_a = a.active + (size_t)s * K;
   int* __restrict__ out_as = a.active_slot + (size_t)s * K;
   int* __restrict__ out_in = a.din_n + (size_t)s * K;
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   grid_dependents_launch();
   const uint32_t rw = has_word ? res[i] : 0u;
   int lsv[32];  // history of the resident neurons now, of the newly active ones below
-  if (ls) {
+  if (HIST) {
 #pragma unroll
     for (int b = 0; b < 32; ++b) lsv[b] = ((rw >> b) & 1u) ? ls[i * 32 + b] : 0;
   }
@@ -282,13 +287,13 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
   // 3. resident set after this token (bit loops are unrolled so that the
   //    history stays in registers)
   uint32_t nw = aw;
-  if (ls) {
+  if (HIST) {
     const uint32_t fresh = aw & ~rw;
 #pragma unroll
     for (int b = 0; b < 32; ++b)
       if ((fresh >> b) & 1u) lsv[b] = ls[i * 32 + b];
   }
-  if (a.window > 1) {
+  if (HIST && a.window > 1) {
     const uint32_t old = rw & ~aw;  // resident, not active now
     uint32_t keep_old = 0;
 #pragma unroll
@@ -331,7 +336,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
       cand &= ~(older | evict_b);
     }
     nw = cand;
-  } else if (a.frequency) {
+  } else if (HIST && a.frequency) {
     uint32_t old = rw & ~aw;  // resident, not active now
     int ctot;
     (void)block_scan(__popc(aw | old), wsum, &ctot);
@@ -494,7 +499,7 @@ __global__ void __launch_bounds__(kSetThreads) set_kernel(SetLaunch a) {
     out_as[bit_rank(s_a, s_ea, n)] = k;
   }
   if (has_word) res[i] = nw;
-  if (ls && has_word) {  // this word's active neurons, history from registers
+  if (HIST && has_word) {  // this word's active neurons, history from registers
     int r = ea;
 #pragma unroll
     for (int b = 0; b < 32; ++b) {
@@ -602,14 +607,18 @@ __global__ void reset_state_kernel(int* slotmap, int* inv, uint32_t* resbits, in
   for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n_res; k += stride) resbits[k] = 0u;
 }
 
+template <bool HIST> struct SetTag {};
+
 cudaError_t launch_set(const SetLaunch& a, cudaStream_t st) {
   if (a.words > kMaxWords || a.K > kMaxKmax) return cudaErrorInvalidValue;
   const size_t dyn = 6 * (size_t)a.K * sizeof(int);
-  cudaError_t e = ensure_dyn_smem<SetLaunch>(reinterpret_cast<const void*>(set_kernel), dyn);
+  const bool hist = a.window > 1 || a.frequency;
+  cudaError_t e = hist ? ensure_dyn_smem<SetTag<true>>(reinterpret_cast<const void*>(set_kernel<true>), dyn)
+                       : ensure_dyn_smem<SetTag<false>>(reinterpret_cast<const void*>(set_kernel<false>), dyn);
   if (e != cudaSuccess) return e;
   PdlConfig c(dim3(a.n_layers_launch), dim3(kSetThreads), dyn, st);
   c.cfg.numAttrs = a.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&c.cfg, set_kernel, a);
+  return hist ? cudaLaunchKernelEx(&c.cfg, set_kernel<true>, a) : cudaLaunchKernelEx(&c.cfg, set_kernel<false>, a);
 }
 
 cudaError_t launch_rollback(const SetLaunch& a, cudaStream_t st) {
