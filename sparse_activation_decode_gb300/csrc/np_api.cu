@@ -157,7 +157,8 @@ struct np_model {
   bool capturing = false;
   bool graph_pdl = true;
   std::vector<CapNode> cap_ffn;
-  std::vector<std::pair<cudaGraphNode_t, cudaGraphNode_t>> relaxed;
+  std::vector<std::pair<cudaGraphNode_t, cudaGraphNode_t>> relaxed;  // valid until the graph is destroyed
+  size_t graph_pdl_edges = 0;   // programmatic FFN edges in the instantiated token
   int64_t graph_launches = 0;   // kernels in one replay
   int64_t eager_tokens = 0;     // tokens issued launch by launch (the first one sets kernel attributes)
   std::vector<EventPair> prof_free;
@@ -1663,6 +1664,8 @@ np_status capture_token(np_model* m) {
       e = restore_ffn_edges(m, g) ? cudaGraphInstantiate(&m->graph, g, 0) : cudaErrorUnknown;
     }
   }
+  m->graph_pdl_edges = m->graph ? m->relaxed.size() : 0;
+  m->relaxed.clear();  // node handles of the graph destroyed below
   if (g) cudaGraphDestroy(g);
   m->cap_ffn.clear();
   if (st != NP_OK || e != cudaSuccess || !m->graph) {
@@ -1677,7 +1680,7 @@ np_status capture_token(np_model* m) {
   m->launches = l0;
   if (m->graph && env_int("NP_TUNE_VERBOSE", 0) == 1)
     std::fprintf(stderr, "np: token captured (%lld kernels, %zu programmatic FFN edges)\n",
-                 (long long)m->graph_launches, m->relaxed.size());
+                 (long long)m->graph_launches, m->graph_pdl_edges);
   return NP_OK;
 }
 
