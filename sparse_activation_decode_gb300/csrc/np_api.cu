@@ -129,7 +129,7 @@ struct np_model {
   uint64_t pending_bits = 0, committed_since_token = 0;
   int64_t token = 0;
   int64_t launches = 0;
-  cudaEvent_t ev_set = nullptr, ev_side_done = nullptr, ev_j[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t ev_set = nullptr, ev_side_done = nullptr, ev_j[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   cudaEvent_t ev_pre = nullptr, ev_ffn = nullptr;
   std::vector<cudaEvent_t> ev_g, ev_layer;  // per sparse layer: gathered, ready
   // profiling
@@ -147,6 +147,14 @@ struct np_model {
   // ev_psrc: the predictions reading it are done)
   cudaStream_t ps = nullptr;
   cudaEvent_t ev_pin = nullptr, ev_psrc = nullptr;
+  // and the set kernels on a stream of their own (ss), so that layer j's set
+  // kernel runs beside layer j+1's predictor: two firing-mask buffers
+  // alternate by layer; ev_pdone[b]: the predictor that wrote buffer b is
+  // done; ev_sdone[b]: the set kernel that read it is done
+  bool set_stream = true;
+  cudaStream_t ss = nullptr;
+  cudaEvent_t ev_pdone[2] = {nullptr, nullptr}, ev_sdone[2] = {nullptr, nullptr};
+  uint32_t* fire2 = nullptr;
   bool graph_off = false;       // disabled, or the capture failed
   // token capture: the per-layer FFN kernel nodes in issue order, and the
   // edges between consecutive ones made programmatic (relax_ffn_edges)
@@ -530,7 +538,9 @@ np_status enqueue_pred_hidden(np_model* m, const float* h, const float* h2) {
                         reinterpret_cast<uint32_t*>(m->keys), 2 * m->NH, m->rps1, m->ns1, h2);
 }
 
-np_status enqueue_predict(np_model* m, int layer, const float* h, bool want_ids = true, const float* h2 = nullptr) {
+np_status enqueue_predict(np_model* m, int layer, const float* h, bool want_ids = true, const float* h2 = nullptr,
+                          uint32_t* fire = nullptr) {
+  if (!fire) fire = m->fire;
   if (m->tc) {
     NP_TRY(enqueue_tc_hidden(m, h, nullptr));
     NP_TRY(enqueue_tc_heads(m, 0, m->NH));
@@ -552,9 +562,9 @@ np_status enqueue_predict(np_model* m, int layer, const float* h, bool want_ids 
       static_cast<const unsigned char*>(m->d.pred_w2) + (size_t)layer * m->F * m->H * m->esz;
   const unsigned char* b2 = static_cast<const unsigned char*>(m->d.pred_b2) + (size_t)layer * m->F * m->esz;
   const bool side = m->ps && m->main == m->ps;  // beside the FFN stream
-  NP_TRY(enqueue_rowdot(m, w1, m->H, m->D, h, 1, 0, nullptr, m->z, nullptr, 0, nullptr, m->fire, m->W, m->rps1,
+  NP_TRY(enqueue_rowdot(m, w1, m->H, m->D, h, 1, 0, nullptr, m->z, nullptr, 0, nullptr, fire, m->W, m->rps1,
                         side ? m->ns1_side : m->ns1, h2));
-  return enqueue_rowdot(m, w2, m->F, m->H, m->z, 0, 2, b2, m->logits, nullptr, 0, m->fire, nullptr, 0, m->rps2,
+  return enqueue_rowdot(m, w2, m->F, m->H, m->z, 0, 2, b2, m->logits, nullptr, 0, fire, nullptr, 0, m->rps2,
                         side ? m->ns2_side : m->ns2);
 }
 
@@ -601,8 +611,8 @@ cudaStream_t gather_stream(const np_model* m, int s) { return (s & 1) ? m->g1 : 
 
 // Make `st` wait for all work queued so far on the gather and scatter streams.
 np_status join_side(np_model* m, cudaStream_t st) {
-  const cudaStream_t src[5] = {m->side, m->g1, m->xs, m->fs, m->ps};
-  for (int k = 0; k < 5; ++k) {
+  const cudaStream_t src[6] = {m->side, m->g1, m->xs, m->fs, m->ps, m->ss};
+  for (int k = 0; k < 6; ++k) {
     CUDA_TRY(cudaEventRecord(m->ev_j[k], src[k]));
     NP_TRY(join(m, st, m->ev_j[k]));
   }
@@ -771,6 +781,8 @@ np_status sync_model(np_model* m) {
   CUDA_TRY(cudaStreamSynchronize(m->xs));
   CUDA_TRY(cudaStreamSynchronize(m->fs));
   if (m->gs) CUDA_TRY(cudaStreamSynchronize(m->gs));
+  if (m->ps) CUDA_TRY(cudaStreamSynchronize(m->ps));
+  if (m->ss) CUDA_TRY(cudaStreamSynchronize(m->ss));
   CUDA_TRY(cudaStreamSynchronize(m->main));
   return NP_OK;
 }
@@ -993,6 +1005,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   // withholds one reader arrival for layer l in the per-token pipeline, so
   // that token ends with NP_ERR_TIMEOUT after the kernel's bounded waits.
   m->withhold_layer = env_int("NP_TEST_WITHHOLD_ARRIVAL", -1);
+  m->set_stream = env_int("NP_TUNE_SET_STREAM", 1) != 0;
   m->pdl_mask = env_int("NP_TUNE_PDL", 5);
   m->gather_grid = env_int("NP_TUNE_GATHER_CTAS", 32);
   m->scatter_grid = env_int("NP_TUNE_SCATTER_CTAS", 4 * m->sms);
@@ -1080,6 +1093,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if ((st = dev_alloc(m, &m->keys, (size_t)m->B * (m->NH > 0 ? m->NH : 1))) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->ids, (size_t)m->B * (m->NH > 0 ? m->NH : 1))) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->fire, (size_t)m->W)) != NP_OK) return fail(st);
+  if ((st = dev_alloc(m, &m->fire2, (size_t)m->W)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->logits, F)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->arrive, 2 * (size_t)m->L)) != NP_OK) return fail(st);
   if ((st = dev_alloc(m, &m->gdone, (size_t)m->L)) != NP_OK) return fail(st);
@@ -1120,7 +1134,7 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
   e = cudaEventCreateWithFlags(&m->ev_side_done, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
-  for (int k = 0; k < 5; ++k) {
+  for (int k = 0; k < 6; ++k) {
     e = cudaEventCreateWithFlags(&m->ev_j[k], cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
   }
@@ -1146,6 +1160,11 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->ps, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_pin, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_psrc, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->ss, cudaStreamNonBlocking);
+    for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+      e = cudaEventCreateWithFlags(&m->ev_pdone[b], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_sdone[b], cudaEventDisableTiming);
+    }
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_gin, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_gout, cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(cuda_fail(e, "cudaStreamCreate"));
@@ -1169,6 +1188,11 @@ np_status np_free_model(np_model* m) {
   if (m->fs) cudaStreamDestroy(m->fs);
   if (m->gs) cudaStreamDestroy(m->gs);
   if (m->ps) cudaStreamDestroy(m->ps);
+  if (m->ss) cudaStreamDestroy(m->ss);
+  for (int b = 0; b < 2; ++b) {
+    if (m->ev_pdone[b]) cudaEventDestroy(m->ev_pdone[b]);
+    if (m->ev_sdone[b]) cudaEventDestroy(m->ev_sdone[b]);
+  }
   if (m->ev_pin) cudaEventDestroy(m->ev_pin);
   if (m->ev_psrc) cudaEventDestroy(m->ev_psrc);
   if (m->ev_gin) cudaEventDestroy(m->ev_gin);
@@ -1505,6 +1529,7 @@ np_status enqueue_token(np_model* m, float* h_dev) {
     const bool split = !shared && k > 0;
     cudaStream_t main_st = m->main;
     bool pred_pending = false;  // predictions of the previous source layer on ps
+    bool fire_used[2] = {false, false};  // firing-mask buffers read by a set kernel this token
     int next = m->dn;           // next sparse layer to predict
     for (int l = 0; l < m->L; ++l) {
       if (split && pred_pending) {
@@ -1519,14 +1544,37 @@ np_status enqueue_token(np_model* m, float* h_dev) {
       for (; !shared && next < m->L && next <= upto; ++next) {
         const int s = next - m->dn;
         const int src = next - k > 0 ? next - k : 0;
-        if (split) m->main = m->ps;
-        np_status rs = enqueue_predict(m, next, base_of(src), true, src == 0 ? nullptr : chain_y(m, src - 1));
-        if (rs == NP_OK) rs = enqueue_set(m, s, 1, nullptr, m->fire);
-        m->main = main_st;
-        NP_TRY(rs);
-        if (split) {
-          CUDA_TRY(cudaEventRecord(m->ev_psrc, m->ps));
+        np_status rs = NP_OK;
+        if (split && m->set_stream) {
+          // ps: the predictor writes firing-mask buffer b, once the set
+          // kernel two layers back has read it; ss: the set kernel reads it
+          const int b = s & 1;
+          uint32_t* fire = b ? m->fire2 : m->fire;
+          if (fire_used[b]) NP_TRY(join(m, m->ps, m->ev_sdone[b]));
+          m->main = m->ps;
+          rs = enqueue_predict(m, next, base_of(src), true, src == 0 ? nullptr : chain_y(m, src - 1), fire);
+          m->main = main_st;
+          NP_TRY(rs);
+          CUDA_TRY(cudaEventRecord(m->ev_psrc, m->ps));  // the source layer's input has been read
           pred_pending = true;
+          CUDA_TRY(cudaEventRecord(m->ev_pdone[b], m->ps));
+          NP_TRY(join(m, m->ss, m->ev_pdone[b]));
+          m->main = m->ss;
+          rs = enqueue_set(m, s, 1, nullptr, fire);  // records ev_set on ss for the reads below
+          m->main = main_st;
+          NP_TRY(rs);
+          CUDA_TRY(cudaEventRecord(m->ev_sdone[b], m->ss));
+          fire_used[b] = true;
+        } else {
+          if (split) m->main = m->ps;
+          rs = enqueue_predict(m, next, base_of(src), true, src == 0 ? nullptr : chain_y(m, src - 1));
+          if (rs == NP_OK) rs = enqueue_set(m, s, 1, nullptr, m->fire);
+          m->main = main_st;
+          NP_TRY(rs);
+          if (split) {
+            CUDA_TRY(cudaEventRecord(m->ev_psrc, m->ps));
+            pred_pending = true;
+          }
         }
         m->pending_bits |= 1ull << s;
         size_t n_moved = 0;

@@ -145,7 +145,7 @@ OPT67B = Config(
     name="opt-6.7b-window", n_layers=32, n_dense=0, d_model=4096, d_ff=16384,
     k_max=4096, n_centroids=0, dtype="f16", pred_hidden=1024,
     pred_kind="perlayer_sigmoid", has_gate=False, residency="window", window=5,
-    planted=False, n_warm=0, n_decode=256, seed=1003)
+    planted=False, n_warm=128, n_decode=256, seed=1003)
 
 BATCHED7B = Config(
     name="llama2-7b-batch8", n_layers=32, n_dense=1, d_model=4096, d_ff=11008,
