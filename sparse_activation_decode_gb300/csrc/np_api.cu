@@ -1047,6 +1047,10 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     const int s2 = pick_stages(m->rps2 * (size_t)m->H * m->esz, rowdot_smem_bytes(m->H, m->esz, m->rps2, 0), side);
     m->ns1_side = s1 >= 2 ? std::min(s1, m->ns1) : m->ns1;
     m->ns2_side = s2 >= 2 ? std::min(s2, m->ns2) : m->ns2;
+    if (env_int("NP_TUNE_PRED_SIDE_FIT", 1) == 0) {  // full rings on the lookahead stream too
+      m->ns1_side = m->ns1;
+      m->ns2_side = m->ns2;
+    }
     // NP_TUNE_PRED_STAGES caps every predictor ring (for sweeps)
     const int cap = env_int("NP_TUNE_PRED_STAGES", 0);
     if (cap >= 2) {
