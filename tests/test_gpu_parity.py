@@ -400,6 +400,35 @@ def test_graph_programmatic_ffn_edges(cfg, tokens, kw, monkeypatch, capfd):
     assert summ["max_h_rel"] < FFN_TOL
 
 
+@pytest.mark.parametrize("residency", ["window", "frequency"])
+@pytest.mark.parametrize("graph", ["1", "0"], ids=["replay", "eager"])
+def test_set_stream_matches_single_stream(residency, graph, monkeypatch):
+    # with a lookahead the set kernels run on a stream of their own, with two
+    # firing-mask buffers alternating by layer; that changes only the
+    # schedule, so the slot state must equal the single-stream run bit for bit
+    # and h must agree up to the FFN's split-K addition order
+    monkeypatch.setenv("NP_TUNE_GRAPH", graph)
+    cfg = SMALL_OPT.replace(lookahead=2, residency=residency)
+    wl = make_workload(cfg)
+    outs = []
+    for ss in ("1", "0"):
+        monkeypatch.setenv("NP_TUNE_SET_STREAM", ss)
+        dec = build_decoder(wl, h2d_mode="fused")
+        hs, states = [], []
+        for t in range(8):
+            h = wl.x[t].cuda().clone()
+            dec.decode_token(h)
+            hs.append(h.cpu())
+            states.append([dec.get_state(cfg.n_dense + s) for s in range(cfg.n_sparse)])
+        dec.check_error()
+        outs.append((hs, states))
+        dec.close()
+    (h1, s1), (h0, s0) = outs
+    assert s1 == s0
+    for a, b in zip(h1, h0):
+        assert oracle.rel_l2(a.numpy().ravel(), b.numpy().ravel()) < 1e-5
+
+
 def test_max_sizes():
     # the largest shapes the ABI accepts: d_model 8192 (fp16 rows of 16 KiB,
     # four chunks per FFN thread), d_ff 16384 (512 mask words, one per set
