@@ -63,3 +63,16 @@ def test_store_holds_bundled_records():
     assert wl.store[0, 5].numel() * wl.store.element_size() == cfg.record_bytes
     opt = make_workload(SMALL_OPT)
     assert opt.store.shape[2] == 2 and opt.pred_b2 is not None       # up | down^T, per-layer predictor
+
+
+def test_full_size_workloads_start_from_a_prompt_warm_fill():
+    # every full-size shape decodes a 128-token prompt (its first token is
+    # the cold start) before the 256 generated tokens; the benchmark times
+    # only generated tokens, after the transient that follows a cold start
+    from workloads import CONFIGS
+    full = [c for c in CONFIGS.values() if c.d_model >= 4096]
+    assert {c.name for c in full} >= {"llama2-7b-relu", "llama2-13b-relu", "opt-6.7b-window",
+                                      "llama2-7b-batch8"}
+    for c in full:
+        assert c.n_warm == 128, c.name
+        assert c.n_decode == 256, c.name
