@@ -1115,9 +1115,23 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     if (want < 0) want = 0;
     if (max_st < 0) max_st = 0;
     const int ffn_mode = m->d.has_gate ? kMmaFfnGated : kMmaFfnUp;
-    if ((e = mma_plan(ffn_mode, dt == NP_BF16, m->D, optin, m->sms, want, max_st, &m->plan_ffn)) != cudaSuccess ||
-        (e = mma_plan(kMmaHidden, dt == NP_BF16, m->D, optin, m->sms, want, max_st, &m->plan_hid)) != cudaSuccess ||
-        (e = mma_plan(kMmaHeads, dt == NP_BF16, m->H, optin, m->sms, want, max_st, &m->plan_heads)) != cudaSuccess)
+    // At most two CTAs of these kernels on one SM: each allocates 256 of the
+    // SM's 512 tensor-memory columns, and a third would wait for columns
+    // inside the kernel.  A stage cap that would leave three CTAs' shared
+    // memory on one SM is raised until it does not.
+    int smem_sm = 0;
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    auto plan2 = [&](int mode, int Kdim, MmaPlan* p) -> cudaError_t {
+      for (int st = max_st;; ++st) {
+        const cudaError_t pe = mma_plan(mode, dt == NP_BF16, Kdim, optin, m->sms, want, st, p);
+        if (pe != cudaSuccess) return pe;
+        if (3 * (p->smem + 1024) > (size_t)smem_sm) return cudaSuccess;
+        if (st == 0 || p->n_stages < st) return cudaErrorInvalidConfiguration;  // no deeper ring fits
+      }
+    };
+    if ((e = plan2(ffn_mode, m->D, &m->plan_ffn)) != cudaSuccess ||
+        (e = plan2(kMmaHidden, m->D, &m->plan_hid)) != cudaSuccess ||
+        (e = plan2(kMmaHeads, m->H, &m->plan_heads)) != cudaSuccess)
       return fail(cuda_fail(e, "mma_plan"));
     if (m->S > 0 && (e = make_row_maps(&m->map_bufs, m->bufs, dt, (uint64_t)m->S * m->nproj * K, m->D)) != cudaSuccess)
       return fail(cuda_fail(e, "tensor map of the resident rows"));
