@@ -31,12 +31,13 @@ X_REL_TC = 1e-5
 
 def rowdot_depth(length: int, elem_bytes: int, bias: bool = False) -> int:
     """Rounded additions on any product's path in the batch-1 predictor
-    kernel: a thread's chunks of 16 bytes (E elements each) by fused
-    multiply-adds, a 5-level warp tree, 8 warp partials added in order, and
-    the bias of the per-layer predictor."""
+    kernel: a thread's chunks of 16 bytes (E elements each) go into two
+    interleaved fp32 sums by fused multiply-adds (even and odd elements, E/2
+    per chunk each), which are then added; a 5-level warp tree; 8 warp
+    partials added in order; and the bias of the per-layer predictor."""
     e = 16 // elem_bytes
     chunks = -(-(length // e) // 256)
-    return e * chunks + 5 + 8 + (1 if bias else 0)
+    return (e // 2) * chunks + 1 + 5 + 8 + (1 if bias else 0)
 
 
 def predictor_bound_args(cfg) -> dict:
