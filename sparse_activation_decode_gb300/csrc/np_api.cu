@@ -19,6 +19,7 @@
 // value it overwrites in the delta lists.  If the incoming rows cannot be
 // read, a rollback kernel restores the previous state from those lists and
 // the rows already overwritten are copied back from the store.
+#include <algorithm>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -363,8 +364,6 @@ np_status enqueue_ffn(np_model* m, cudaStream_t st, int kind, const unsigned cha
 np_status enqueue_tc_ffn(np_model* m, cudaStream_t st, int l, const float* hb, const float* yprev, float* hb_out,
                          float* y_acc, float* y_zero);
 
-// FFN of layer l (dense or sparse) for every sequence, on the kernel that
-// fits the batch: x = rmsnorm(hb + yprev), y added into y_acc.
 // During the token capture, remember the kernel node just added to `st`.
 void note_ffn_node(np_model* m, cudaStream_t st) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -389,6 +388,8 @@ np_status enqueue_layer_ffn(np_model* m, cudaStream_t st, int l, const float* hb
   return NP_OK;
 }
 
+// FFN of layer l (dense or sparse) for every sequence, on the kernel that
+// fits the batch: x = rmsnorm(hb + yprev), y added into y_acc.
 np_status enqueue_layer_ffn_kernel(np_model* m, cudaStream_t st, int l, const float* hb, const float* yprev,
                                    float* hb_out, float* y_acc, float* y_zero) {
   if (m->tc) return enqueue_tc_ffn(m, st, l, hb, yprev, hb_out, y_acc, y_zero);
@@ -1012,7 +1013,8 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
   if (m->gather_grid < 1) m->gather_grid = 32;
   if (m->scatter_grid < 1) m->scatter_grid = 4 * m->sms;
   m->pred_grid = 2 * m->sms;
-  if (env_int("NP_TUNE_PRED_CTAS", 0) > 0) m->pred_grid = env_int("NP_TUNE_PRED_CTAS", 0);
+  const int pred_ctas = env_int("NP_TUNE_PRED_CTAS", 0);
+  if (pred_ctas > 0) m->pred_grid = pred_ctas;
   if (env_int("NP_TUNE_VERBOSE", 0) == 1)
     std::fprintf(stderr, "np: ffn grid %d, ring %d slots; gather %d scatter %d CTAs\n", m->ffn_grid, m->ffn_stages,
                  m->gather_grid, m->scatter_grid);
@@ -1036,8 +1038,9 @@ np_status np_init_model(const np_model_desc* desc, np_model** out) {
     // their rings are cut to what fits beside it; otherwise a second
     // predictor CTA finds no room on SMs that hold an FFN CTA and the
     // predictor runs in two waves.  Measured on the OPT window workload
-    // (lookahead 2): 666-686 tok/s with the full rings, 730-754 with rings
-    // that fit; alone, the full rings stream faster (0.59 vs 0.47 of HBM).
+    // (lookahead 2, from its warm fill): 935 tok/s with the full rings,
+    // 1030-1049 with rings that fit; alone, the full rings stream faster
+    // (0.59 vs 0.47 of HBM).
     int smem_sm = 0;
     cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
     const size_t ffn_cta = ffn_smem_bytes(m->D, m->esz, m->nproj, m->ffn_stages) + 1024;
