@@ -638,3 +638,38 @@ def test_lookahead_source_is_an_earlier_layer():
                 elif m == src - 1:
                     assert not same, (k, m, l)
     assert [oracle.predictor_source_layer(l, 2) for l in range(5)] == [0, 0, 0, 1, 2]
+
+
+def test_assign_slots_hand_worked():
+    # NeuroPrefetcher full text, delta runtime: outgoing neurons give up their
+    # slots and the incoming ones take free slots.  Reading: free slots in
+    # ascending order go to incoming IDs in ascending order.  K = 4 slots,
+    # neurons 2, 5, 7 resident in slots 0, 1, 2; slot 3 free.  Neuron 5 goes,
+    # neurons 1 and 8 come: the free slots are then 1 (just released) and 3,
+    # so 1 -> slot 1 and 8 -> slot 3.
+    slotmap = np.full(10, -1, dtype=np.int64)
+    inv = np.full(4, -1, dtype=np.int64)
+    for n, s in ((2, 0), (5, 1), (7, 2)):
+        slotmap[n], inv[s] = s, n
+    pairs = oracle.assign_slots(slotmap, inv, d_in=[1, 8], d_out=[5], k_max=4)
+    assert pairs == [(1, 1), (8, 3)]
+    assert slotmap.tolist() == [-1, 1, 0, -1, -1, -1, -1, 2, 3, -1]
+    assert inv.tolist() == [2, 1, 7, 8]
+
+
+def test_window_resident_hand_worked():
+    # LLM in a flash 3.1 "Windowing": the rows of neurons active in the last
+    # `window` tokens stay.  Reading for the cap: the oldest last use goes
+    # first, equal ages by ascending ID, and a neuron active now never goes.
+    # t = 10, window = 3: ages are 10 - last_seen; neuron 4 (age 3) is out of
+    # the window, neurons 1 and 5 are active now.
+    last_seen = {1: 10, 2: 9, 3: 8, 4: 7, 5: 10, 6: 9}
+    prev, active = [2, 3, 4, 6], [1, 5]
+    # no cap binding: every neuron inside the window stays
+    assert oracle.window_resident(prev, active, last_seen, 10, 3, 8) == [1, 2, 3, 5, 6]
+    # K = 4: one must go, the oldest (3, last seen at 8)
+    assert oracle.window_resident(prev, active, last_seen, 10, 3, 4) == [1, 2, 5, 6]
+    # K = 3: then between 2 and 6 (both last seen at 9) the lower ID goes
+    assert oracle.window_resident(prev, active, last_seen, 10, 3, 3) == [1, 5, 6]
+    # K = 2: only the active neurons are left, however old the rest
+    assert oracle.window_resident(prev, active, last_seen, 10, 3, 2) == [1, 5]
